@@ -1,0 +1,92 @@
+"""Seeded synthetic inputs for the decode GEMV.
+
+This module draws numbers and lays them out; it holds none of the GEMV's
+arithmetic. Tests, the benchmark and the oracle checks all take their inputs
+from here, so the CUDA path and the CPU oracle see the same bits.
+
+Recipe (the shapes and value distributions of the decode projections of a
+Llama-3.1-8B-shaped model; random init, no trained weights):
+  - weights  W ~ N(0, 0.02^2) drawn in FP32, rounded to BF16 (round to nearest
+    even), row-major [N, ldw] with ldw = K rounded up to a multiple of 8 and
+    the padding columns k in [K, ldw) filled with a BF16 NaN (0x7FC0), so that
+    any use of padding, even a multiply by zero, shows up as a NaN;
+  - activations x ~ N(0, 1) drawn in FP32, rounded to BF16, [B, K] row-major
+    with row stride K;
+  - every tensor draws from its own generator, seeded seed * 1_000_003 + index,
+    where index numbers the tensors of one workload in a fixed order.
+Device-side draws (``device="cuda"``) and host-side draws give different bits
+for the same seed; parity always copies the exact device bits to the host.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+BF16_NAN = 0x7FC0
+
+
+def padded_ldw(K: int) -> int:
+    """K rounded up to a multiple of 8 BF16 elements (16 bytes)."""
+    return (int(K) + 7) // 8 * 8
+
+
+def generator(seed: int, index: int, device="cpu") -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1_000_003 + int(index))
+    return g
+
+
+def _fill_padding(W: torch.Tensor, K: int, pad: int | None) -> None:
+    if pad is not None and W.shape[1] > K:
+        W.view(torch.int16)[:, K:] = np.int16(np.uint16(pad).view(np.int16))
+
+
+def weight(N: int, K: int, ldw: int | None = None, *, seed: int = 0, index: int = 0,
+           std: float = 0.02, device="cpu", pad: int | None = BF16_NAN) -> torch.Tensor:
+    """BF16 [N, ldw] with W[:, :K] ~ N(0, std^2) and NaN padding."""
+    ldw = padded_ldw(K) if ldw is None else int(ldw)
+    g = generator(seed, index, device)
+    W = torch.empty((N, ldw), dtype=torch.bfloat16, device=device)
+    rows = max(1, (1 << 26) // max(K, 1))  # bounded FP32 staging
+    for r0 in range(0, N, rows):
+        r1 = min(N, r0 + rows)
+        part = torch.randn((r1 - r0, K), generator=g, dtype=torch.float32, device=device)
+        part.mul_(std)
+        W[r0:r1, :K] = part.to(torch.bfloat16)
+    _fill_padding(W, K, pad)
+    return W
+
+
+def activations(B: int, K: int, *, seed: int = 0, index: int = 1, device="cpu") -> torch.Tensor:
+    """BF16 [B, K] with entries N(0, 1), row stride K."""
+    g = generator(seed, index, device)
+    return torch.randn((B, K), generator=g, dtype=torch.float32, device=device).to(torch.bfloat16)
+
+
+def int_weight(N: int, K: int, ldw: int | None = None, *, lo: int = -3, hi: int = 3,
+               seed: int = 0, index: int = 0, device="cpu",
+               pad: int | None = BF16_NAN) -> torch.Tensor:
+    """BF16 [N, ldw] of small integers in [lo, hi] (exact in BF16)."""
+    ldw = padded_ldw(K) if ldw is None else int(ldw)
+    g = generator(seed, index, device)
+    W = torch.empty((N, ldw), dtype=torch.bfloat16, device=device)
+    W[:, :K] = torch.randint(lo, hi + 1, (N, K), generator=g, device=device).to(torch.bfloat16)
+    _fill_padding(W, K, pad)
+    return W
+
+
+def int_activations(B: int, K: int, *, lo: int = -2, hi: int = 2, seed: int = 0,
+                    index: int = 1, device="cpu") -> torch.Tensor:
+    g = generator(seed, index, device)
+    return torch.randint(lo, hi + 1, (B, K), generator=g, device=device).to(torch.bfloat16)
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """The BF16 bit patterns of a tensor as a host uint16 array (a copy)."""
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def from_bits(a: np.ndarray, device="cpu") -> torch.Tensor:
+    """A BF16 tensor holding the given uint16 bit patterns."""
+    a = np.ascontiguousarray(a, dtype=np.uint16)
+    return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16).to(device)

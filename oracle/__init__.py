@@ -1,0 +1,2 @@
+"""CPU oracle for the decode GEMV (test infrastructure only; see oracle.py)."""
+from .oracle import RTOL, accept, build, default_threads, gemv, gemv_one, load  # noqa: F401

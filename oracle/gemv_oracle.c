@@ -1,0 +1,97 @@
+/*
+ * Plain CPU oracle for the decode GEMV  y[b][n] = sum_k W[n][k] * x[b][k].
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may link, load or call
+ * this file: only the tests, the package's smoke check and the benchmark's CPU
+ * baseline leg use it. It shares no code, header or constant with the CUDA
+ * library.
+ *
+ * What it follows:
+ *   - "Decode GEMV at half of HBM bandwidth" (inferenceinterviews.com), the
+ *     split-K listing in "A strong answer": each output row is the dot product of
+ *     one weight row (row-major, row stride in elements) with the activation
+ *     vector, the BF16 inputs widened before the multiply-add, and columns at or
+ *     beyond K masked out. Split-K and vector loads only reorder the additions,
+ *     so the oracle is that definition with no reordering at all: k ascending.
+ *   - The same page, "What interviewers probe next": the order of additions is
+ *     what the reproducibility question turns on, so the oracle fixes one order.
+ *   - Precision: the page accumulates in FP32; the oracle accumulates in FP64
+ *     so that its own rounding is far below any FP32 result it checks.
+ *
+ * Layouts (all row-major):
+ *   W  : N rows of ldw BF16 values; only columns k < K are read.
+ *   x  : B rows of K BF16 values (row stride K).
+ *   y  : B rows of N doubles (row stride N).
+ *   s  : same shape as y; s[b][n] = sum_k |W[n][k] * x[b][k]|, the scale the
+ *        acceptance tolerance is measured against.
+ *
+ * BF16 -> double: a BF16 value is the high half of an IEEE binary32 pattern,
+ * so shifting its 16 bits up by 16 gives that binary32 exactly; widening to
+ * double is exact as well.
+ */
+#include <stdint.h>
+#include <string.h>
+
+static double bf16_to_double(uint16_t h)
+{
+    uint32_t bits = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/*
+ * Rows [n0, n1) of every batch row. Returns 0, or -1 on a bad argument.
+ * y and s hold B*N doubles each; only the columns n in [n0, n1) are written.
+ */
+int oracle_gemv_f64(const uint16_t *W, const uint16_t *x,
+                    int64_t N, int64_t K, int64_t B, int64_t ldw,
+                    int64_t n0, int64_t n1, double *y, double *s)
+{
+    if (!W || !x || !y || !s) return -1;
+    if (N < 1 || K < 1 || B < 1 || ldw < K) return -1;
+    if (n0 < 0 || n1 > N || n0 > n1) return -1;
+
+    for (int64_t b = 0; b < B; ++b) {
+        const uint16_t *xb = x + b * K;
+        for (int64_t n = n0; n < n1; ++n) {
+            const uint16_t *wn = W + n * ldw;
+            double acc = 0.0;
+            double mag = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double term = bf16_to_double(wn[k]) * bf16_to_double(xb[k]);
+                acc += term;
+                mag += term < 0.0 ? -term : term;
+            }
+            y[b * N + n] = acc;
+            s[b * N + n] = mag;
+        }
+    }
+    return 0;
+}
+
+/*
+ * One output element (b, n), for checking sampled outputs of very large
+ * problems without computing every row. Returns 0, or -1 on a bad argument.
+ */
+int oracle_gemv_f64_one(const uint16_t *W, const uint16_t *x,
+                        int64_t N, int64_t K, int64_t B, int64_t ldw,
+                        int64_t b, int64_t n, double *y_out, double *s_out)
+{
+    if (!W || !x || !y_out || !s_out) return -1;
+    if (N < 1 || K < 1 || B < 1 || ldw < K) return -1;
+    if (b < 0 || b >= B || n < 0 || n >= N) return -1;
+
+    const uint16_t *xb = x + b * K;
+    const uint16_t *wn = W + n * ldw;
+    double acc = 0.0;
+    double mag = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        double term = bf16_to_double(wn[k]) * bf16_to_double(xb[k]);
+        acc += term;
+        mag += term < 0.0 ? -term : term;
+    }
+    *y_out = acc;
+    *s_out = mag;
+    return 0;
+}

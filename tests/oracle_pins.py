@@ -1,0 +1,196 @@
+"""Pins for the CPU oracle: checks against facts fixed by mathematics, not by the
+oracle itself. Each function takes an oracle handle (``oracle.OracleLib``) and
+raises AssertionError on a violation, so the same pins run against the real
+oracle and against deliberately broken copies of it (see test_oracle_pins.py).
+
+What pins what:
+  exact_rational      every output and scale on tiny inputs, against an exact
+                      rational sum (fractions.Fraction) of values decoded by
+                      torch, an independent BF16 decoder
+  integer_matmul      all outputs on integer data, against numpy int64 matmul
+  ones_row_sums       x = ones gives the row sums of W
+  one_hot_column      one-hot x at column j selects column j, exactly
+  identity_padded     W = [I | 0] returns x itself
+  scaling_exact       y(2^e x) = 2^e y(x) bitwise
+  linearity           y(x1 + x2) = y(x1) + y(x2) within FP64 rounding
+  row_permutation     permuting rows of W permutes y, bitwise
+  batch_rows          row b of a batch equals a single-row call on x[b]
+  padding_unread      NaN in the ldw padding never reaches y
+  float64_matmul      random BF16 data against numpy float64 matmul
+"""
+from __future__ import annotations
+
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+from memory_bound_decode_gb300 import inputs
+
+EPS64 = 2.0 ** -53
+
+
+def _decode(bits: np.ndarray) -> np.ndarray:
+    """BF16 bits -> float64 via torch's own conversion (independent of the oracle)."""
+    return inputs.from_bits(bits).to(torch.float64).numpy()
+
+
+def _rand_case(N, K, B, ldw, seed):
+    W = inputs.bits(inputs.weight(N, K, ldw, seed=seed, index=0, std=1.0))
+    x = inputs.bits(inputs.activations(B, K, seed=seed, index=1))
+    return W, x
+
+
+def exact_rational(lib):
+    cases = [(7, 129, 1, 136), (3, 17, 2, 24), (1, 8, 1, 8), (2, 1, 3, 8),
+             (5, 33, 16, 40), (4, 9, 5, 16)]
+    for i, (N, K, B, ldw) in enumerate(cases):
+        W, x = _rand_case(N, K, B, ldw, seed=100 + i)
+        y, s = lib.gemv(W, x)
+        Wd = _decode(W[:, :K])
+        xd = _decode(x)
+        for b in range(B):
+            for n in range(N):
+                terms = [Fraction(float(Wd[n, k])) * Fraction(float(xd[b, k])) for k in range(K)]
+                exact = sum(terms, Fraction(0))
+                mag = sum((abs(t) for t in terms), Fraction(0))
+                bound = 4 * K * EPS64 * float(mag)
+                assert abs(y[b, n] - float(exact)) <= bound, (N, K, B, b, n)
+                assert abs(s[b, n] - float(mag)) <= bound, (N, K, B, b, n)
+
+
+def integer_matmul(lib):
+    for (N, K, B, ldw) in [(7, 129, 1, 136), (33, 1000, 3, 1000), (16, 4103, 2, 4104)]:
+        W = inputs.bits(inputs.int_weight(N, K, ldw, seed=7))
+        x = inputs.bits(inputs.int_activations(B, K, seed=7))
+        Wi = _decode(W[:, :K]).astype(np.int64)
+        xi = _decode(x).astype(np.int64)
+        y, s = lib.gemv(W, x)
+        assert np.array_equal(y, (xi @ Wi.T).astype(np.float64))
+        assert np.array_equal(s, (np.abs(xi) @ np.abs(Wi).T).astype(np.float64))
+
+
+def ones_row_sums(lib):
+    N, K, ldw = 9, 300, 304
+    W = inputs.bits(inputs.int_weight(N, K, ldw, lo=-100, hi=100, seed=3))
+    ones = np.full((1, K), 0x3F80, dtype=np.uint16)  # BF16 1.0
+    y, s = lib.gemv(W, ones)
+    Wd = _decode(W[:, :K])
+    assert np.array_equal(y[0], Wd.sum(axis=1))
+    assert np.array_equal(s[0], np.abs(Wd).sum(axis=1))
+
+
+def one_hot_column(lib):
+    N, K, ldw = 11, 77, 80
+    W, _ = _rand_case(N, K, 1, ldw, seed=5)
+    Wd = _decode(W[:, :K])
+    for j in (0, 7, 8, K - 1):
+        x = np.zeros((1, K), dtype=np.uint16)
+        x[0, j] = 0x3F80
+        y, _ = lib.gemv(W, x)
+        assert np.array_equal(y[0], Wd[:, j]), j
+
+
+def identity_padded(lib):
+    for N, K in [(5, 9), (12, 8), (8, 8)]:
+        ldw = inputs.padded_ldw(K)
+        W = np.zeros((N, ldw), dtype=np.uint16)
+        for n in range(min(N, K)):
+            W[n, n] = 0x3F80
+        W[:, K:] = inputs.BF16_NAN
+        x = inputs.bits(inputs.activations(1, K, seed=9))
+        y, _ = lib.gemv(W, x)
+        xd = _decode(x)[0]
+        want = np.zeros(N)
+        want[:min(N, K)] = xd[:min(N, K)]
+        assert np.array_equal(y[0], want), (N, K)
+
+
+def scaling_exact(lib):
+    N, K, ldw = 6, 129, 136
+    W, x = _rand_case(N, K, 1, ldw, seed=11)
+    y1, _ = lib.gemv(W, x)
+    x4 = inputs.bits(inputs.from_bits(x).float().mul(4.0).to(torch.bfloat16))
+    y4, _ = lib.gemv(W, x4)
+    assert np.array_equal(y4, 4.0 * y1)
+
+
+def linearity(lib):
+    N, K, ldw = 6, 200, 200
+    W, _ = _rand_case(N, K, 1, ldw, seed=12)
+    xa = inputs.int_activations(1, K, lo=-8, hi=8, seed=1)
+    xb = inputs.int_activations(1, K, lo=-8, hi=8, seed=2)
+    xs = (xa.float() + xb.float()).to(torch.bfloat16)  # exact: small integers
+    ya, sa = lib.gemv(W, inputs.bits(xa))
+    yb, sb = lib.gemv(W, inputs.bits(xb))
+    ys, _ = lib.gemv(W, inputs.bits(xs))
+    assert np.all(np.abs(ys - (ya + yb)) <= 4 * K * EPS64 * (sa + sb))
+    assert not np.allclose(ya, 0.0)
+
+
+def row_permutation(lib):
+    N, K, ldw = 10, 129, 136
+    W, x = _rand_case(N, K, 2, ldw, seed=13)
+    perm = np.random.default_rng(0).permutation(N)
+    y, s = lib.gemv(W, x)
+    yp, sp = lib.gemv(np.ascontiguousarray(W[perm]), x)
+    assert np.array_equal(yp, y[:, perm])
+    assert np.array_equal(sp, s[:, perm])
+
+
+def batch_rows(lib):
+    N, K, ldw, B = 6, 131, 136, 5
+    W, x = _rand_case(N, K, B, ldw, seed=14)
+    y, _ = lib.gemv(W, x)
+    for b in range(B):
+        yb, _ = lib.gemv(W, x[b:b + 1])
+        assert np.array_equal(yb[0], y[b]), b
+
+
+def padding_unread(lib):
+    N, K, ldw = 4, 13, 24
+    W, x = _rand_case(N, K, 2, ldw, seed=15)
+    W[:, K:] = inputs.BF16_NAN
+    y, s = lib.gemv(W, x)
+    assert np.all(np.isfinite(y)) and np.all(np.isfinite(s))
+    W2 = W.copy()
+    W2[:, K:] = 0x3F80
+    y2, _ = lib.gemv(W2, x)
+    assert np.array_equal(y, y2)
+
+
+def float64_matmul(lib):
+    N, K, B, ldw = 64, 1000, 3, 1000
+    W, x = _rand_case(N, K, B, ldw, seed=16)
+    y, s = lib.gemv(W, x)
+    Wd = _decode(W[:, :K])
+    xd = _decode(x)
+    ref = xd @ Wd.T
+    assert np.all(np.abs(y - ref) <= 4 * K * EPS64 * s)
+    assert np.allclose(s, np.abs(xd) @ np.abs(Wd).T, rtol=1e-12, atol=0)
+
+
+def single_element(lib):
+    N, K, B, ldw = 9, 70, 3, 72
+    W, x = _rand_case(N, K, B, ldw, seed=17)
+    y, s = lib.gemv(W, x)
+    for b, n in [(0, 0), (2, 8), (1, 4)]:
+        yo, so = lib.gemv_one(W, x, b, n)
+        assert yo == y[b, n] and so == s[b, n]
+
+
+ALL_PINS = [exact_rational, integer_matmul, ones_row_sums, one_hot_column,
+            identity_padded, scaling_exact, linearity, row_permutation,
+            batch_rows, padding_unread, float64_matmul, single_element]
+
+
+def failures(lib) -> list[str]:
+    out = []
+    for pin in ALL_PINS:
+        try:
+            pin(lib)
+        except AssertionError as e:
+            out.append(f"{pin.__name__}: {e}")
+        except Exception as e:  # a broken oracle may also crash a pin
+            out.append(f"{pin.__name__}: {type(e).__name__}: {e}")
+    return out

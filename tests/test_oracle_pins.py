@@ -1,0 +1,87 @@
+"""The CPU oracle against its pins, and the pins against planted mistakes.
+
+A pin is only worth something if a plausible mistake in the oracle breaks it.
+``test_planted_mistake_is_caught`` copies the oracle's C source, plants one
+mistake (a dropped term, a wrong sign, a wrong index or stride, a transposed
+output, a wrong BF16 decode, FP32 accumulation), builds the copy on the CPU and
+requires that at least one pin fails on it. The real oracle is never modified.
+"""
+import os
+
+import numpy as np
+import pytest
+
+from oracle import oracle
+from tests import oracle_pins
+
+MUTATIONS = {
+    "drop_last_term": ("for (int64_t k = 0; k < K; ++k) {\n                double term",
+                       "for (int64_t k = 0; k < K - 1; ++k) {\n                double term"),
+    "drop_first_term": ("for (int64_t k = 0; k < K; ++k) {\n                double term",
+                        "for (int64_t k = 1; k < K; ++k) {\n                double term"),
+    "wrong_sign": ("            acc += term;\n                mag",
+                   "            acc -= term;\n                mag"),
+    "row_stride_K": ("const uint16_t *wn = W + n * ldw;\n            double acc",
+                     "const uint16_t *wn = W + n * K;\n            double acc"),
+    "x_stride_ldw": ("const uint16_t *xb = x + b * K;\n        for",
+                     "const uint16_t *xb = x + b * ldw;\n        for"),
+    "signed_scale": ("mag += term < 0.0 ? -term : term;\n            }\n            y[",
+                     "mag += term;\n            }\n            y["),
+    "transposed_y": ("y[b * N + n] = acc;", "y[n * B + b] = acc;"),
+    "bf16_shift": ("((uint32_t)h) << 16", "((uint32_t)h) << 15"),
+    "fp32_accumulate": ("double acc = 0.0;\n            double mag = 0.0;\n            for (int64_t k = 0; k < K; ++k) {\n                double term",
+                        "float acc = 0.0f;\n            double mag = 0.0;\n            for (int64_t k = 0; k < K; ++k) {\n                double term"),
+    "operand_swap_W_for_x": ("bf16_to_double(wn[k]) * bf16_to_double(xb[k]);\n                acc",
+                             "bf16_to_double(wn[k]) * bf16_to_double(wn[k]);\n                acc"),
+}
+
+
+@pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda p: p.__name__)
+def test_oracle_pin(pin, oracle_lib):
+    pin(oracle_lib)
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    src = open(oracle.SOURCE).read()
+    old, new = MUTATIONS[name]
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    mutant_src = tmp_path / f"mutant_{name}.c"
+    mutant_src.write_text(src.replace(old, new))
+    so = oracle.build(str(mutant_src), str(tmp_path / f"libmutant_{name}.so"), force=True)
+    lib = oracle.OracleLib(so)
+    fails = oracle_pins.failures(lib)
+    assert fails, f"planted mistake {name} passed every pin"
+
+
+def test_accept_rule():
+    y_ref = np.array([[1.0, -2.0, 0.0, 3.0]])
+    scale = np.array([[10.0, 10.0, 0.0, 1.0]])
+    y_gpu = np.array([[1.0 + 9e-5, -2.0 - 1.1e-4, -0.0, np.nan]])
+    ok = oracle.accept(y_gpu, y_ref, scale, rtol=1e-5)
+    assert ok.tolist() == [[True, False, True, False]]
+
+
+def test_threads_do_not_change_results(oracle_lib):
+    from memory_bound_decode_gb300 import inputs
+    W = inputs.bits(inputs.weight(257, 513, seed=1))
+    x = inputs.bits(inputs.activations(2, 513, seed=1))
+    y1, s1 = oracle_lib.gemv(W, x, threads=1)
+    y4, s4 = oracle_lib.gemv(W, x, threads=4)
+    assert np.array_equal(y1, y4) and np.array_equal(s1, s4)
+
+
+def test_argument_checks(oracle_lib):
+    W = np.zeros((4, 8), dtype=np.uint16)
+    with pytest.raises(ValueError):
+        oracle_lib.gemv(W, np.zeros((1, 9), dtype=np.uint16))
+    with pytest.raises(TypeError):
+        oracle_lib.gemv(W.astype(np.int32), np.zeros((1, 8), dtype=np.uint16))
+    with pytest.raises(ValueError):
+        oracle_lib.gemv_one(W, np.zeros((1, 8), dtype=np.uint16), 1, 0)
+
+
+def test_source_is_test_infrastructure():
+    head = open(oracle.SOURCE).read(600)
+    assert "TEST INFRASTRUCTURE ONLY" in head
+    assert os.path.basename(oracle.SOURCE) == "gemv_oracle.c"
