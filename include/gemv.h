@@ -1,0 +1,195 @@
+/*
+ * gemv.h — C ABI of libgemv.so, the GB300 (sm_103a) decode GEMV.
+ *
+ * The operation ("Decode GEMV at half of HBM bandwidth", inferenceinterviews.com,
+ * "A strong answer" and its split-K listing): for every batch row b and output
+ * row n,
+ *
+ *     y[b][n] = sum_{k < K} float(W[n][k]) * float(x[b][k])
+ *
+ * with BF16 weights and activations, products and sums in FP32. At batch 1 this
+ * is a byte stream: the time is the weight bytes over the HBM bandwidth the
+ * kernel sustains ("How to approach it"), so the library is built to keep enough
+ * 16-byte loads in flight on every SM ("A strong answer", Little's law) and to
+ * size its grid to whole waves of the GPU's SMs (cause 1 and "The reversal
+ * condition": split K only when the rows alone do not fill the GPU).
+ *
+ * Layouts (all row-major, all device memory owned by the caller):
+ *   W : N rows of ldw BF16 values; only columns k < K are read. The padding
+ *       columns [K, ldw) are never part of a sum (their contents may be NaN).
+ *   x : B rows of K BF16 values, row stride K (row b starts at x + b*K).
+ *   y : B rows of N FP32 values, row stride N. y is overwritten (not
+ *       accumulated): every element is written exactly once per call.
+ *
+ * Preconditions checked before anything is launched (GEMV_ERR_INVALID /
+ * GEMV_ERR_ALIGN on violation):
+ *   1 <= N <= 2^31-1, 1 <= K <= 2^31-1, 1 <= B <= 16, K <= ldw, ldw % 8 == 0;
+ *   W 16-byte aligned; x 2-byte aligned; y 4-byte aligned; no pointer NULL.
+ * Not checked: y must not overlap W or x; W must hold N*ldw elements, x B*K,
+ * y B*N.
+ *
+ * Results are deterministic: the same call on the same inputs returns the same
+ * bits on every run. Partial sums (over lanes, warps and K-splits) are combined
+ * in a fixed order and never with atomics ("What interviewers probe next":
+ * reproducibility needs a fixed reduction order). Any FP32 summation order is
+ * within the accuracy bound |y - exact| <= 1e-5 * sum_k |W[n][k] * x[b][k]|.
+ *
+ * Streams: every call is asynchronous on the given stream (a cudaStream_t passed
+ * as void*; NULL means the legacy default stream) and never synchronizes.
+ * Launch failures return GEMV_ERR_CUDA; gemv_last_cuda_error() then returns the
+ * cudaError_t. Faults inside a kernel surface at the caller's next
+ * synchronization, as for any CUDA kernel. The kernels read W before they wait
+ * for the preceding grid on the stream (programmatic dependent launch), so W
+ * must not be written by a kernel that immediately precedes a call on the same
+ * stream and triggers its dependents early; x and y are touched only after the
+ * wait. Calls are thread-safe; the library keeps only per-device launch
+ * settings, created on first use.
+ */
+#ifndef GEMV_H
+#define GEMV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    GEMV_OK = 0,
+    GEMV_ERR_INVALID = -1,      /* a size, count or pointer is out of range      */
+    GEMV_ERR_ALIGN = -2,        /* W not 16-B aligned, ldw % 8 != 0, x or y misaligned */
+    GEMV_ERR_CUDA = -3,         /* a CUDA runtime call failed (see gemv_last_cuda_error) */
+    GEMV_ERR_NOMEM = -4,        /* host allocation for a plan failed             */
+    GEMV_ERR_CAPTURE = -5,      /* graph capture or instantiation failed         */
+    GEMV_ERR_UNSUPPORTED = -6   /* no sm_103a device, or a plan used before capture */
+};
+
+#define GEMV_MAX_BATCH 16
+#define GEMV_MAX_SEGMENTS 8
+
+/*
+ * y = W·x for one weight matrix ("Decode GEMV at half of HBM bandwidth",
+ * "A strong answer": the split-K GEMV). W is [N, ldw] BF16, x is [B, K] BF16,
+ * y is [B, N] FP32; see the layout rules above. Returns GEMV_OK or an error
+ * code; on an error nothing was launched (validation) or the launch failed.
+ */
+int gemv_bf16(const void *W, const void *x, float *y,
+              int64_t N, int64_t K, int B, int64_t ldw, void *stream);
+
+/*
+ * One weight matrix of a fused launch: y_i = W_i · x, W_i [N_i, ldw_i], y_i
+ * [B, N_i] (row stride N_i).
+ */
+typedef struct {
+    const void *W;
+    float *y;
+    int64_t N;
+    int64_t ldw;
+} gemv_segment;
+
+/*
+ * Several projections that share x, in ONE launch ("Decode GEMV at half of HBM
+ * bandwidth", "A strong answer", cause 3: fuse Q, K and V into one 6,144-row
+ * projection, and gate with up, so that launch gaps do not rival the few
+ * microseconds a small matrix takes to stream). segs holds 1..GEMV_MAX_SEGMENTS
+ * host-side descriptors (read during the call only); each segment obeys the
+ * same rules as gemv_bf16 with the common x, K and B. The sum of N_i must not
+ * exceed 2^31-1. Each y_i is computed exactly as a separate gemv_bf16 on the
+ * concatenated rows would compute it.
+ */
+int gemv_bf16_multi(const gemv_segment *segs, int nsegs, const void *x,
+                    int64_t K, int B, void *stream);
+
+/*
+ * One projection of a decode step. Projections with the same fuse_group > 0,
+ * the same x, K and B, that are adjacent in the list, become one fused launch
+ * (at most GEMV_MAX_SEGMENTS per launch); fuse_group 0 means "alone".
+ */
+typedef struct {
+    const void *W;
+    const void *x;
+    float *y;
+    int64_t N;
+    int64_t K;
+    int64_t ldw;
+    int B;
+    int fuse_group;
+} gemv_proj;
+
+typedef struct gemv_plan gemv_plan;   /* opaque; owned by the library */
+
+/*
+ * Build a decode-step plan over nproj projections, launched in list order
+ * ("GPU performance chains", "Launch gaps in a decode step": many small gaps
+ * between kernels call for CUDA graphs). The projection list is copied; every
+ * pointer in it must stay valid while the plan is used. Validates every
+ * projection as gemv_bf16 would. On success *out owns a plan to be released
+ * with gemv_plan_destroy. Allocates host memory only.
+ */
+int gemv_plan_create(const gemv_proj *projs, int nproj, gemv_plan **out);
+
+/*
+ * Record the plan's launches on `stream` (which must not be the legacy NULL
+ * stream and must not already be capturing) into a CUDA graph and instantiate
+ * it. Nothing executes. Calling it again replaces the previous graph.
+ */
+int gemv_plan_capture(gemv_plan *plan, void *stream);
+
+/*
+ * Run the whole captured step as one graph launch on `stream`. Inputs are read
+ * at the addresses given at create time, so callers update x in place between
+ * launches. Returns GEMV_ERR_UNSUPPORTED if the plan was never captured.
+ */
+int gemv_plan_launch(gemv_plan *plan, void *stream);
+
+/* Number of kernel launches one gemv_plan_launch performs (after fusion). */
+int gemv_plan_num_launches(const gemv_plan *plan);
+
+/* Release a plan and its graph. NULL is ignored. Not while a launch runs. */
+void gemv_plan_destroy(gemv_plan *plan);
+
+/*
+ * How a shape is launched, for tests and the benchmark. Pure host arithmetic;
+ * makes no CUDA call. sm_count is the GPU's SM count (e.g. 152 on a GB300);
+ * ctas_per_sm is how many CTAs of the chosen kernel fit on one SM.
+ */
+typedef struct {
+    int64_t rows_per_cta;    /* output rows one CTA produces                      */
+    int64_t row_tiles;       /* ceil(N / rows_per_cta)                            */
+    int64_t grid;            /* CTAs launched = row_tiles * splits                */
+    int64_t kslice;          /* columns per K-split (all but the last)            */
+    int64_t kchunk;          /* columns of x staged in shared memory at a time    */
+    int32_t warps_per_cta;
+    int32_t warps_per_row;   /* warps of one CTA that share a row along K         */
+    int32_t splits;          /* CTAs along K (one thread-block cluster)           */
+    int32_t rows_per_warp;
+    int32_t unroll;          /* independent 16-byte loads per lane per row before use */
+    int32_t smem_bytes;      /* dynamic shared memory per CTA                     */
+    int32_t variant;         /* kernel instance index                             */
+} gemv_launch_info;
+
+int gemv_query_launch(int64_t N, int64_t K, int B, int sm_count,
+                      gemv_launch_info *out);
+
+/*
+ * Read-only bandwidth probe: streams `bytes` (a multiple of 16, >= 16) from the
+ * 16-byte aligned device buffer `src` with the same 16-byte non-allocating
+ * loads as the GEMV and writes one checksum word per CTA to `sink` (at least
+ * gemv_probe_sink_words() floats). It measures the read-only HBM ceiling the
+ * GEMV is held to ("How to optimize an ML kernel that underutilizes the GPU",
+ * Step 5: compare achieved bandwidth with peak).
+ */
+int gemv_probe_stream_read(const void *src, int64_t bytes, float *sink, void *stream);
+int gemv_probe_sink_words(void);
+
+/* Human-readable name of a status code. Never NULL. */
+const char *gemv_status_string(int status);
+
+/* The cudaError_t behind the calling thread's most recent GEMV_ERR_CUDA (0 if none). */
+int gemv_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMV_H */

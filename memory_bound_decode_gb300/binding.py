@@ -1,0 +1,211 @@
+"""Python binding of libgemv.so: argument marshalling only.
+
+Every function here has the name of the C entry point it calls (include/gemv.h)
+and does nothing but turn tensors into pointers and streams into handles. There
+is no fallback: if the library is not built, the first call raises.
+
+Pointers may be given as integers or as tensors (their ``data_ptr()``);
+``stream`` may be an integer handle, a ``torch.cuda.Stream`` or None (the
+current PyTorch stream).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_lib", "libgemv.so")
+
+GEMV_OK = 0
+GEMV_ERR_INVALID = -1
+GEMV_ERR_ALIGN = -2
+GEMV_ERR_CUDA = -3
+GEMV_ERR_NOMEM = -4
+GEMV_ERR_CAPTURE = -5
+GEMV_ERR_UNSUPPORTED = -6
+GEMV_MAX_BATCH = 16
+GEMV_MAX_SEGMENTS = 8
+
+EXPORTED = [
+    "gemv_bf16", "gemv_bf16_multi", "gemv_plan_create", "gemv_plan_capture",
+    "gemv_plan_launch", "gemv_plan_num_launches", "gemv_plan_destroy",
+    "gemv_query_launch", "gemv_probe_stream_read", "gemv_probe_sink_words",
+    "gemv_status_string", "gemv_last_cuda_error",
+]
+
+i64 = ctypes.c_int64
+vp = ctypes.c_void_p
+
+
+class gemv_segment(ctypes.Structure):
+    _fields_ = [("W", vp), ("y", vp), ("N", i64), ("ldw", i64)]
+
+
+class gemv_proj(ctypes.Structure):
+    _fields_ = [("W", vp), ("x", vp), ("y", vp), ("N", i64), ("K", i64), ("ldw", i64),
+                ("B", ctypes.c_int), ("fuse_group", ctypes.c_int)]
+
+
+class gemv_launch_info(ctypes.Structure):
+    _fields_ = [("rows_per_cta", i64), ("row_tiles", i64), ("grid", i64), ("kslice", i64),
+                ("kchunk", i64), ("warps_per_cta", ctypes.c_int32), ("warps_per_row", ctypes.c_int32),
+                ("splits", ctypes.c_int32), ("rows_per_warp", ctypes.c_int32),
+                ("unroll", ctypes.c_int32), ("smem_bytes", ctypes.c_int32), ("variant", ctypes.c_int32)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class GemvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = gemv_status_string(status)
+        if status == GEMV_ERR_CUDA:
+            msg += f" (cudaError {gemv_last_cuda_error()})"
+        super().__init__(f"{where}: {msg}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libgemv.so is not built ({LIB_PATH}); "
+                                   "run memory_bound_decode_gb300.build_lib.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            L.gemv_bf16.argtypes = [vp, vp, vp, i64, i64, ctypes.c_int, i64, vp]
+            L.gemv_bf16_multi.argtypes = [ctypes.POINTER(gemv_segment), ctypes.c_int, vp, i64,
+                                          ctypes.c_int, vp]
+            L.gemv_plan_create.argtypes = [ctypes.POINTER(gemv_proj), ctypes.c_int,
+                                           ctypes.POINTER(vp)]
+            L.gemv_plan_capture.argtypes = [vp, vp]
+            L.gemv_plan_launch.argtypes = [vp, vp]
+            L.gemv_plan_num_launches.argtypes = [vp]
+            L.gemv_plan_destroy.argtypes = [vp]
+            L.gemv_plan_destroy.restype = None
+            L.gemv_query_launch.argtypes = [i64, i64, ctypes.c_int, ctypes.c_int,
+                                            ctypes.POINTER(gemv_launch_info)]
+            L.gemv_probe_stream_read.argtypes = [vp, i64, vp, vp]
+            L.gemv_probe_sink_words.argtypes = []
+            L.gemv_status_string.argtypes = [ctypes.c_int]
+            L.gemv_status_string.restype = ctypes.c_char_p
+            L.gemv_last_cuda_error.argtypes = []
+            for name in EXPORTED:
+                f = getattr(L, name)
+                if name not in ("gemv_plan_destroy", "gemv_status_string"):
+                    f.restype = ctypes.c_int
+            _lib = L
+        return _lib
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(rc: int, where: str) -> int:
+    if rc != GEMV_OK:
+        raise GemvError(rc, where)
+    return rc
+
+
+def gemv_status_string(status: int) -> str:
+    return lib().gemv_status_string(int(status)).decode()
+
+
+def gemv_last_cuda_error() -> int:
+    return lib().gemv_last_cuda_error()
+
+
+def gemv_bf16(W, x, y, N: int, K: int, B: int, ldw: int, stream=None, check: bool = True) -> int:
+    rc = lib().gemv_bf16(_ptr(W), _ptr(x), _ptr(y), N, K, B, ldw, _stream(stream))
+    return _check(rc, "gemv_bf16") if check else rc
+
+
+def gemv_bf16_multi(segments, x, K: int, B: int, stream=None, check: bool = True) -> int:
+    """``segments``: sequence of (W, y, N, ldw)."""
+    arr = (gemv_segment * max(1, len(segments)))()
+    for i, (W, y, N, ldw) in enumerate(segments):
+        arr[i] = gemv_segment(_ptr(W), _ptr(y), N, ldw)
+    rc = lib().gemv_bf16_multi(arr, len(segments), _ptr(x), K, B, _stream(stream))
+    return _check(rc, "gemv_bf16_multi") if check else rc
+
+
+def gemv_query_launch(N: int, K: int, B: int, sm_count: int) -> dict:
+    info = gemv_launch_info()
+    _check(lib().gemv_query_launch(N, K, B, sm_count, ctypes.byref(info)), "gemv_query_launch")
+    return info.as_dict()
+
+
+def gemv_probe_sink_words() -> int:
+    return lib().gemv_probe_sink_words()
+
+
+def gemv_probe_stream_read(src, nbytes: int, sink, stream=None) -> int:
+    return _check(lib().gemv_probe_stream_read(_ptr(src), nbytes, _ptr(sink), _stream(stream)),
+                  "gemv_probe_stream_read")
+
+
+class Plan:
+    """Owner of a gemv_plan handle (gemv_plan_create / capture / launch / destroy).
+
+    ``projections``: sequence of (W, x, y, N, K, ldw, B, fuse_group). The
+    tensors behind the pointers must outlive the plan; keep them referenced.
+    """
+
+    def __init__(self, projections, keepalive=None):
+        n = len(projections)
+        arr = (gemv_proj * max(1, n))()
+        for i, (W, x, y, N, K, ldw, B, grp) in enumerate(projections):
+            arr[i] = gemv_proj(_ptr(W), _ptr(x), _ptr(y), N, K, ldw, B, grp)
+        handle = vp()
+        _check(lib().gemv_plan_create(arr, n, ctypes.byref(handle)), "gemv_plan_create")
+        self._h = handle
+        self._keepalive = keepalive
+
+    @property
+    def handle(self) -> int:
+        return self._h.value or 0
+
+    def capture(self, stream) -> None:
+        _check(lib().gemv_plan_capture(self._h, _stream(stream)), "gemv_plan_capture")
+
+    def launch(self, stream=None, check: bool = True) -> int:
+        rc = lib().gemv_plan_launch(self._h, _stream(stream))
+        return _check(rc, "gemv_plan_launch") if check else rc
+
+    def num_launches(self) -> int:
+        return lib().gemv_plan_num_launches(self._h)
+
+    def destroy(self) -> None:
+        if self._h is not None and self._h.value:
+            lib().gemv_plan_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def gemv_plan_create(projections, keepalive=None) -> Plan:
+    return Plan(projections, keepalive)

@@ -1,0 +1,337 @@
+// C-ABI front end of libgemv.so: argument checks, per-device set-up, fused
+// launches and the CUDA-graph decode-step plan. Every operation on data runs
+// in the kernels; this file only validates, plans and launches.
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "../../include/gemv.h"
+#include "gemv_internal.h"
+
+using gemv::Launch;
+using gemv::Params;
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = static_cast<int>(e);
+    return GEMV_ERR_CUDA;
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int status = GEMV_OK;
+    int sm_count = 0;
+};
+
+std::mutex g_dev_mutex;
+DeviceState g_dev[kMaxDevices];
+
+// Per-device set-up on first use: check for an sm_103 device, read the SM
+// count and raise the kernels' dynamic shared-memory limit.
+int device_state(int* sm_count) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return GEMV_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceState& st = g_dev[dev];
+    if (!st.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        if (major != 10 || minor != 3) {
+            st.status = GEMV_ERR_UNSUPPORTED;
+        } else if ((e = gemv::prepare_kernels(dev)) != cudaSuccess) {
+            return cuda_fail(e);
+        } else {
+            st.status = GEMV_OK;
+        }
+        st.sm_count = sms;
+        st.ready = true;
+    }
+    *sm_count = st.sm_count;
+    return st.status;
+}
+
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("GEMV_PDL");
+        return !(v && v[0] == '0');
+    }();
+    return on;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_common(const void* x, int64_t K, int B) {
+    if (!x) return GEMV_ERR_INVALID;
+    if (K < 1 || K > 0x7fffffffLL || B < 1 || B > GEMV_MAX_BATCH) return GEMV_ERR_INVALID;
+    if (!aligned(x, 2)) return GEMV_ERR_ALIGN;
+    return GEMV_OK;
+}
+
+int check_matrix(const void* W, const float* y, int64_t N, int64_t K, int64_t ldw) {
+    if (!W || !y) return GEMV_ERR_INVALID;
+    if (N < 1 || N > 0x7fffffffLL || ldw < K) return GEMV_ERR_INVALID;
+    if (ldw % 8 != 0 || !aligned(W, 16) || !aligned(y, 4)) return GEMV_ERR_ALIGN;
+    return GEMV_OK;
+}
+
+// One prepared launch: parameters plus grid shape.
+struct Prepared {
+    Params p;
+    Launch l;
+    int B;
+};
+
+// Validate a group of segments sharing x, K, B and plan one launch over them.
+int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B, int sm_count,
+            Prepared* out) {
+    if (!segs || nsegs < 1 || nsegs > GEMV_MAX_SEGMENTS) return GEMV_ERR_INVALID;
+    int rc = check_common(x, K, B);
+    if (rc != GEMV_OK) return rc;
+    int64_t total = 0;
+    for (int i = 0; i < nsegs; ++i) {
+        if ((rc = check_matrix(segs[i].W, segs[i].y, segs[i].N, K, segs[i].ldw)) != GEMV_OK) return rc;
+        total += segs[i].N;
+        if (total > 0x7fffffffLL) return GEMV_ERR_INVALID;
+    }
+    Launch l;
+    if ((rc = gemv::plan_launch(total, K, B, sm_count, &l)) != GEMV_OK) return rc;
+
+    Params p;
+    std::memset(&p, 0, sizeof p);
+    int64_t tiles = 0;
+    for (int i = 0; i < nsegs; ++i) {
+        p.seg[i].W = static_cast<const uint16_t*>(segs[i].W);
+        p.seg[i].y = segs[i].y;
+        p.seg[i].N = segs[i].N;
+        p.seg[i].ldw = segs[i].ldw;
+        p.seg[i].tile_begin = tiles;
+        tiles += (segs[i].N + l.rows_per_cta - 1) / l.rows_per_cta;
+    }
+    l.row_tiles = tiles;
+    l.grid = tiles * l.splits;
+    if (l.grid > 0x7fffffffLL) return GEMV_ERR_UNSUPPORTED;
+    p.x = static_cast<const uint16_t*>(x);
+    p.K = K;
+    p.kslice = l.kslice;
+    p.kchunk = l.kchunk;
+    p.nseg = nsegs;
+    p.splits = l.splits;
+    p.kw = l.kw;
+    p.xstride = static_cast<int32_t>(l.kchunk);
+    out->p = p;
+    out->l = l;
+    out->B = B;
+    return GEMV_OK;
+}
+
+int run(const Prepared& pr, cudaStream_t s) {
+    cudaError_t e = gemv::launch_gemv(pr.B, pr.p, pr.l, s, pdl_enabled());
+    if (e != cudaSuccess) return cuda_fail(e);
+    return GEMV_OK;
+}
+
+}  // namespace
+
+struct gemv_plan {
+    std::vector<Prepared> launches;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+};
+
+extern "C" {
+
+int gemv_bf16(const void* W, const void* x, float* y, int64_t N, int64_t K, int B, int64_t ldw,
+              void* stream) {
+    gemv_segment seg{W, y, N, ldw};
+    int rc = check_common(x, K, B);
+    if (rc != GEMV_OK) return rc;
+    if ((rc = check_matrix(W, y, N, K, ldw)) != GEMV_OK) return rc;
+    int sm_count = 0;
+    if ((rc = device_state(&sm_count)) != GEMV_OK) return rc;
+    Prepared pr;
+    if ((rc = prepare(&seg, 1, x, K, B, sm_count, &pr)) != GEMV_OK) return rc;
+    return run(pr, static_cast<cudaStream_t>(stream));
+}
+
+int gemv_bf16_multi(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B,
+                    void* stream) {
+    if (!segs || nsegs < 1 || nsegs > GEMV_MAX_SEGMENTS) return GEMV_ERR_INVALID;
+    int rc = check_common(x, K, B);
+    if (rc != GEMV_OK) return rc;
+    for (int i = 0; i < nsegs; ++i)
+        if ((rc = check_matrix(segs[i].W, segs[i].y, segs[i].N, K, segs[i].ldw)) != GEMV_OK) return rc;
+    int sm_count = 0;
+    if ((rc = device_state(&sm_count)) != GEMV_OK) return rc;
+    Prepared pr;
+    if ((rc = prepare(segs, nsegs, x, K, B, sm_count, &pr)) != GEMV_OK) return rc;
+    return run(pr, static_cast<cudaStream_t>(stream));
+}
+
+int gemv_plan_create(const gemv_proj* projs, int nproj, gemv_plan** out) {
+    if (!out) return GEMV_ERR_INVALID;
+    *out = nullptr;
+    if (!projs || nproj < 1) return GEMV_ERR_INVALID;
+    // Check every projection before touching the device.
+    for (int i = 0; i < nproj; ++i) {
+        int rc = check_common(projs[i].x, projs[i].K, projs[i].B);
+        if (rc != GEMV_OK) return rc;
+        if ((rc = check_matrix(projs[i].W, projs[i].y, projs[i].N, projs[i].K, projs[i].ldw)) != GEMV_OK)
+            return rc;
+        if (projs[i].fuse_group < 0) return GEMV_ERR_INVALID;
+    }
+    int sm_count = 0;
+    int rc = device_state(&sm_count);
+    if (rc != GEMV_OK) return rc;
+
+    gemv_plan* plan = new (std::nothrow) gemv_plan;
+    if (!plan) return GEMV_ERR_NOMEM;
+    try {
+        int i = 0;
+        while (i < nproj) {
+            const gemv_proj& a = projs[i];
+            int j = i + 1;
+            if (a.fuse_group > 0) {
+                while (j < nproj && j - i < GEMV_MAX_SEGMENTS && projs[j].fuse_group == a.fuse_group &&
+                       projs[j].x == a.x && projs[j].K == a.K && projs[j].B == a.B)
+                    ++j;
+            }
+            gemv_segment segs[GEMV_MAX_SEGMENTS];
+            for (int q = i; q < j; ++q) segs[q - i] = gemv_segment{projs[q].W, projs[q].y, projs[q].N, projs[q].ldw};
+            Prepared pr;
+            if ((rc = prepare(segs, j - i, a.x, a.K, a.B, sm_count, &pr)) != GEMV_OK) {
+                delete plan;
+                return rc;
+            }
+            plan->launches.push_back(pr);
+            i = j;
+        }
+    } catch (const std::bad_alloc&) {
+        delete plan;
+        return GEMV_ERR_NOMEM;
+    }
+    *out = plan;
+    return GEMV_OK;
+}
+
+int gemv_plan_capture(gemv_plan* plan, void* stream) {
+    if (!plan || !stream) return GEMV_ERR_INVALID;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (cs != cudaStreamCaptureStatusNone) return GEMV_ERR_CAPTURE;
+
+    if ((e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal)) != cudaSuccess) return cuda_fail(e);
+    int rc = GEMV_OK;
+    for (const Prepared& pr : plan->launches) {
+        if ((rc = run(pr, s)) != GEMV_OK) break;
+    }
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(s, &g);
+    if (rc != GEMV_OK) {
+        if (g) cudaGraphDestroy(g);
+        return rc;
+    }
+    if (e != cudaSuccess) {
+        if (g) cudaGraphDestroy(g);
+        g_last_cuda_error = static_cast<int>(e);
+        return GEMV_ERR_CAPTURE;
+    }
+    cudaGraphExec_t ex = nullptr;
+    if ((e = cudaGraphInstantiate(&ex, g, 0)) != cudaSuccess) {
+        cudaGraphDestroy(g);
+        g_last_cuda_error = static_cast<int>(e);
+        return GEMV_ERR_CAPTURE;
+    }
+    if (plan->exec) cudaGraphExecDestroy(plan->exec);
+    if (plan->graph) cudaGraphDestroy(plan->graph);
+    plan->graph = g;
+    plan->exec = ex;
+    return GEMV_OK;
+}
+
+int gemv_plan_launch(gemv_plan* plan, void* stream) {
+    if (!plan) return GEMV_ERR_INVALID;
+    if (!plan->exec) return GEMV_ERR_UNSUPPORTED;
+    cudaError_t e = cudaGraphLaunch(plan->exec, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return GEMV_OK;
+}
+
+int gemv_plan_num_launches(const gemv_plan* plan) {
+    return plan ? static_cast<int>(plan->launches.size()) : 0;
+}
+
+void gemv_plan_destroy(gemv_plan* plan) {
+    if (!plan) return;
+    if (plan->exec) cudaGraphExecDestroy(plan->exec);
+    if (plan->graph) cudaGraphDestroy(plan->graph);
+    delete plan;
+}
+
+int gemv_query_launch(int64_t N, int64_t K, int B, int sm_count, gemv_launch_info* out) {
+    if (!out) return GEMV_ERR_INVALID;
+    Launch l;
+    int rc = gemv::plan_launch(N, K, B, sm_count, &l);
+    if (rc != GEMV_OK) return rc;
+    out->rows_per_cta = l.rows_per_cta;
+    out->row_tiles = l.row_tiles;
+    out->grid = l.grid;
+    out->kslice = l.kslice;
+    out->kchunk = l.kchunk;
+    out->warps_per_cta = gemv::kWarps;
+    out->warps_per_row = l.kw;
+    out->splits = l.splits;
+    out->rows_per_warp = l.rows_per_warp;
+    out->unroll = l.unroll;
+    out->smem_bytes = l.smem_bytes;
+    out->variant = B - 1;
+    return GEMV_OK;
+}
+
+int gemv_probe_sink_words(void) { return 4096; }
+
+int gemv_probe_stream_read(const void* src, int64_t bytes, float* sink, void* stream) {
+    if (!src || !sink || bytes < 16 || bytes % 16 != 0) return GEMV_ERR_INVALID;
+    if (!aligned(src, 16) || !aligned(sink, 4)) return GEMV_ERR_ALIGN;
+    int sm_count = 0;
+    int rc = device_state(&sm_count);
+    if (rc != GEMV_OK) return rc;
+    int grid = sm_count * 8;
+    if (grid > gemv_probe_sink_words()) grid = gemv_probe_sink_words();
+    cudaError_t e = gemv::launch_probe_read(src, bytes, sink, grid, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return GEMV_OK;
+}
+
+const char* gemv_status_string(int status) {
+    switch (status) {
+    case GEMV_OK: return "GEMV_OK";
+    case GEMV_ERR_INVALID: return "GEMV_ERR_INVALID: a size, count or pointer is out of range";
+    case GEMV_ERR_ALIGN: return "GEMV_ERR_ALIGN: W must be 16-byte aligned, ldw a multiple of 8, x 2-byte and y 4-byte aligned";
+    case GEMV_ERR_CUDA: return "GEMV_ERR_CUDA: a CUDA runtime call failed (see gemv_last_cuda_error)";
+    case GEMV_ERR_NOMEM: return "GEMV_ERR_NOMEM: host allocation failed";
+    case GEMV_ERR_CAPTURE: return "GEMV_ERR_CAPTURE: graph capture or instantiation failed";
+    case GEMV_ERR_UNSUPPORTED: return "GEMV_ERR_UNSUPPORTED: needs an sm_103 GPU, a captured plan, or a smaller problem";
+    default: return "unknown gemv status";
+    }
+}
+
+int gemv_last_cuda_error(void) { return g_last_cuda_error; }
+
+}  // extern "C"

@@ -1,0 +1,76 @@
+// Batch-size dispatch and the read-only bandwidth probe.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "gemv_internal.h"
+
+namespace gemv {
+
+cudaError_t launch_gemv_b1_4(int B, const Params& p, const Launch& l, cudaStream_t s, bool pdl);
+cudaError_t launch_gemv_b5_8(int B, const Params& p, const Launch& l, cudaStream_t s, bool pdl);
+cudaError_t launch_gemv_b9_12(int B, const Params& p, const Launch& l, cudaStream_t s, bool pdl);
+cudaError_t launch_gemv_b13_16(int B, const Params& p, const Launch& l, cudaStream_t s, bool pdl);
+cudaError_t prepare_b1_4();
+cudaError_t prepare_b5_8();
+cudaError_t prepare_b9_12();
+cudaError_t prepare_b13_16();
+
+cudaError_t launch_gemv(int B, const Params& p, const Launch& l, cudaStream_t s, bool pdl) {
+    if (B >= 1 && B <= 4) return launch_gemv_b1_4(B, p, l, s, pdl);
+    if (B >= 5 && B <= 8) return launch_gemv_b5_8(B, p, l, s, pdl);
+    if (B >= 9 && B <= 12) return launch_gemv_b9_12(B, p, l, s, pdl);
+    if (B >= 13 && B <= 16) return launch_gemv_b13_16(B, p, l, s, pdl);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t prepare_kernels(int /*device: attributes apply to the current device*/) {
+    cudaError_t e;
+    if ((e = prepare_b1_4()) != cudaSuccess) return e;
+    if ((e = prepare_b5_8()) != cudaSuccess) return e;
+    if ((e = prepare_b9_12()) != cudaSuccess) return e;
+    return prepare_b13_16();
+}
+
+// Streams `nvec` 16-byte vectors with the GEMV's load form, 8 independent loads
+// per thread in flight, and leaves one checksum per CTA so that nothing is
+// optimised away. Measures the read-only HBM ceiling.
+__global__ void __launch_bounds__(256) probe_read_kernel(const uint4* __restrict__ src, int64_t nvec,
+                                                         float* __restrict__ sink) {
+    constexpr int U = 8;
+    uint32_t h = 0;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (; i + (U - 1) * stride < nvec; i += U * stride) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint4* q = src + i + u * stride;
+            asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                : "=r"(v[u].x), "=r"(v[u].y), "=r"(v[u].z), "=r"(v[u].w)
+                : "l"(q));
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) h ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
+    }
+    for (; i < nvec; i += stride) {
+        const uint4 v = __ldg(src + i);
+        h ^= v.x ^ v.y ^ v.z ^ v.w;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) h ^= __shfl_xor_sync(0xffffffffu, h, off);
+    __shared__ uint32_t part[8];
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = h;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t t = 0;
+        for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t ^= part[w];
+        sink[blockIdx.x] = __uint_as_float(t & 0x007fffffu);   // a finite float
+    }
+}
+
+cudaError_t launch_probe_read(const void* src, int64_t bytes, float* sink, int grid, cudaStream_t s) {
+    probe_read_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(src), bytes / 16, sink);
+    return cudaGetLastError();
+}
+
+}  // namespace gemv

@@ -1,0 +1,131 @@
+"""Decode-projection workloads: shapes of a Llama-3.1-8B-shaped model (random
+init, shapes only) and the device-resident decode step built from them.
+
+One decode step at batch 1 multiplies, in every layer, the hidden vector by the
+fused Q/K/V projection (4,096 + 1,024 + 1,024 rows), the output projection
+(4,096 rows), the fused gate/up projection (14,336 + 14,336 rows) and the down
+projection (4,096 rows over K = 14,336), then the LM head (128,256 rows)
+("Decode GEMV at half of HBM bandwidth", causes 1 and 3; "GPU performance
+chains", "Launch gaps in a decode step"). The projections are not chained: with
+random weights and no nonlinearity in between, each layer reads its own
+activation vector x4096_l (shared by QKV, o_proj and gate/up) and x14336_l
+(read by down); the LM head reads its own x. Each projection group is one
+launch: 4 per layer plus the LM head, 129 for 32 layers, captured as one graph.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import binding, inputs, roofline
+
+LLAMA_8B = dict(layers=32, hidden=4096, intermediate=14336, vocab=128256, q_rows=4096, kv_rows=1024)
+
+# Single-projection shapes (N, K) of that model.
+SHAPES = {
+    "k_proj": (1024, 4096),
+    "down_proj": (4096, 14336),
+    "qkv": (6144, 4096),
+    "o_proj": (4096, 4096),
+    "gate_up": (28672, 4096),
+    "lm_head": (128256, 4096),
+}
+
+# Ragged shapes with ldw = K rounded up to a multiple of 8.
+TAILS = [(7, 129), (4097, 4103), (1, 8191), (33, 65537)]
+
+
+def decode_step_spec(**overrides) -> dict:
+    spec = dict(LLAMA_8B)
+    spec.update(overrides)
+    return spec
+
+
+@dataclass
+class Proj:
+    name: str
+    W: torch.Tensor
+    x: torch.Tensor
+    y: torch.Tensor
+    N: int
+    K: int
+    ldw: int
+    group: int
+
+
+class DecodeStep:
+    """Device-resident weights, activations and outputs of one decode step."""
+
+    def __init__(self, spec: dict, seed: int = 0, device="cuda"):
+        self.spec = spec
+        self.device = device
+        self.projs: list[Proj] = []
+        self.xs: list[tuple[torch.Tensor, int]] = []
+        H, I, V = spec["hidden"], spec["intermediate"], spec["vocab"]
+        Q, KV = spec["q_rows"], spec["kv_rows"]
+        group = 0
+        for l in range(spec["layers"]):
+            base = 16 * l
+            xh = inputs.activations(1, H, seed=seed, index=base + 14, device=device)
+            xi = inputs.activations(1, I, seed=seed, index=base + 15, device=device)
+            self.xs += [(xh, base + 14), (xi, base + 15)]
+            group += 1
+            for j, (nm, n) in enumerate([("q", Q), ("k", KV), ("v", KV)]):
+                self._add(f"l{l}.{nm}_proj", n, H, xh, group, seed, base + j)
+            self._add(f"l{l}.o_proj", H, H, xh, 0, seed, base + 3)
+            group += 1
+            self._add(f"l{l}.gate_proj", I, H, xh, group, seed, base + 4)
+            self._add(f"l{l}.up_proj", I, H, xh, group, seed, base + 5)
+            self._add(f"l{l}.down_proj", H, I, xi, 0, seed, base + 6)
+        base = 16 * spec["layers"]
+        xl = inputs.activations(1, H, seed=seed, index=base + 1, device=device)
+        self.xs.append((xl, base + 1))
+        self._add("lm_head", V, H, xl, 0, seed, base)
+
+    def _add(self, name, N, K, x, group, seed, index):
+        ldw = inputs.padded_ldw(K)
+        W = inputs.weight(N, K, ldw, seed=seed, index=index, device=self.device)
+        y = torch.empty((1, N), dtype=torch.float32, device=self.device)
+        self.projs.append(Proj(name, W, x, y, N, K, ldw, group))
+
+    def plan(self) -> binding.Plan:
+        return binding.Plan([(p.W, p.x, p.y, p.N, p.K, p.ldw, 1, p.group) for p in self.projs],
+                            keepalive=self)
+
+    def outputs(self):
+        return [p.y for p in self.projs]
+
+    def refresh_x(self, seed: int) -> None:
+        """Overwrite every activation vector in place (the plan keeps its addresses)."""
+        for x, index in self.xs:
+            x.copy_(inputs.activations(1, x.shape[1], seed=seed, index=index, device=self.device))
+
+    def checks(self):
+        for p in self.projs:
+            yield p.name, p.W, p.x, p.y, p.K
+
+    def algorithmic_bytes(self) -> int:
+        """Sum of N*K*2 + K*2 + N*4 over the projections; a fused launch moves
+        its x once, so each launch group counts x once."""
+        total = 0
+        seen_groups = set()
+        for p in self.projs:
+            total += 2 * p.N * p.K + 4 * p.N
+            if p.group == 0 or p.group not in seen_groups:
+                total += 2 * p.K
+                seen_groups.add(p.group)
+        return total
+
+    def weight_bytes(self) -> int:
+        return sum(2 * p.N * p.K for p in self.projs)
+
+
+def step_bytes_formula(spec: dict) -> int:
+    """Algorithmic bytes of the step with fused groups counted as one GEMV each
+    (QKV 6,144 rows; gate/up 28,672 rows)."""
+    H, I, V = spec["hidden"], spec["intermediate"], spec["vocab"]
+    Q, KV = spec["q_rows"], spec["kv_rows"]
+    layer = (roofline.algorithmic_bytes(Q + 2 * KV, H) + roofline.algorithmic_bytes(H, H)
+             + roofline.algorithmic_bytes(2 * I, H) + roofline.algorithmic_bytes(H, I))
+    return spec["layers"] * layer + roofline.algorithmic_bytes(V, H)

@@ -1,0 +1,153 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every entry
+point include/gemv.h declares, rejects bad arguments before touching the
+device, and plans launches by the stated rules."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from memory_bound_decode_gb300 import binding, build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gemv.h")
+GB300_SMS = 152
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_lib.build()
+    return binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(gemv_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ["gemv_bf16", "gemv_bf16_multi", "gemv_plan_create", "gemv_plan_capture",
+                     "gemv_plan_launch", "gemv_plan_destroy", "gemv_status_string",
+                     "gemv_last_cuda_error"]:
+        assert required in names
+    assert sorted(names) == sorted(binding.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_status_strings(L):
+    for s in [0, -1, -2, -3, -4, -5, -6]:
+        assert binding.gemv_status_string(s).startswith("GEMV_")
+    assert binding.gemv_status_string(12345) == "unknown gemv status"
+    assert binding.gemv_last_cuda_error() == 0
+
+
+A16 = 1 << 20   # a fake, 16-byte aligned address: never dereferenced by validation
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, A16, A16, 8, 8, 1, 8), binding.GEMV_ERR_INVALID),          # W NULL
+    ((A16, 0, A16, 8, 8, 1, 8), binding.GEMV_ERR_INVALID),          # x NULL
+    ((A16, A16, 0, 8, 8, 1, 8), binding.GEMV_ERR_INVALID),          # y NULL
+    ((A16, A16, A16, 0, 8, 1, 8), binding.GEMV_ERR_INVALID),        # N = 0
+    ((A16, A16, A16, 8, 0, 1, 8), binding.GEMV_ERR_INVALID),        # K = 0
+    ((A16, A16, A16, 8, 8, 0, 8), binding.GEMV_ERR_INVALID),        # B = 0
+    ((A16, A16, A16, 8, 8, 17, 8), binding.GEMV_ERR_INVALID),       # B > 16
+    ((A16, A16, A16, 8, 9, 1, 8), binding.GEMV_ERR_INVALID),        # ldw < K
+    ((A16, A16, A16, 8, 9, 1, 12), binding.GEMV_ERR_ALIGN),         # ldw % 8
+    ((A16 + 8, A16, A16, 8, 8, 1, 8), binding.GEMV_ERR_ALIGN),      # W not 16-B aligned
+    ((A16, A16 + 1, A16, 8, 8, 1, 8), binding.GEMV_ERR_ALIGN),      # x odd address
+    ((A16, A16, A16 + 2, 8, 8, 1, 8), binding.GEMV_ERR_ALIGN),      # y not 4-B aligned
+    ((A16, A16, A16, 1 << 31, 8, 1, 8), binding.GEMV_ERR_INVALID),  # N too large
+])
+def test_gemv_bf16_rejects_before_launch(L, args, status):
+    assert binding.gemv_bf16(*args, stream=0, check=False) == status
+
+
+def test_multi_rejects(L):
+    seg = (A16, A16, 8, 8)
+    assert binding.gemv_bf16_multi([], A16, 8, 1, stream=0, check=False) == binding.GEMV_ERR_INVALID
+    assert binding.gemv_bf16_multi([seg] * 9, A16, 8, 1, stream=0, check=False) == binding.GEMV_ERR_INVALID
+    assert binding.gemv_bf16_multi([seg, (A16 + 8, A16, 8, 8)], A16, 8, 1, stream=0,
+                                   check=False) == binding.GEMV_ERR_ALIGN
+    assert binding.gemv_bf16_multi([seg, (A16, A16, 8, 4)], A16, 8, 1, stream=0,
+                                   check=False) == binding.GEMV_ERR_INVALID
+
+
+def test_plan_rejects(L):
+    good = (A16, A16, A16, 8, 8, 8, 1, 0)
+    with pytest.raises(binding.GemvError) as e:
+        binding.Plan([good, (A16, A16, A16, 8, 8, 8, 17, 0)])
+    assert e.value.status == binding.GEMV_ERR_INVALID
+    with pytest.raises(binding.GemvError) as e:
+        binding.Plan([(A16, A16, A16, 8, 8, 8, 1, -1)])
+    assert e.value.status == binding.GEMV_ERR_INVALID
+    assert L.gemv_plan_create(None, 1, None) == binding.GEMV_ERR_INVALID
+    assert L.gemv_plan_launch(None, None) == binding.GEMV_ERR_INVALID
+    assert L.gemv_plan_capture(None, None) == binding.GEMV_ERR_INVALID
+    assert L.gemv_plan_num_launches(None) == 0
+    L.gemv_plan_destroy(None)
+
+
+def test_probe_rejects(L):
+    assert L.gemv_probe_stream_read(A16, 15, A16, None) == binding.GEMV_ERR_INVALID
+    assert L.gemv_probe_stream_read(A16 + 4, 64, A16, None) == binding.GEMV_ERR_ALIGN
+    assert binding.gemv_probe_sink_words() >= GB300_SMS * 8
+
+
+SHAPES = [  # (N, K) of the decode projections and the ragged cases
+    (1024, 4096), (4096, 14336), (6144, 4096), (28672, 4096), (4096, 4096), (128256, 4096),
+    (7, 129), (4097, 4103), (1, 8191), (33, 65537), (1, 1), (3, 8), (100000, 300),
+]
+
+
+@pytest.mark.parametrize("B", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("N,K", SHAPES)
+def test_plan_covers_the_problem(L, N, K, B):
+    q = binding.gemv_query_launch(N, K, B, GB300_SMS)
+    assert q["warps_per_cta"] * 32 == 256
+    assert q["warps_per_row"] in (1, 2, 4, 8)
+    assert 1 <= q["splits"] <= 8
+    assert q["rows_per_cta"] == (8 // q["warps_per_row"]) * q["rows_per_warp"]
+    assert q["row_tiles"] * q["rows_per_cta"] >= N > (q["row_tiles"] - 1) * q["rows_per_cta"]
+    assert q["grid"] == q["row_tiles"] * q["splits"]
+    # K-slices are whole 256-column warp-steps, cover K, and none is empty
+    assert q["kslice"] % 256 == 0 and q["kchunk"] % 256 == 0
+    assert q["splits"] * q["kslice"] >= K > (q["splits"] - 1) * q["kslice"]
+    assert q["kchunk"] <= q["kslice"]
+    assert B * q["kchunk"] * 2 <= 40 * 1024 or q["kchunk"] == 256
+    assert q["smem_bytes"] <= 96 * 1024
+
+
+def test_no_split_when_rows_fill_the_gpu(L):
+    # "Splitting K on every shape, including those that already fill the
+    # machine many times over" is the mistake to avoid: large-N projections
+    # stream whole rows per warp with no split at all.
+    for N, K in [(4096, 14336), (6144, 4096), (28672, 4096), (4096, 4096), (128256, 4096)]:
+        q = binding.gemv_query_launch(N, K, 1, GB300_SMS)
+        assert q["splits"] == 1 and q["warps_per_row"] == 1, (N, K, q)
+        assert q["grid"] * 8 >= GB300_SMS * 16
+
+
+def test_split_when_rows_do_not_fill_the_gpu(L):
+    # few rows, long K: K is split until the GPU is covered
+    q = binding.gemv_query_launch(33, 65537, 1, GB300_SMS)
+    assert q["warps_per_row"] * q["splits"] > 1
+    assert q["grid"] * 8 >= 33 * 8
+    small = binding.gemv_query_launch(1024, 4096, 1, GB300_SMS)
+    assert small["warps_per_row"] * small["splits"] > 1
+
+
+def test_planner_rejects(L):
+    with pytest.raises(binding.GemvError):
+        binding.gemv_query_launch(0, 8, 1, GB300_SMS)
+    with pytest.raises(binding.GemvError):
+        binding.gemv_query_launch(8, 8, 17, GB300_SMS)
+    with pytest.raises(binding.GemvError):
+        binding.gemv_query_launch(8, 8, 1, 0)

@@ -1,0 +1,111 @@
+"""Host-side logic of bench.py and the workload definitions, on the CPU: the
+JSON contract of the reference arm, the byte accounting of the decode step and
+the multi-rank combination (world size 2 over gloo)."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+from memory_bound_decode_gb300 import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_defaults_and_workloads():
+    a = bench.parse_args([])
+    assert a.gpus == 1 and a.impl == "ours" and a.workload == "down_proj"
+    assert a.warmup >= 3
+    assert bench.describe("down_proj") == ("single", [4096], 14336, 1)
+    assert bench.describe("qkv") == ("fused", [4096, 1024, 1024], 4096, 1)
+    assert bench.describe("gate_up") == ("fused", [14336, 14336], 4096, 1)
+    assert bench.describe("skinny:4096x14336:B16") == ("single", [4096], 14336, 16)
+    assert bench.describe("tail:33x65537") == ("single", [33], 65537, 1)
+    with pytest.raises(SystemExit):
+        bench.describe("nonsense")
+
+
+def test_decode_step_bytes():
+    spec = workloads.decode_step_spec()
+    assert workloads.step_bytes_formula(spec) == 15_017_047_040
+    tiny = workloads.decode_step_spec(layers=2, hidden=64, intermediate=192, vocab=300,
+                                      q_rows=64, kv_rows=16)
+    step = workloads.DecodeStep(tiny, seed=0, device="cpu")
+    assert step.algorithmic_bytes() == workloads.step_bytes_formula(tiny)
+    assert len(step.projs) == 2 * 7 + 1
+    groups = [p.group for p in step.projs]
+    assert groups[:3] == [groups[0]] * 3 and groups[0] > 0      # q, k, v fused
+    assert groups[3] == 0                                        # o_proj alone
+
+
+def test_peaks_and_traffic_lookup(tmp_path, monkeypatch):
+    peak, kind = bench.load_peaks()
+    assert peak > 1000 and kind in ("measured", "fallback")
+    h = bench.kernel_source_hash()
+    assert len(h) == 16
+    assert bench.profiled_traffic("no_such_workload", h) is None
+
+
+def test_reference_arm_json_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "2", "--warmup", "3"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    lines = [l for l in out.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference"
+    for key in ["metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "config", "cpu_baseline", "e2e"]:
+        assert key in rec
+    assert rec["steps"] == 2 and rec["value"] > 0
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["cores"] >= 1
+    assert rec["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_other_ranks_are_silent(monkeypatch):
+    args = bench.parse_args(["--impl", "reference", "--steps", "1"])
+    assert bench.run_reference(args, rank=1) is None
+
+
+def test_clock_sampler_without_nvidia_smi(monkeypatch):
+    monkeypatch.setenv("PATH", "/nonexistent")
+    c = bench.ClockSampler(0)
+    c.start()
+    info = c.stop()
+    assert info["samples"] == 0 and info["sm_mhz"] is None
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    got = bench.max_over_ranks(1.5 + rank, dist, "cpu")
+    dist.barrier()
+    dist.destroy_process_group()
+    q.put((rank, got))
+
+
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == {0: 2.5, 1: 2.5}
+    assert bench.max_over_ranks(3.0, None, "cpu") == 3.0

@@ -1,0 +1,194 @@
+"""Parity of the CUDA GEMV (through the C ABI) with the CPU oracle.
+
+Every comparison is element by element: |y_gpu - y_ref| <= 1e-5 * sum_k |W x|
+and y_gpu finite, y surrounded by sentinel guard bands that must survive and
+prefilled with NaN so that every element must be written. Integer-valued and
+one-hot inputs, for which every FP32 summation order is exact, are compared
+bitwise.
+"""
+import numpy as np
+import pytest
+import torch
+
+from memory_bound_decode_gb300 import binding, inputs
+from oracle import oracle
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+SMALL = [  # (N, K): ragged tails, split-K, tiny and degenerate shapes
+    (7, 129), (1, 1), (3, 8), (5, 9), (65, 300), (300, 2056), (1, 8191),
+    (4097, 4103), (33, 65537), (1024, 4096), (17, 100000),
+]
+
+
+def make(N, K, B, seed=0, device=DEV):
+    ldw = inputs.padded_ldw(K)
+    W = inputs.weight(N, K, ldw, seed=seed, index=0, device=device)
+    x = inputs.activations(B, K, seed=seed, index=1, device=device)
+    return W, x, ldw
+
+
+@pytest.mark.parametrize("B", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("N,K", SMALL)
+def test_parity_small(N, K, B):
+    W, x, _ = make(N, K, B, seed=N + K + B)
+    y = gu.gemv(W, x, K)
+    y_ref, s = gu.reference(W, x, K)
+    gu.assert_parity(y, y_ref, s, f"N={N} K={K} B={B}")
+
+
+@pytest.mark.parametrize("N,K,ldw", [(64, 1000, 1024), (9, 129, 256), (100, 4096, 4104)])
+def test_wide_row_stride(N, K, ldw):
+    """ldw well beyond K: the padding (NaN) is never part of a sum."""
+    W, x, _ = make(N, K, 2)
+    W2 = torch.full((N, ldw), float("nan"), dtype=torch.bfloat16, device=DEV)
+    W2[:, :K] = W[:, :K]
+    y = gu.gemv(W2, x, K)
+    y_ref, s = gu.reference(W2, x, K)
+    gu.assert_parity(y, y_ref, s)
+
+
+FULL = [  # the decode projections of a Llama-3.1-8B-shaped layer, and the LM head
+    ("k_proj", 1024, 4096), ("down_proj", 4096, 14336), ("qkv", 6144, 4096),
+    ("o_proj", 4096, 4096), ("gate_up", 28672, 4096), ("lm_head", 128256, 4096),
+]
+
+
+@pytest.mark.parametrize("name,N,K", FULL, ids=[f[0] for f in FULL])
+def test_parity_full_size(name, N, K):
+    W, x, _ = make(N, K, 1, seed=1)
+    y = gu.gemv(W, x, K)
+    y_ref, s = gu.reference(W, x, K)
+    gu.assert_parity(y, y_ref, s, name)
+
+
+@pytest.mark.parametrize("B", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("N,K", [(4096, 4096), (4096, 14336)])
+def test_parity_skinny_batch(N, K, B):
+    W, x, _ = make(N, K, B, seed=2)
+    y = gu.gemv(W, x, K)
+    y_ref, s = gu.reference(W, x, K)
+    gu.assert_parity(y, y_ref, s, f"B={B}")
+
+
+@pytest.mark.parametrize("N,K,B", [(7, 129, 1), (4097, 4103, 3), (33, 65537, 1), (1, 8191, 16),
+                                   (128256, 4096, 1), (4096, 14336, 16)])
+def test_integer_inputs_are_exact(N, K, B):
+    """Small integers: every partial sum is an integer below 2^24, so any FP32
+    order gives the exact result, bit for bit."""
+    ldw = inputs.padded_ldw(K)
+    W = inputs.int_weight(N, K, ldw, seed=3, device=DEV)
+    x = inputs.int_activations(B, K, seed=3, device=DEV)
+    y = gu.gemv(W, x, K)
+    y_ref, _ = gu.reference(W, x, K)
+    assert np.array_equal(y.astype(np.float64), y_ref)
+
+
+@pytest.mark.parametrize("N,K", [(4097, 4103), (33, 65537), (1024, 4096)])
+def test_one_hot_selects_a_column(N, K):
+    W, _, _ = make(N, K, 1, seed=4)
+    Wh = inputs.bits(W)
+    for j in (0, 7, 8, 255, 256, K - 1):
+        x = torch.zeros((1, K), dtype=torch.bfloat16, device=DEV)
+        x[0, j] = 1.0
+        y = gu.gemv(W, x, K)
+        col = inputs.from_bits(Wh[:, j]).float().numpy()
+        assert np.array_equal(y[0], col), j
+
+
+def test_identity_padded():
+    N, K = 300, 129
+    ldw = inputs.padded_ldw(K)
+    W = torch.zeros((N, ldw), dtype=torch.bfloat16, device=DEV)
+    W[:, K:] = float("nan")
+    idx = torch.arange(min(N, K), device=DEV)
+    W[idx, idx] = 1.0
+    x = inputs.activations(1, K, seed=5, device=DEV)
+    y = gu.gemv(W, x, K)
+    want = np.zeros(N, dtype=np.float32)
+    want[:K] = x[0].float().cpu().numpy()
+    assert np.array_equal(y[0], want)
+
+
+@pytest.mark.parametrize("N,K,B", [(4096, 14336, 1), (33, 65537, 1), (1000, 3000, 4)])
+def test_deterministic_and_scale_exact(N, K, B):
+    W, x, _ = make(N, K, B, seed=6)
+    y1 = gu.gemv(W, x, K)
+    y2 = gu.gemv(W, x, K)
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+    y4 = gu.gemv(W, (x.float() * 4.0).to(torch.bfloat16), K)
+    assert np.array_equal(y4, y1 * np.float32(4.0))
+
+
+def test_row_permutation_permutes_y():
+    N, K, B = 4097, 4103, 2
+    W, x, _ = make(N, K, B, seed=7)
+    perm = torch.randperm(N, generator=torch.Generator().manual_seed(0)).to(DEV)
+    y = gu.gemv(W, x, K)
+    yp = gu.gemv(W[perm].contiguous(), x, K)
+    assert np.array_equal(yp, y[:, perm.cpu().numpy()])
+
+
+def test_batch_rows_match_single_calls():
+    N, K, B = 2048, 5000, 8
+    W, x, _ = make(N, K, B, seed=8)
+    y = gu.gemv(W, x, K)
+    y_ref, s = gu.reference(W, x, K)
+    for b in range(B):
+        yb = gu.gemv(W, x[b:b + 1].contiguous(), K)
+        assert np.all(np.abs(yb[0].astype(np.float64) - y[b]) <= 2e-5 * s[b])
+
+
+def test_linearity():
+    N, K = 1024, 4096
+    W, _, _ = make(N, K, 1, seed=9)
+    xa = inputs.int_activations(1, K, lo=-8, hi=8, seed=1, device=DEV)
+    xb = inputs.int_activations(1, K, lo=-8, hi=8, seed=2, device=DEV)
+    ya = gu.gemv(W, xa, K).astype(np.float64)
+    yb = gu.gemv(W, xb, K).astype(np.float64)
+    ys = gu.gemv(W, (xa.float() + xb.float()).to(torch.bfloat16), K).astype(np.float64)
+    _, sa = gu.reference(W, xa, K)
+    _, sb = gu.reference(W, xb, K)
+    assert np.all(np.abs(ys - (ya + yb)) <= 2e-5 * (sa + sb))
+
+
+def test_misaligned_x_rows():
+    """x rows start at odd 2-byte offsets when K % 8 != 0; x itself may start at
+    any even address."""
+    N, K, B = 500, 1001, 5
+    W, x, _ = make(N, K, B, seed=10)
+    xbuf = torch.zeros(B * K + 3, dtype=torch.bfloat16, device=DEV)
+    xbuf[3:] = x.reshape(-1)
+    xs = xbuf[3:].view(B, K)
+    buf, y = gu.guarded_y(B, N)
+    binding.gemv_bf16(W, xs, y, N, K, B, W.shape[1])
+    torch.cuda.synchronize()
+    gu.check_guards(buf)
+    y_ref, s = gu.reference(W, x, K)
+    gu.assert_parity(y.cpu().numpy(), y_ref, s)
+
+
+def test_side_stream_and_no_sync():
+    N, K = 4096, 4096
+    W, x, _ = make(N, K, 1, seed=11)
+    s = torch.cuda.Stream()
+    buf, y = gu.guarded_y(1, N)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        binding.gemv_bf16(W, x, y, N, K, 1, W.shape[1], s)
+    s.synchronize()
+    gu.check_guards(buf)
+    y_ref, sc = gu.reference(W, x, K)
+    gu.assert_parity(y.cpu().numpy(), y_ref, sc)
+
+
+def test_probe_stream_read_runs():
+    nbytes = 64 << 20
+    src = torch.randint(-1000, 1000, (nbytes // 2,), dtype=torch.int16, device=DEV)
+    sink = torch.full((binding.gemv_probe_sink_words(),), -1.0, device=DEV)
+    binding.gemv_probe_stream_read(src, nbytes, sink)
+    torch.cuda.synchronize()
+    assert torch.isfinite(sink[:152]).all()
