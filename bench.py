@@ -52,6 +52,8 @@ def parse_args(argv=None):
                          "skinny:<N>x<K>:B<b> | tail:<N>x<K>")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-probe", action="store_true",
+                    help="skip the read-only ceiling probe (keeps device memory small)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args(argv)
 
@@ -338,7 +340,9 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
                "d2h_bytes_per_step": int(sum(y.numel() * y.element_size() for y in y_host)),
                "us_per_step": round(e2e_s / e2e_steps * 1e6, 3), "steps": e2e_steps}
 
-    read_ceiling = read_ceiling_gbs(torch, binding, stream) if rank == 0 else None
+    read_ceiling = None
+    if rank == 0 and not args.no_probe:
+        read_ceiling = read_ceiling_gbs(torch, binding, stream)
 
     if rank != 0:
         return None
@@ -361,9 +365,10 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
                      "peak_kind": f"{peak_kind} copy (MEASURED_PEAKS hbm_gbs, burst)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "kernel": "gemv_bf16_kernel", "kernel_source_hash": src_hash},
-        "ceilings": {"copy_gbs": peak, "read_probe_gbs": round(read_ceiling, 1),
+        "ceilings": {"copy_gbs": peak,
+                     "read_probe_gbs": round(read_ceiling, 1) if read_ceiling else None,
                      "vendor_gbs": VENDOR_HBM_GBS,
-                     "frac_of_read_probe": round(achieved / read_ceiling, 4),
+                     "frac_of_read_probe": round(achieved / read_ceiling, 4) if read_ceiling else None,
                      "frac_of_vendor": round(achieved / VENDOR_HBM_GBS, 4)},
         "gpu_launches": steps * wk.launches_per_step,
         "clocks": clock_info,
