@@ -9,7 +9,8 @@
 //     per row before it consumes any, so a resident warp keeps
 //     32 * UJ * RPW * 16 bytes in flight (Little's law sets how many are needed).
 //   * x (the CTA's K-range, in chunks) is staged once per CTA in shared memory
-//     and reused by every row of the CTA; W is never staged: it has no reuse.
+//     with asynchronous 16-byte copies (all in flight at once) and reused by
+//     every row of the CTA; W is never staged: it has no reuse.
 //   * The first batch of W loads is issued before the CTA waits on the
 //     preceding grid (programmatic dependent launch) and before x is staged, so
 //     neither the previous kernel's tail nor the x copy leaves the HBM idle.
@@ -89,8 +90,24 @@ __device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank) {
     return v;
 }
 
+// 16-byte asynchronous global->shared copy of `nbytes` (2..16) bytes; the rest
+// of the 16 bytes is zero-filled. Both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src, int nbytes) {
+    const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                 :: "r"(dst), "l"(gmem_src), "r"(nbytes) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // Copy x[b][c0 .. c0 + 8*nv) for every batch row into shared memory (row
-// stride xstride), zero-filling columns >= K.
+// stride xstride), zero-filling columns >= K. Aligned 16-byte pieces go out as
+// asynchronous copies, all in flight at once and holding no registers;
+// misaligned ones (rows of x start at 2-byte offsets when K % 8 != 0) are
+// loaded element by element. The caller waits with cp_async_wait_all() and a
+// barrier.
 template <int B>
 __device__ __forceinline__ void stage_x(uint16_t* xs, int xstride, const uint16_t* __restrict__ x,
                                         int64_t K, int64_t c0, int nv) {
@@ -101,9 +118,9 @@ __device__ __forceinline__ void stage_x(uint16_t* xs, int xstride, const uint16_
         const int i = it - b * nv;
         const int64_t col = c0 + 8 * static_cast<int64_t>(i);
         const uint16_t* src = x + static_cast<int64_t>(b) * K + col;
-        uint4 v;
-        if (col + 8 <= K && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
-            v = __ldg(reinterpret_cast<const uint4*>(src));
+        uint16_t* dst = xs + static_cast<int64_t>(b) * xstride + 8 * i;
+        if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+            cp_async16(dst, src, (col + 8 <= K) ? 16 : static_cast<int>(K - col) * 2);
         } else {
             uint32_t w[4];
 #pragma unroll
@@ -112,9 +129,8 @@ __device__ __forceinline__ void stage_x(uint16_t* xs, int xstride, const uint16_
                 uint32_t hi = (col + 2 * q + 1 < K) ? __ldg(src + 2 * q + 1) : 0u;
                 w[q] = lo | (hi << 16);
             }
-            v = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        *reinterpret_cast<uint4*>(xs + static_cast<int64_t>(b) * xstride + 8 * i) = v;
     }
 }
 
@@ -260,6 +276,7 @@ gemv_bf16_kernel(const __grid_constant__ Params p) {
             __syncthreads();   // every warp is done reading the previous chunk
         }
         stage_x<B>(xs, xstride, p.x, K, c0, nv);
+        cp_async_wait_all();
         __syncthreads();
         consume_batch<B, RPW, UJ, true>(acc, wv, ok, xl, xstride);
 
