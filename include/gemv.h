@@ -7,7 +7,10 @@
  *
  *     y[b][n] = sum_{k < K} float(W[n][k]) * float(x[b][k])
  *
- * with BF16 weights and activations, products and sums in FP32. At batch 1 this
+ * with BF16 weights and activations, products and sums in FP32 (batch 1 on the
+ * CUDA cores; batches 2..16 on the BF16 tensor cores with FP32 accumulation,
+ * where B multiply-adds per weight element would otherwise make the CUDA cores,
+ * not HBM, the limit: "What interviewers probe next"). At batch 1 this
  * is a byte stream: the time is the weight bytes over the HBM bandwidth the
  * kernel sustains ("How to approach it"), so the library is built to keep enough
  * 16-byte loads in flight on every SM ("A strong answer", Little's law) and to
@@ -150,22 +153,23 @@ void gemv_plan_destroy(gemv_plan *plan);
 
 /*
  * How a shape is launched, for tests and the benchmark. Pure host arithmetic;
- * makes no CUDA call. sm_count is the GPU's SM count (e.g. 152 on a GB300);
- * ctas_per_sm is how many CTAs of the chosen kernel fit on one SM.
+ * makes no CUDA call. sm_count is the GPU's SM count (152 on a GB300).
  */
 typedef struct {
     int64_t rows_per_cta;    /* output rows one CTA produces                      */
-    int64_t row_tiles;       /* ceil(N / rows_per_cta)                            */
+    int64_t row_tiles;       /* ceil(N / rows_per_cta), per fused launch summed   */
     int64_t grid;            /* CTAs launched = row_tiles * splits                */
     int64_t kslice;          /* columns per K-split (all but the last)            */
     int64_t kchunk;          /* columns of x staged in shared memory at a time    */
     int32_t warps_per_cta;
-    int32_t warps_per_row;   /* warps of one CTA that share a row along K         */
+    int32_t warps_per_row;   /* warps of one CTA that share a row group along K   */
     int32_t splits;          /* CTAs along K (one thread-block cluster)           */
-    int32_t rows_per_warp;
-    int32_t unroll;          /* independent 16-byte loads per lane per row before use */
+    int32_t rows_per_warp;   /* rows one warp streams together (16: tensor-core tile) */
+    int32_t unroll;          /* loads per lane per row in flight before any is used */
     int32_t smem_bytes;      /* dynamic shared memory per CTA                     */
-    int32_t variant;         /* kernel instance index                             */
+    int32_t path;            /* 0: CUDA-core FP32 FMA (batch 1), 1: BF16 tensor-core MMA */
+    int32_t xstride;         /* shared-memory elements per staged x row           */
+    int32_t nbuf;            /* x buffers: 2 when the K-range is staged in chunks */
 } gemv_launch_info;
 
 int gemv_query_launch(int64_t N, int64_t K, int B, int sm_count,

@@ -51,7 +51,8 @@ class gemv_launch_info(ctypes.Structure):
     _fields_ = [("rows_per_cta", i64), ("row_tiles", i64), ("grid", i64), ("kslice", i64),
                 ("kchunk", i64), ("warps_per_cta", ctypes.c_int32), ("warps_per_row", ctypes.c_int32),
                 ("splits", ctypes.c_int32), ("rows_per_warp", ctypes.c_int32),
-                ("unroll", ctypes.c_int32), ("smem_bytes", ctypes.c_int32), ("variant", ctypes.c_int32)]
+                ("unroll", ctypes.c_int32), ("smem_bytes", ctypes.c_int32), ("path", ctypes.c_int32),
+                ("xstride", ctypes.c_int32), ("nbuf", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -22,15 +22,14 @@ OBJ_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libgemv.so")
 
 SOURCES = [
-    "gemv_kernels_b1_4.cu",
-    "gemv_kernels_b5_8.cu",
-    "gemv_kernels_b9_12.cu",
-    "gemv_kernels_b13_16.cu",
+    "gemv_fma_instances.cu",
+    "gemv_mma_instances_nb1.cu",
+    "gemv_mma_instances_nb2.cu",
     "gemv_dispatch.cu",
     "planner.cpp",
     "gemv_api.cpp",
 ]
-HEADERS = ["gemv_internal.h", "gemv_kernel.cuh", os.path.join("..", "..", "include", "gemv.h")]
+HEADERS = ["gemv_internal.h", "gemv_common.cuh", "gemv_kernel.cuh", "gemv_mma_kernel.cuh", os.path.join("..", "..", "include", "gemv.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -132,7 +132,9 @@ int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B
     p.nseg = nsegs;
     p.splits = l.splits;
     p.kw = l.kw;
-    p.xstride = static_cast<int32_t>(l.kchunk);
+    p.xstride = l.xstride;
+    p.batch = B;
+    p.nbuf = l.nbuf;
     out->p = p;
     out->l = l;
     out->B = B;
@@ -300,7 +302,9 @@ int gemv_query_launch(int64_t N, int64_t K, int B, int sm_count, gemv_launch_inf
     out->rows_per_warp = l.rows_per_warp;
     out->unroll = l.unroll;
     out->smem_bytes = l.smem_bytes;
-    out->variant = B - 1;
+    out->path = l.path;
+    out->xstride = l.xstride;
+    out->nbuf = l.nbuf;
     return GEMV_OK;
 }
 

@@ -1,0 +1,229 @@
+// Device helpers shared by the decode-GEMV kernels: streaming loads, BF16
+// unpacking, programmatic dependent launch, cluster / distributed shared memory,
+// asynchronous x staging and the fixed-order combine of partial sums.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "gemv_internal.h"
+
+namespace gemv {
+
+// 16-byte weight load: read-only path, not allocated in L1 (W is read once).
+__device__ __forceinline__ uint4 ld_stream16(const uint16_t* p) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+// BF16 -> FP32 is exact: the BF16 bits are the high half of the FP32 pattern.
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+// Keep the first m (1..7) BF16 elements of an 8-element vector, zero the rest
+// (bits are selected, so a NaN in the padding never enters a product).
+__device__ __forceinline__ uint4 keep_first(uint4 v, int m) {
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t keep = (2 * q < m ? 0x0000ffffu : 0u) | (2 * q + 1 < m ? 0xffff0000u : 0u);
+        w[q] &= keep;
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_prerequisites() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Load a float from the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank) {
+    uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+    uint32_t r;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
+    return v;
+}
+
+// 16-byte asynchronous global->shared copy of `nbytes` (2..16) bytes; the rest
+// of the 16 bytes is zero-filled. Both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src, int nbytes) {
+    const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                 :: "r"(dst), "l"(gmem_src), "r"(nbytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most `pending` of this thread's committed copy groups are in flight.
+template <int pending>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" :: "n"(pending) : "memory");
+}
+
+// Copy x[b][c0 .. c0 + 8*nv) for b < B into shared memory (row stride
+// xstride), zero-filling columns >= K. Aligned 16-byte pieces go out as
+// asynchronous copies, all in flight at once and holding no registers;
+// misaligned ones (rows of x start at 2-byte offsets when K % 8 != 0) are
+// loaded element by element. Commits one copy group.
+__device__ __forceinline__ void stage_x(uint16_t* xs, int xstride, const uint16_t* __restrict__ x,
+                                        int B, int64_t K, int64_t c0, int nv) {
+    const int items = B * nv;
+#pragma unroll 4
+    for (int it = threadIdx.x; it < items; it += kThreads) {
+        const int b = (B == 1) ? 0 : it / nv;
+        const int i = it - b * nv;
+        const int64_t col = c0 + 8 * static_cast<int64_t>(i);
+        const uint16_t* src = x + static_cast<int64_t>(b) * K + col;
+        uint16_t* dst = xs + static_cast<int64_t>(b) * xstride + 8 * i;
+        if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+            cp_async16(dst, src, (col + 8 <= K) ? 16 : static_cast<int>(K - col) * 2);
+        } else {
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t lo = (col + 2 * q < K) ? __ldg(src + 2 * q) : 0u;
+                uint32_t hi = (col + 2 * q + 1 < K) ? __ldg(src + 2 * q + 1) : 0u;
+                w[q] = lo | (hi << 16);
+            }
+            *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    cp_async_commit();
+}
+
+// Geometry of one staged chunk of K, [c0, c1), in 8-column vectors.
+struct Chunk {
+    int64_t c0;
+    int nfull;    // whole vectors
+    int nv;       // vectors including a partial one at column K
+    int tail_m;   // valid columns of the partial vector (0 if none)
+};
+
+__device__ __forceinline__ Chunk chunk_at(int64_t c0, int64_t k1, int64_t kchunk, int64_t K) {
+    Chunk c;
+    const int64_t c1 = (c0 + kchunk < k1) ? c0 + kchunk : k1;
+    c.c0 = c0;
+    c.nfull = static_cast<int>((c1 - c0) >> 3);
+    const bool tailv = (c1 == K) && ((K & 7) != 0);
+    c.nv = c.nfull + (tailv ? 1 : 0);
+    c.tail_m = tailv ? static_cast<int>(K - (c0 + 8 * static_cast<int64_t>(c.nfull))) : 0;
+    return c;
+}
+
+// Where warp kq of a row group puts its partial sum of (row_local, b): rows
+// of B + 1 floats, so that the lanes of a warp writing neighbouring rows do
+// not fall on the same shared-memory bank.
+__device__ __forceinline__ int red_index(int kq, int rows_per_cta, int row_local, int B, int b) {
+    return (kq * rows_per_cta + row_local) * (B + 1) + b;
+}
+
+// After every warp has written its partial sums with red_index: sum them over
+// kq in order, then (with a cluster along K) over the CTAs of the cluster in
+// rank order, and store each output once.
+__device__ __forceinline__ void combine_and_store(const float* red, float* cpart, int rows_per_cta, int B,
+                                                  int kw, int S, int split, int64_t n_base, int64_t N,
+                                                  float* __restrict__ y) {
+    __syncthreads();
+    const int nout = rows_per_cta * B;   // index i = row_local * B + b
+    for (int i = threadIdx.x; i < nout; i += kThreads) {
+        const int rl = i / B, b = i - (i / B) * B;
+        float s = red[red_index(0, rows_per_cta, rl, B, b)];
+        for (int q = 1; q < kw; ++q) s += red[red_index(q, rows_per_cta, rl, B, b)];
+        if (S == 1) {
+            const int64_t n = n_base + i / B;
+            if (n < N) y[static_cast<int64_t>(i % B) * N + n] = s;
+        } else {
+            cpart[i] = s;
+        }
+    }
+    if (S > 1) {
+        cluster_sync_all();   // every CTA of the cluster has its partials in shared memory
+        for (int i = threadIdx.x; i < nout; i += kThreads) {
+            if (i % S != split) continue;   // outputs are shared out over the ranks
+            float s = ld_dsmem(&cpart[i], 0);
+            for (int q = 1; q < S; ++q) s += ld_dsmem(&cpart[i], static_cast<uint32_t>(q));
+            const int64_t n = n_base + i / B;
+            if (n < N) y[static_cast<int64_t>(i % B) * N + n] = s;
+        }
+        cluster_sync_all();   // no CTA leaves while another still reads its shared memory
+    }
+}
+
+// Segment of a (possibly fused) launch that owns row tile `tile`.
+struct SegView {
+    const uint16_t* W;
+    float* y;
+    int64_t N;
+    int64_t ldw;
+    int64_t tile_local;
+};
+
+__device__ __forceinline__ SegView segment_of(const Params& p, int64_t tile) {
+    int si = 0;
+#pragma unroll 1
+    for (int i = 1; i < p.nseg; ++i)
+        if (tile >= p.seg[i].tile_begin) si = i;
+    SegView s;
+    s.W = p.seg[si].W;
+    s.y = p.seg[si].y;
+    s.N = p.seg[si].N;
+    s.ldw = p.seg[si].ldw;
+    s.tile_local = tile - p.seg[si].tile_begin;
+    return s;
+}
+
+// Launch a kernel with the plan's grid, cluster (when K is split over CTAs)
+// and programmatic dependent launch.
+template <typename KernelT>
+cudaError_t launch_kernel(KernelT kernel, const Params& p, const Launch& l, cudaStream_t s, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(l.grid), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(l.smem_bytes);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (l.splits > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = static_cast<unsigned>(l.splits);
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+}  // namespace gemv

@@ -6,29 +6,24 @@
 
 namespace gemv {
 
-cudaError_t launch_gemv_b1_4(int B, const Params& p, const Launch& l, cudaStream_t s, bool pdl);
-cudaError_t launch_gemv_b5_8(int B, const Params& p, const Launch& l, cudaStream_t s, bool pdl);
-cudaError_t launch_gemv_b9_12(int B, const Params& p, const Launch& l, cudaStream_t s, bool pdl);
-cudaError_t launch_gemv_b13_16(int B, const Params& p, const Launch& l, cudaStream_t s, bool pdl);
-cudaError_t prepare_b1_4();
-cudaError_t prepare_b5_8();
-cudaError_t prepare_b9_12();
-cudaError_t prepare_b13_16();
+cudaError_t launch_fma_batch(int B, const Params& p, const Launch& l, cudaStream_t s, bool pdl);
+cudaError_t prepare_fma_all();
+cudaError_t launch_mma_nb1(const Params& p, const Launch& l, cudaStream_t s, bool pdl);
+cudaError_t launch_mma_nb2(const Params& p, const Launch& l, cudaStream_t s, bool pdl);
+cudaError_t prepare_mma_nb1();
+cudaError_t prepare_mma_nb2();
 
 cudaError_t launch_gemv(int B, const Params& p, const Launch& l, cudaStream_t s, bool pdl) {
-    if (B >= 1 && B <= 4) return launch_gemv_b1_4(B, p, l, s, pdl);
-    if (B >= 5 && B <= 8) return launch_gemv_b5_8(B, p, l, s, pdl);
-    if (B >= 9 && B <= 12) return launch_gemv_b9_12(B, p, l, s, pdl);
-    if (B >= 13 && B <= 16) return launch_gemv_b13_16(B, p, l, s, pdl);
-    return cudaErrorInvalidValue;
+    if (B < 1 || B > kMaxBatch) return cudaErrorInvalidValue;
+    if (l.path == kPathFma) return launch_fma_batch(B, p, l, s, pdl);
+    return mma_nblocks(B) == 1 ? launch_mma_nb1(p, l, s, pdl) : launch_mma_nb2(p, l, s, pdl);
 }
 
 cudaError_t prepare_kernels(int /*device: attributes apply to the current device*/) {
     cudaError_t e;
-    if ((e = prepare_b1_4()) != cudaSuccess) return e;
-    if ((e = prepare_b5_8()) != cudaSuccess) return e;
-    if ((e = prepare_b9_12()) != cudaSuccess) return e;
-    return prepare_b13_16();
+    if ((e = prepare_fma_all()) != cudaSuccess) return e;
+    if ((e = prepare_mma_nb1()) != cudaSuccess) return e;
+    return prepare_mma_nb2();
 }
 
 // Streams `nvec` 16-byte vectors with the GEMV's load form, 8 independent loads

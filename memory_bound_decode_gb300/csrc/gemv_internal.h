@@ -12,7 +12,6 @@ constexpr int kThreads = kWarps * 32;     // threads per CTA
 constexpr int kMaxSegs = 8;               // segments of one fused launch
 constexpr int kMaxBatch = 16;
 constexpr int kMaxSplits = 8;             // CTAs along K: one portable cluster
-constexpr int kStepCols = 256;            // columns one warp covers per 16-byte load
 
 // One weight matrix of a launch. Row tiles of all segments are numbered
 // consecutively; tile_begin is the first tile of this segment.
@@ -29,23 +28,38 @@ struct Params {
     Seg seg[kMaxSegs];
     const uint16_t* x;
     int64_t K;
-    int64_t kslice;   // columns per K-split (multiple of 256)
-    int64_t kchunk;   // columns of x staged in shared memory at a time (multiple of 256)
+    int64_t kslice;   // columns per K-split (multiple of the warp batch width)
+    int64_t kchunk;   // columns of x staged in shared memory at a time
     int32_t nseg;
     int32_t splits;   // CTAs per row tile along K (== cluster size when > 1)
     int32_t kw;       // warps of one CTA that share a row group along K (1, 2, 4, 8)
-    int32_t xstride;  // shared-memory elements per staged x row (== kchunk)
+    int32_t xstride;  // shared-memory elements per staged x row (>= kchunk)
+    int32_t batch;    // B
+    int32_t nbuf;     // x buffers (2 when the K-range takes more than one chunk)
 };
 
-// Compile-time shape of the kernel instance for batch B.
+// Kernel families.
+enum Path : int32_t {
+    kPathFma = 0,   // CUDA-core FP32 multiply-adds, one warp streams RPW whole rows
+    kPathMma = 1,   // BF16 tensor-core mma.sync, one warp streams a 16-row tile
+};
+
+// Compile-time shape of the CUDA-core kernel instance for batch B.
 struct Variant {
     int rows_per_warp;   // rows one warp streams at once
     int unroll;          // 16-byte loads per lane per row issued before any is used
 };
 
-constexpr Variant variant_for(int B) {
-    return B <= 2 ? Variant{1, 8} : (B <= 8 ? Variant{2, 4} : Variant{2, 2});
-}
+constexpr Variant fma_variant(int B) { return B <= 1 ? Variant{1, 8} : Variant{1, 8}; }
+
+// The tensor-core kernel: 16-row tile per warp, n8 blocks of the batch, and
+// k32 blocks (two 16-byte loads per lane each) in flight per batch.
+constexpr int kMmaRows = 16;
+constexpr int kMmaUnroll = 8;
+constexpr int mma_nblocks(int B) { return B <= 8 ? 1 : 2; }
+
+// Which family serves batch B.
+constexpr Path path_for(int B) { return B == 1 ? kPathFma : kPathMma; }
 
 // Host-side launch decision (see planner.cpp).
 struct Launch {
@@ -56,21 +70,21 @@ struct Launch {
     int64_t kchunk;
     int32_t kw;
     int32_t splits;
-    int32_t rows_per_warp;
+    int32_t rows_per_warp;   // rows of one warp's group (RPW, or 16 for the tensor-core path)
     int32_t unroll;
     int32_t smem_bytes;
+    int32_t path;
+    int32_t xstride;
+    int32_t nbuf;
 };
 
 // Returns 0 and fills `out`, or a negative GEMV_ERR_* code.
 int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out);
 
-// Dynamic shared memory the kernel needs for a launch.
-int32_t smem_bytes_for(int B, int64_t kchunk, int64_t rows_per_cta, int kw);
-
 // Largest dynamic shared memory any plan requests (set as the kernel attribute).
-constexpr int32_t kMaxDynSmem = 96 * 1024;
+constexpr int32_t kMaxDynSmem = 112 * 1024;
 
-// Kernel launchers (one per batch size), defined in the kernel translation units.
+// Kernel launchers, defined in the kernel translation units.
 cudaError_t launch_gemv(int B, const Params& p, const Launch& l, cudaStream_t s, bool pdl);
 cudaError_t prepare_kernels(int device);   // per-device function attributes
 cudaError_t launch_probe_read(const void* src, int64_t bytes, float* sink, int grid,

@@ -1,0 +1,12 @@
+// Tensor-core kernel instance for batches of up to 8 rows.
+#include "gemv_mma_kernel.cuh"
+
+namespace gemv {
+
+cudaError_t launch_mma_nb1(const Params& p, const Launch& l, cudaStream_t s, bool pdl) {
+    return launch_mma<1>(p, l, s, pdl);
+}
+
+cudaError_t prepare_mma_nb1() { return prepare_mma<1>(); }
+
+}  // namespace gemv

@@ -1,0 +1,265 @@
+// Skinny-batch decode GEMV on the BF16 tensor cores (mma.sync m16n8k16, FP32
+// accumulate) for sm_103a: y[b][n] = sum_k W[n][k] * x[b][k] with 2 <= B <= 16.
+//
+// Why tensor cores here: at batch B every weight element feeds B multiply-adds.
+// On the CUDA cores that, plus the BF16 widening and the shared-memory x reads,
+// costs more issue slots than the byte stream leaves for B >= 4, so the kernel
+// would run at the ALU roof, not the HBM roof ("Decode GEMV at half of HBM
+// bandwidth", "What interviewers probe next": at batch 16 the operation is a
+// skinny GEMM and tensor cores become worth using for the arithmetic). The
+// contraction over k is done by the tensor cores; W still streams straight
+// from HBM into registers with 16-byte loads and is never staged.
+//
+// Layout. A warp owns a 16-row tile of W. Lane (g, t) = (lane / 4, lane % 4)
+// loads, per 32-column block j, the 16-byte vectors W[row g][32j + 8t .. +7]
+// and W[row g + 8][same columns]; the 4 lanes of a row read 64 contiguous
+// bytes, whole sectors, and UJ blocks per batch are in flight per lane before
+// any is used. Those two vectors ARE the A fragments of two m16n8k16 MMAs
+// under a fixed permutation of k: the MMA's k-slots {2t, 2t+1, 2t+8, 2t+9}
+// map to physical columns {8t, 8t+1, 8t+2, 8t+3} in the first MMA and
+// {8t+4, .., 8t+7} in the second. The B fragments (x, k x batch) use the same
+// permutation, so one 16-byte shared-memory read of x[b][32j + 8t .. +7]
+// feeds both MMAs; any permutation of k applied to both operands leaves the
+// dot products unchanged. Batch rows b >= B enter as zeros.
+//
+// Accumulation: the 2*UJ MMAs of a batch accumulate into two fresh FP32 tiles
+// (even and odd blocks), which are then added to the running tile (blocked
+// summation), and the usual
+// fixed-order combine over warps and cluster CTAs follows. x staging, the
+// programmatic dependent launch and the split-K cluster are those of the
+// CUDA-core kernel.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "gemv_common.cuh"
+
+namespace gemv {
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// This warp's contiguous range of 32-column blocks within a chunk.
+struct MmaRange {
+    int j_begin;
+    int my_blocks;
+};
+
+__device__ __forceinline__ MmaRange mma_range(const Chunk& c, int kw, int kq) {
+    const int nblk = (c.nv + 3) >> 2;
+    const int span = (nblk + kw - 1) / kw;
+    MmaRange r;
+    r.j_begin = kq * span;
+    const int j_end = (r.j_begin + span < nblk) ? r.j_begin + span : nblk;
+    r.my_blocks = j_end > r.j_begin ? j_end - r.j_begin : 0;
+    return r;
+}
+
+// Issue one batch: UJ 32-column blocks, two 16-byte W loads (rows g and g+8)
+// per block per lane. `v` is the lane's vector index for block u = 0.
+template <int UJ, bool PRED>
+__device__ __forceinline__ void mma_issue(uint4 (&w0)[UJ], uint4 (&w1)[UJ], bool (&ok)[UJ],
+                                          const uint16_t* p0, const uint16_t* p1, int v,
+                                          int blocks_left, const Chunk& c) {
+#pragma unroll
+    for (int u = 0; u < UJ; ++u) {
+        const int vu = v + 4 * u;
+        ok[u] = PRED ? (u < blocks_left && vu < c.nv) : true;
+        uint4 a = make_uint4(0u, 0u, 0u, 0u);
+        uint4 b = make_uint4(0u, 0u, 0u, 0u);
+        if (ok[u]) {
+            a = ld_stream16(p0 + 32 * u);
+            b = ld_stream16(p1 + 32 * u);
+            if (PRED && vu == c.nfull && c.tail_m != 0) {
+                a = keep_first(a, c.tail_m);
+                b = keep_first(b, c.tail_m);
+            }
+        }
+        w0[u] = a;
+        w1[u] = b;
+    }
+}
+
+template <int NB, bool PRED>
+__device__ __forceinline__ void load_xfrag(uint4 (&xr)[NB], bool ok, const uint16_t* xrow0, int xstride,
+                                           int vu, int g, int B) {
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        xr[nb] = make_uint4(0u, 0u, 0u, 0u);
+        if ((nb * 8 + g < B) && (!PRED || ok))
+            xr[nb] = *reinterpret_cast<const uint4*>(xrow0 + nb * 8 * xstride + 8 * vu);
+    }
+}
+
+// Tensor-core multiply-adds of one batch. The x fragments of block u+1 are
+// read from shared memory while block u's MMAs run, and even and odd blocks
+// accumulate into separate tiles, so neither the shared-memory latency nor
+// the MMA latency is exposed block after block.
+template <int NB, int UJ, bool PRED>
+__device__ __forceinline__ void mma_consume(float (&acc)[NB][4], const uint4 (&w0)[UJ], const uint4 (&w1)[UJ],
+                                            const bool (&ok)[UJ], const uint16_t* xrow0, int xstride,
+                                            int v, int g, int B) {
+    float t[2][NB][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) t[h][nb][i] = 0.f;
+    uint4 xr[NB];
+    load_xfrag<NB, PRED>(xr, ok[0], xrow0, xstride, v, g, B);
+#pragma unroll
+    for (int u = 0; u < UJ; ++u) {
+        uint4 xn[NB];
+        if (u + 1 < UJ) load_xfrag<NB, PRED>(xn, ok[u + 1 < UJ ? u + 1 : u], xrow0, xstride, v + 4 * (u + 1), g, B);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            mma_bf16_16816(t[u & 1][nb], w0[u].x, w1[u].x, w0[u].y, w1[u].y, xr[nb].x, xr[nb].y);
+            mma_bf16_16816(t[u & 1][nb], w0[u].z, w1[u].z, w0[u].w, w1[u].w, xr[nb].z, xr[nb].w);
+        }
+        if (u + 1 < UJ) {
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) xr[nb] = xn[nb];
+        }
+    }
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nb][i] += t[0][nb][i] + t[1][nb][i];
+}
+
+template <int NB, int UJ>
+__global__ void __launch_bounds__(kThreads)
+gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+
+    pdl_launch_dependents();
+
+    const int S = p.splits;
+    const int64_t tile = blockIdx.x / S;
+    const int split = (S > 1) ? static_cast<int>(cluster_rank()) : 0;
+    const SegView sg = segment_of(p, tile);
+
+    const int B = p.batch;
+    const int kw = p.kw;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int gw = warp / kw;        // 16-row tile of this warp within the CTA
+    const int kq = warp - gw * kw;   // position of this warp along K within the tile
+    const int g = lane >> 2;
+    const int t = lane & 3;
+    const int rows_per_cta = (kWarps / kw) * kMmaRows;
+    const int64_t tile_row0 = sg.tile_local * rows_per_cta + static_cast<int64_t>(gw) * kMmaRows;
+    int64_t n0 = tile_row0 + g, n1 = tile_row0 + g + 8;
+    n0 = n0 < sg.N ? n0 : sg.N - 1;   // rows past N stream a valid row; results dropped
+    n1 = n1 < sg.N ? n1 : sg.N - 1;
+    const uint16_t* w0row = sg.W + n0 * sg.ldw;
+    const uint16_t* w1row = sg.W + n1 * sg.ldw;
+
+    const int xstride = p.xstride;
+    const int xbuf = B * xstride;
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem_raw);
+    float* red = reinterpret_cast<float*>(smem_raw + static_cast<size_t>(p.nbuf) * xbuf * 2);
+    float* cpart = red + rows_per_cta * (B + 1) * kw;
+
+    const int64_t K = p.K;
+    const int64_t k0 = static_cast<int64_t>(split) * p.kslice;
+    const int64_t k1 = (k0 + p.kslice < K) ? k0 + p.kslice : K;
+
+    float acc[NB][4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nb][i] = 0.f;
+
+    uint4 w0[UJ], w1[UJ];
+    bool ok[UJ];
+
+    Chunk ch = chunk_at(k0, k1, p.kchunk, K);
+    MmaRange rg = mma_range(ch, kw, kq);
+    int v = 4 * rg.j_begin + t;   // this lane's vector index in the chunk
+    const uint16_t* p0 = w0row + ch.c0 + 8 * static_cast<int64_t>(v);
+    const uint16_t* p1 = w1row + ch.c0 + 8 * static_cast<int64_t>(v);
+    mma_issue<UJ, true>(w0, w1, ok, p0, p1, v, rg.my_blocks, ch);
+    pdl_wait_prerequisites();
+    stage_x(xs, xstride, p.x, B, K, ch.c0, ch.nv);
+
+#pragma unroll 1
+    for (int c = 0;; ++c) {
+        const uint16_t* xrow0 = xs + (c & 1) * xbuf + g * xstride;
+        const int64_t next_c0 = ch.c0 + p.kchunk;
+        const bool more = next_c0 < k1;
+        Chunk nch{};
+        if (more) {
+            nch = chunk_at(next_c0, k1, p.kchunk, K);
+            stage_x(xs + ((c + 1) & 1) * xbuf, xstride, p.x, B, K, nch.c0, nch.nv);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+
+        mma_consume<NB, UJ, true>(acc, w0, w1, ok, xrow0, xstride, v, g, B);
+        int j = UJ;
+        auto advance = [&]() {
+            p0 += 32 * UJ;
+            p1 += 32 * UJ;
+            v += 4 * UJ;
+        };
+        advance();
+#pragma unroll 1
+        for (; j + UJ <= rg.my_blocks && (v - t) + 4 * UJ <= ch.nfull; j += UJ) {
+            mma_issue<UJ, false>(w0, w1, ok, p0, p1, v, UJ, ch);
+            mma_consume<NB, UJ, false>(acc, w0, w1, ok, xrow0, xstride, v, g, B);
+            advance();
+        }
+#pragma unroll 1
+        for (; j < rg.my_blocks; j += UJ) {
+            mma_issue<UJ, true>(w0, w1, ok, p0, p1, v, rg.my_blocks - j, ch);
+            mma_consume<NB, UJ, true>(acc, w0, w1, ok, xrow0, xstride, v, g, B);
+            advance();
+        }
+        if (!more) break;
+
+        ch = nch;
+        rg = mma_range(ch, kw, kq);
+        v = 4 * rg.j_begin + t;
+        p0 = w0row + ch.c0 + 8 * static_cast<int64_t>(v);
+        p1 = w1row + ch.c0 + 8 * static_cast<int64_t>(v);
+        mma_issue<UJ, true>(w0, w1, ok, p0, p1, v, rg.my_blocks, ch);
+        __syncthreads();
+    }
+
+    // acc[nb] holds D[row g][b], D[row g][b+1], D[row g+8][b], D[row g+8][b+1]
+    // with b = 8*nb + 2t.
+    const int rl0 = gw * kMmaRows + g;
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int b = nb * 8 + 2 * t + (i & 1);
+            const int rl = rl0 + ((i & 2) ? 8 : 0);
+            if (b < B) red[red_index(kq, rows_per_cta, rl, B, b)] = acc[nb][i];
+        }
+    }
+    combine_and_store(red, cpart, rows_per_cta, B, kw, S, split, sg.tile_local * rows_per_cta, sg.N, sg.y);
+}
+
+template <int NB>
+cudaError_t launch_mma(const Params& p, const Launch& l, cudaStream_t s, bool pdl) {
+    return launch_kernel(gemv_bf16_mma_kernel<NB, kMmaUnroll>, p, l, s, pdl);
+}
+
+template <int NB>
+cudaError_t prepare_mma() {
+    return cudaFuncSetAttribute(gemv_bf16_mma_kernel<NB, kMmaUnroll>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+}
+
+}  // namespace gemv

@@ -114,15 +114,21 @@ def test_plan_covers_the_problem(L, N, K, B):
     assert q["warps_per_cta"] * 32 == 256
     assert q["warps_per_row"] in (1, 2, 4, 8)
     assert 1 <= q["splits"] <= 8
+    # batch 1 on the CUDA cores, batches 2..16 on the BF16 tensor cores (16-row tiles)
+    assert q["path"] == (0 if B == 1 else 1)
+    assert q["rows_per_warp"] == (1 if B == 1 else 16)
     assert q["rows_per_cta"] == (8 // q["warps_per_row"]) * q["rows_per_warp"]
     assert q["row_tiles"] * q["rows_per_cta"] >= N > (q["row_tiles"] - 1) * q["rows_per_cta"]
     assert q["grid"] == q["row_tiles"] * q["splits"]
-    # K-slices are whole 256-column warp-steps, cover K, and none is empty
+    # K-slices are whole 256-column steps, cover K, and none is empty
     assert q["kslice"] % 256 == 0 and q["kchunk"] % 256 == 0
     assert q["splits"] * q["kslice"] >= K > (q["splits"] - 1) * q["kslice"]
     assert q["kchunk"] <= q["kslice"]
-    assert B * q["kchunk"] * 2 <= 40 * 1024 or q["kchunk"] == 256
-    assert q["smem_bytes"] <= 96 * 1024
+    # x fits its budget, double-buffered exactly when the slice takes several chunks
+    assert q["xstride"] >= q["kchunk"]
+    assert q["nbuf"] == (1 if q["kchunk"] == q["kslice"] else 2)
+    assert q["nbuf"] * B * q["xstride"] * 2 <= 80 * 1024 or q["kchunk"] == 256
+    assert q["smem_bytes"] <= 112 * 1024
 
 
 def test_no_split_when_rows_fill_the_gpu(L):
