@@ -76,6 +76,17 @@ int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out) {
         while (splits < kMaxSplits && warps_for(kw, splits) < target_warps && room(kw, splits)) splits *= 2;
     }
 
+    // On the tensor-core path, trade warps along K for CTAs along K while the
+    // CTA's x slice does not fit in one staged chunk (same warps, fewer x bytes
+    // per CTA, no chunk barriers).
+    if (cluster_first) {
+        while (splits < kMaxSplits && kw > 1 &&
+               static_cast<int64_t>(B) * (cdiv(K, splits) + xpad) * 2 > kXBudgetBytes) {
+            splits *= 2;
+            kw /= 2;
+        }
+    }
+
     // Slices are whole multiples of the grain; recount so that no slice is empty.
     int64_t kslice = round_up(cdiv(K, splits), kSliceGrain);
     splits = static_cast<int>(cdiv(K, kslice));
