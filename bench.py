@@ -81,7 +81,8 @@ def kernel_source_hash() -> str:
 def profiled_traffic(workload: str, src_hash: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary for this workload, if it was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", f"gemv_{workload}.md")
+    safe = re.sub(r"[^A-Za-z0-9_]+", "_", workload)
+    path = os.path.join(ROOT, "profiles", f"gemv_{safe}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -364,7 +365,8 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_kind": f"{peak_kind} copy (MEASURED_PEAKS hbm_gbs, burst)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "kernel": "gemv_bf16_kernel", "kernel_source_hash": src_hash},
+                     "kernel": "gemv_bf16_kernel (CUDA cores)" if wk.B == 1 else "gemv_bf16_mma_kernel (BF16 tensor cores)",
+                     "kernel_source_hash": src_hash},
         "ceilings": {"copy_gbs": peak,
                      "read_probe_gbs": round(read_ceiling, 1) if read_ceiling else None,
                      "vendor_gbs": VENDOR_HBM_GBS,

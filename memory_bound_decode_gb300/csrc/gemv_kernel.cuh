@@ -106,7 +106,10 @@ __device__ __forceinline__ FmaRange fma_range(const Chunk& c, int kw, int kq) {
     return r;
 }
 
-template <int B, int RPW, int UJ>
+// CHUNKED: the CTA's K-range is staged in several double-buffered chunks;
+// otherwise it is one chunk and the chunk loop runs once (a separate, leaner
+// instance, since the common large projections need no chunking).
+template <int B, int RPW, int UJ, bool CHUNKED>
 __global__ void __launch_bounds__(kThreads)
 gemv_bf16_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -171,7 +174,7 @@ gemv_bf16_kernel(const __grid_constant__ Params p) {
     for (int c = 0;; ++c) {
         const uint16_t* xcur = xs + (c & 1) * xbuf;
         const int64_t next_c0 = ch.c0 + p.kchunk;
-        const bool more = next_c0 < k1;
+        const bool more = CHUNKED && next_c0 < k1;
         Chunk nch{};
         if (more) {   // copy the next chunk of x while this one is used
             nch = chunk_at(next_c0, k1, p.kchunk, K);
@@ -241,13 +244,17 @@ gemv_bf16_kernel(const __grid_constant__ Params p) {
 template <int B>
 cudaError_t launch_fma(const Params& p, const Launch& l, cudaStream_t s, bool pdl) {
     constexpr Variant v = fma_variant(B);
-    return launch_kernel(gemv_bf16_kernel<B, v.rows_per_warp, v.unroll>, p, l, s, pdl);
+    if (l.nbuf > 1) return launch_kernel(gemv_bf16_kernel<B, v.rows_per_warp, v.unroll, true>, p, l, s, pdl);
+    return launch_kernel(gemv_bf16_kernel<B, v.rows_per_warp, v.unroll, false>, p, l, s, pdl);
 }
 
 template <int B>
 cudaError_t prepare_fma() {
     constexpr Variant v = fma_variant(B);
-    return cudaFuncSetAttribute(gemv_bf16_kernel<B, v.rows_per_warp, v.unroll>,
+    cudaError_t e = cudaFuncSetAttribute(gemv_bf16_kernel<B, v.rows_per_warp, v.unroll, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(gemv_bf16_kernel<B, v.rows_per_warp, v.unroll, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
 }
 

@@ -134,7 +134,9 @@ __device__ __forceinline__ void mma_consume(float (&acc)[NB][4], const uint4 (&w
         for (int i = 0; i < 4; ++i) acc[nb][i] += t[0][nb][i] + t[1][nb][i];
 }
 
-template <int NB, int UJ>
+// CHUNKED: as for the CUDA-core kernel, a separate instance for K-ranges
+// staged in several chunks.
+template <int NB, int UJ, bool CHUNKED>
 __global__ void __launch_bounds__(kThreads)
 gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -194,7 +196,7 @@ gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
     for (int c = 0;; ++c) {
         const uint16_t* xrow0 = xs + (c & 1) * xbuf + g * xstride;
         const int64_t next_c0 = ch.c0 + p.kchunk;
-        const bool more = next_c0 < k1;
+        const bool more = CHUNKED && next_c0 < k1;
         Chunk nch{};
         if (more) {
             nch = chunk_at(next_c0, k1, p.kchunk, K);
@@ -253,12 +255,16 @@ gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
 
 template <int NB>
 cudaError_t launch_mma(const Params& p, const Launch& l, cudaStream_t s, bool pdl) {
-    return launch_kernel(gemv_bf16_mma_kernel<NB, kMmaUnroll>, p, l, s, pdl);
+    if (l.nbuf > 1) return launch_kernel(gemv_bf16_mma_kernel<NB, kMmaUnroll, true>, p, l, s, pdl);
+    return launch_kernel(gemv_bf16_mma_kernel<NB, kMmaUnroll, false>, p, l, s, pdl);
 }
 
 template <int NB>
 cudaError_t prepare_mma() {
-    return cudaFuncSetAttribute(gemv_bf16_mma_kernel<NB, kMmaUnroll>,
+    cudaError_t e = cudaFuncSetAttribute(gemv_bf16_mma_kernel<NB, kMmaUnroll, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(gemv_bf16_mma_kernel<NB, kMmaUnroll, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
 }
 
