@@ -1,2 +1,3 @@
 """CPU oracle for the decode GEMV (test infrastructure only; see oracle.py)."""
-from .oracle import RTOL, accept, build, default_threads, gemv, gemv_one, load  # noqa: F401
+from .oracle import (RTOL, accept, build, default_threads, gemv, gemv_one,  # noqa: F401
+                     gemv_rmsnorm, load)

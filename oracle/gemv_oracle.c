@@ -30,6 +30,7 @@
  * double is exact as well.
  */
 #include <stdint.h>
+#include <math.h>
 #include <string.h>
 
 static double bf16_to_double(uint16_t h)
@@ -93,5 +94,43 @@ int oracle_gemv_f64_one(const uint16_t *W, const uint16_t *x,
     }
     *y_out = acc;
     *s_out = mag;
+    return 0;
+}
+
+/*
+ * The GEMV with an RMSNorm prologue on x ("GPU performance chains", "Fused
+ * RMSNorm traffic": at decode the norm's launches, not its bytes, are the cost,
+ * so it is fused into the projection that reads x). RMSNorm scales each
+ * activation row by r_b = (mean_k x[b][k]^2 + eps)^(-1/2); its elementwise
+ * weight is taken as already folded into W's columns, so
+ *
+ *     y[b][n] = r_b * sum_k W[n][k] * x[b][k]
+ *     s[b][n] = r_b * sum_k |W[n][k] * x[b][k]|   (the tolerance scale)
+ *     r[b]    = r_b
+ *
+ * for rows [n0, n1). FP64 throughout; the mean divides by K. Returns 0, or -1
+ * on a bad argument (eps < 0 included).
+ */
+int oracle_gemv_rmsnorm_f64(const uint16_t *W, const uint16_t *x,
+                            int64_t N, int64_t K, int64_t B, int64_t ldw, double eps,
+                            int64_t n0, int64_t n1, double *y, double *s, double *r)
+{
+    if (!r || !(eps >= 0.0)) return -1;
+    int rc = oracle_gemv_f64(W, x, N, K, B, ldw, n0, n1, y, s);
+    if (rc != 0) return rc;
+    for (int64_t b = 0; b < B; ++b) {
+        const uint16_t *xb = x + b * K;
+        double sq = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double v = bf16_to_double(xb[k]);
+            sq += v * v;
+        }
+        double rb = 1.0 / sqrt(sq / (double)K + eps);
+        r[b] = rb;
+        for (int64_t n = n0; n < n1; ++n) {
+            y[b * N + n] *= rb;
+            s[b * N + n] *= rb;
+        }
+    }
     return 0;
 }

@@ -56,7 +56,7 @@ def build(source: str = SOURCE, out: str | None = None, force: bool = False) -> 
         return out
     tmp = f"{out}.{os.getpid()}.tmp"
     cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
-           "-shared", "-fPIC", "-o", tmp, source]
+           "-shared", "-fPIC", "-o", tmp, source, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out
@@ -76,6 +76,9 @@ class OracleLib:
         g = self._lib.oracle_gemv_f64_one
         g.restype = ctypes.c_int
         g.argtypes = [vp, vp, i64, i64, i64, i64, i64, i64, vp, vp]
+        h = self._lib.oracle_gemv_rmsnorm_f64
+        h.restype = ctypes.c_int
+        h.argtypes = [vp, vp, i64, i64, i64, i64, ctypes.c_double, i64, i64, vp, vp, vp]
 
     def gemv(self, W: np.ndarray, x: np.ndarray, K: int | None = None,
              threads: int | None = None) -> tuple[np.ndarray, np.ndarray]:
@@ -102,6 +105,35 @@ class OracleLib:
         if any(rc != 0 for rc in rcs):
             raise ValueError("oracle rejected its arguments")
         return y, s
+
+    def gemv_rmsnorm(self, W: np.ndarray, x: np.ndarray, eps: float, K: int | None = None,
+                     threads: int | None = None) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+        """Return (y_ref, scale, r): the GEMV of the RMS-normalised x.
+
+        r[b] = (mean_k x[b][k]^2 + eps)^(-1/2); y_ref and scale as for gemv, times r[b].
+        """
+        W, x, N, K, B, ldw = _check(W, x, K)
+        y = np.empty((B, N), dtype=np.float64)
+        s = np.empty((B, N), dtype=np.float64)
+        r = np.empty((B,), dtype=np.float64)
+        threads = max(1, min(threads or 1, N))
+        bounds = np.linspace(0, N, threads + 1).astype(np.int64)
+        rs = [np.empty((B,), dtype=np.float64) for _ in range(threads)]
+
+        def run(i: int) -> int:
+            return self._lib.oracle_gemv_rmsnorm_f64(
+                W.ctypes.data, x.ctypes.data, N, K, B, ldw, float(eps),
+                int(bounds[i]), int(bounds[i + 1]), y.ctypes.data, s.ctypes.data, rs[i].ctypes.data)
+
+        if threads == 1:
+            rcs = [run(0)]
+        else:
+            with ThreadPoolExecutor(max_workers=threads) as ex:
+                rcs = list(ex.map(run, range(threads)))
+        if any(rc != 0 for rc in rcs):
+            raise ValueError("oracle rejected its arguments")
+        r[:] = rs[0]
+        return y, s, r
 
     def gemv_one(self, W: np.ndarray, x: np.ndarray, b: int, n: int,
                  K: int | None = None) -> tuple[float, float]:
@@ -146,6 +178,11 @@ def load(path: str | None = None) -> OracleLib:
 def gemv(W: np.ndarray, x: np.ndarray, K: int | None = None,
          threads: int | None = None) -> tuple[np.ndarray, np.ndarray]:
     return load().gemv(W, x, K, threads)
+
+
+def gemv_rmsnorm(W: np.ndarray, x: np.ndarray, eps: float, K: int | None = None,
+                 threads: int | None = None):
+    return load().gemv_rmsnorm(W, x, eps, K, threads)
 
 
 def gemv_one(W: np.ndarray, x: np.ndarray, b: int, n: int, K: int | None = None):

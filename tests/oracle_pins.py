@@ -179,9 +179,54 @@ def single_element(lib):
         assert yo == y[b, n] and so == s[b, n]
 
 
+def rms_constant_x(lib):
+    N, K, ldw = 6, 40, 48
+    W = inputs.bits(inputs.int_weight(N, K, ldw, lo=-5, hi=5, seed=21))
+    Wd = _decode(W[:, :K])
+    for c_bits, c in [(0x3F00, 0.5), (0xC040, -3.0)]:
+        x = np.full((2, K), c_bits, dtype=np.uint16)
+        for eps in (0.0, 1e-5, 0.25):
+            y, sc, r = lib.gemv_rmsnorm(W, x, eps)
+            r_want = 1.0 / np.sqrt(c * c + eps)
+            assert np.allclose(r, r_want, rtol=1e-15, atol=0), (c, eps, r)
+            want = r_want * c * Wd.sum(axis=1)
+            assert np.allclose(y[0], want, rtol=1e-14, atol=0) and np.array_equal(y[0], y[1])
+            assert np.allclose(sc[0], r_want * abs(c) * np.abs(Wd).sum(axis=1), rtol=1e-14, atol=0)
+
+
+def rms_scale_free(lib):
+    N, K, ldw, B = 7, 129, 136, 3
+    W, x = _rand_case(N, K, B, ldw, seed=22)
+    x4 = inputs.bits(inputs.from_bits(x).float().mul(4.0).to(torch.bfloat16))
+    y1, s1, r1 = lib.gemv_rmsnorm(W, x, 0.0)
+    y4, s4, r4 = lib.gemv_rmsnorm(W, x4, 0.0)
+    assert np.array_equal(y1, y4) and np.array_equal(s1, s4)
+    assert np.array_equal(r4 * 4.0, r1)
+
+
+def rms_independent(lib):
+    N, K, ldw, B = 33, 1000, 1008, 4
+    W, x = _rand_case(N, K, B, ldw, seed=23)
+    eps = 1e-6
+    y0, s0 = lib.gemv(W, x)
+    y, sc, r = lib.gemv_rmsnorm(W, x, eps)
+    xd = _decode(x)
+    r_np = 1.0 / np.sqrt(np.mean(xd * xd, axis=1) + eps)
+    assert np.allclose(r, r_np, rtol=1e-13, atol=0)
+    assert np.allclose(y, y0 * r_np[:, None], rtol=1e-12, atol=1e-300)
+    assert np.allclose(sc, s0 * r_np[:, None], rtol=1e-12, atol=0)
+    try:
+        lib.gemv_rmsnorm(W, x, -1.0)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("negative eps accepted")
+
+
 ALL_PINS = [exact_rational, integer_matmul, ones_row_sums, one_hot_column,
             identity_padded, scaling_exact, linearity, row_permutation,
-            batch_rows, padding_unread, float64_matmul, single_element]
+            batch_rows, padding_unread, float64_matmul, single_element,
+            rms_constant_x, rms_scale_free, rms_independent]
 
 
 def failures(lib) -> list[str]:

@@ -33,6 +33,12 @@ MUTATIONS = {
                         "float acc = 0.0f;\n            double mag = 0.0;\n            for (int64_t k = 0; k < K; ++k) {\n                double term"),
     "operand_swap_W_for_x": ("bf16_to_double(wn[k]) * bf16_to_double(xb[k]);\n                acc",
                              "bf16_to_double(wn[k]) * bf16_to_double(wn[k]);\n                acc"),
+    "rms_no_eps": ("1.0 / sqrt(sq / (double)K + eps)", "1.0 / sqrt(sq / (double)K)"),
+    "rms_sum_not_mean": ("1.0 / sqrt(sq / (double)K + eps)", "1.0 / sqrt(sq + eps)"),
+    "rms_no_sqrt": ("1.0 / sqrt(sq / (double)K + eps)", "1.0 / (sq / (double)K + eps)"),
+    "rms_abs_not_square": ("            sq += v * v;", "            sq += v < 0.0 ? -v : v;"),
+    "rms_scale_unscaled": ("            s[b * N + n] *= rb;\n", ""),
+    "rms_mean_over_ldw": ("1.0 / sqrt(sq / (double)K + eps)", "1.0 / sqrt(sq / (double)ldw + eps)"),
 }
 
 
