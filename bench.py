@@ -154,9 +154,22 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- workloads
 
+RMS_EPS = 1e-5
+RMS_SUFFIX = "+rmsnorm"
+
+
+def split_norm(workload: str) -> tuple[str, float | None]:
+    """A workload name may end in "+rmsnorm": the same projections with the
+    RMSNorm prologue on x (eps 1e-5)."""
+    if workload.endswith(RMS_SUFFIX):
+        return workload[: -len(RMS_SUFFIX)], RMS_EPS
+    return workload, None
+
+
 def describe(workload: str):
     """(kind, N-list, K, B) of a named workload."""
     from memory_bound_decode_gb300 import workloads as wl
+    workload, _ = split_norm(workload)
     if workload in ("down_proj", "k_proj", "o_proj", "lm_head"):
         N, K = wl.SHAPES[workload]
         return "single", [N], K, 1
@@ -178,10 +191,11 @@ def describe(workload: str):
 class GemvWorkload:
     """Rotating device-resident weight copies for one (possibly fused) GEMV."""
 
-    def __init__(self, kind, rows, K, B, device, l2_bytes):
+    def __init__(self, kind, rows, K, B, device, l2_bytes, rms_eps=None):
         import torch
         from memory_bound_decode_gb300 import inputs, roofline
         self.kind, self.rows, self.K, self.B = kind, rows, K, B
+        self.rms_eps = rms_eps
         self.ldw = inputs.padded_ldw(K)
         self.N = sum(rows)
         self.bytes_per_step = roofline.algorithmic_bytes(self.N, K, B)
@@ -198,15 +212,22 @@ class GemvWorkload:
         from memory_bound_decode_gb300 import binding
         Ws = self.Ws[i % self.copies]
         x = self.x if x is None else x
-        if self.kind == "single":
+        if self.kind == "single" and self.rms_eps is None:
             binding.gemv_bf16(Ws[0], x, self.ys[0], self.N, self.K, self.B, self.ldw, stream)
-        else:
+        elif self.kind == "single":
+            binding.gemv_bf16_ex(Ws[0], x, self.ys[0], self.N, self.K, self.B, self.ldw,
+                                 rms_eps=self.rms_eps, stream=stream)
+        elif self.rms_eps is None:
             binding.gemv_bf16_multi([(W, y, n, self.ldw) for W, y, n in zip(Ws, self.ys, self.rows)],
                                     x, self.K, self.B, stream)
+        else:
+            binding.gemv_bf16_multi_ex([(W, y, n, self.ldw) for W, y, n in zip(Ws, self.ys, self.rows)],
+                                       x, self.K, self.B, rms_eps=self.rms_eps, stream=stream)
 
     def config(self) -> dict:
         shape = "+".join(str(n) for n in self.rows)
-        return {"workload": f"{self.kind} BF16 GEMV N={shape} K={self.K} B={self.B}",
+        norm = f", RMSNorm prologue eps={self.rms_eps}" if self.rms_eps is not None else ""
+        return {"workload": f"{self.kind} BF16 GEMV N={shape} K={self.K} B={self.B}{norm}",
                 "N": self.N, "K": self.K, "B": self.B, "ldw": self.ldw,
                 "segments": len(self.rows),
                 "l2": f"inputs larger than L2: {self.copies} rotating weight copies, "
@@ -216,11 +237,12 @@ class GemvWorkload:
 class StepWorkload:
     """The full decode-step projection set replayed as one CUDA graph."""
 
-    def __init__(self, device, stream):
+    def __init__(self, device, stream, rms_eps=None):
         from memory_bound_decode_gb300 import workloads as wl
         self.spec = wl.decode_step_spec()
         self.data = wl.DecodeStep(self.spec, seed=0, device=device)
-        self.plan = self.data.plan()
+        self.rms_eps = rms_eps
+        self.plan = self.data.plan(rms_eps=rms_eps)
         self.plan.capture(stream)
         self.bytes_per_step = wl.step_bytes_formula(self.spec)
         self.launches_per_step = self.plan.num_launches()
@@ -231,8 +253,10 @@ class StepWorkload:
         self.plan.launch(stream)
 
     def config(self) -> dict:
+        norm = (f"; RMSNorm prologue (eps={self.rms_eps}) on QKV, gate_up and lm_head"
+                if self.rms_eps is not None else "")
         return {"workload": "decode step: 32 x {QKV 6144x4096, o 4096x4096, gate_up 28672x4096, "
-                            "down 4096x14336} + lm_head 128256x4096, BF16, batch 1, one CUDA graph",
+                            "down 4096x14336} + lm_head 128256x4096, BF16, batch 1, one CUDA graph" + norm,
                 "launches_per_step": self.launches_per_step,
                 "l2": f"inputs larger than L2: {self.data.weight_bytes() / 1e9:.2f} GB of weights per step"}
 
@@ -282,8 +306,9 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
     l2 = getattr(props, "L2_cache_size", 126 << 20)
 
     kind, rows, K, B = describe(args.workload)
-    wk = StepWorkload(device, torch.cuda.Stream()) if kind == "step" else \
-        GemvWorkload(kind, rows, K, B, device, l2)
+    _, rms_eps = split_norm(args.workload)
+    wk = StepWorkload(device, torch.cuda.Stream(), rms_eps) if kind == "step" else \
+        GemvWorkload(kind, rows, K, B, device, l2, rms_eps)
     torch.cuda.synchronize()
 
     def barrier():

@@ -80,6 +80,34 @@ int gemv_bf16(const void *W, const void *x, float *y,
               int64_t N, int64_t K, int B, int64_t ldw, void *stream);
 
 /*
+ * Options of the *_ex calls. flags is 0 or a set of GEMV_FLAG_* bits; a NULL
+ * options pointer means flags = 0.
+ *
+ * GEMV_FLAG_RMSNORM: RMSNorm prologue on x ("GPU performance chains", "Fused
+ * RMSNorm traffic": at decode the bytes of a separate norm kernel are trivial
+ * and its launch is the cost, so it is fused into the projection that reads
+ * x). Each output row b is scaled by
+ *     r_b = (mean_{k<K} x[b][k]^2 + rms_eps)^(-1/2),
+ * computed in FP32 from the x the kernel stages anyway, i.e.
+ *     y[b][n] = r_b * sum_k W[n][k] * x[b][k].
+ * The norm's elementwise weight is expected folded into W's columns (W'[n][k]
+ * = W[n][k] * gamma[k], done once when the weights are loaded), which makes
+ * this equal to W · RMSNorm(x). rms_eps must be finite and >= 0; with
+ * rms_eps = 0 an all-zero x row gives non-finite outputs.
+ */
+#define GEMV_FLAG_RMSNORM 1
+
+typedef struct {
+    int flags;
+    float rms_eps;
+} gemv_options;
+
+/* gemv_bf16 with options (see gemv_options). */
+int gemv_bf16_ex(const void *W, const void *x, float *y,
+                 int64_t N, int64_t K, int B, int64_t ldw,
+                 const gemv_options *opt, void *stream);
+
+/*
  * One weight matrix of a fused launch: y_i = W_i · x, W_i [N_i, ldw_i], y_i
  * [B, N_i] (row stride N_i).
  */
@@ -103,10 +131,15 @@ typedef struct {
 int gemv_bf16_multi(const gemv_segment *segs, int nsegs, const void *x,
                     int64_t K, int B, void *stream);
 
+/* gemv_bf16_multi with options; the options apply to every segment (one x). */
+int gemv_bf16_multi_ex(const gemv_segment *segs, int nsegs, const void *x,
+                       int64_t K, int B, const gemv_options *opt, void *stream);
+
 /*
  * One projection of a decode step. Projections with the same fuse_group > 0,
- * the same x, K and B, that are adjacent in the list, become one fused launch
- * (at most GEMV_MAX_SEGMENTS per launch); fuse_group 0 means "alone".
+ * the same x, K, B, flags and rms_eps, that are adjacent in the list, become
+ * one fused launch (at most GEMV_MAX_SEGMENTS per launch); fuse_group 0 means
+ * "alone". flags and rms_eps are those of gemv_options.
  */
 typedef struct {
     const void *W;
@@ -117,6 +150,8 @@ typedef struct {
     int64_t ldw;
     int B;
     int fuse_group;
+    int flags;
+    float rms_eps;
 } gemv_proj;
 
 typedef struct gemv_plan gemv_plan;   /* opaque; owned by the library */

@@ -27,8 +27,10 @@ GEMV_ERR_UNSUPPORTED = -6
 GEMV_MAX_BATCH = 16
 GEMV_MAX_SEGMENTS = 8
 
+GEMV_FLAG_RMSNORM = 1
+
 EXPORTED = [
-    "gemv_bf16", "gemv_bf16_multi", "gemv_plan_create", "gemv_plan_capture",
+    "gemv_bf16", "gemv_bf16_ex", "gemv_bf16_multi", "gemv_bf16_multi_ex", "gemv_plan_create", "gemv_plan_capture",
     "gemv_plan_launch", "gemv_plan_num_launches", "gemv_plan_destroy",
     "gemv_query_launch", "gemv_probe_stream_read", "gemv_probe_sink_words",
     "gemv_status_string", "gemv_last_cuda_error",
@@ -44,7 +46,12 @@ class gemv_segment(ctypes.Structure):
 
 class gemv_proj(ctypes.Structure):
     _fields_ = [("W", vp), ("x", vp), ("y", vp), ("N", i64), ("K", i64), ("ldw", i64),
-                ("B", ctypes.c_int), ("fuse_group", ctypes.c_int)]
+                ("B", ctypes.c_int), ("fuse_group", ctypes.c_int), ("flags", ctypes.c_int),
+                ("rms_eps", ctypes.c_float)]
+
+
+class gemv_options(ctypes.Structure):
+    _fields_ = [("flags", ctypes.c_int), ("rms_eps", ctypes.c_float)]
 
 
 class gemv_launch_info(ctypes.Structure):
@@ -83,6 +90,10 @@ def lib() -> ctypes.CDLL:
             L.gemv_bf16.argtypes = [vp, vp, vp, i64, i64, ctypes.c_int, i64, vp]
             L.gemv_bf16_multi.argtypes = [ctypes.POINTER(gemv_segment), ctypes.c_int, vp, i64,
                                           ctypes.c_int, vp]
+            L.gemv_bf16_ex.argtypes = [vp, vp, vp, i64, i64, ctypes.c_int, i64,
+                                       ctypes.POINTER(gemv_options), vp]
+            L.gemv_bf16_multi_ex.argtypes = [ctypes.POINTER(gemv_segment), ctypes.c_int, vp, i64,
+                                             ctypes.c_int, ctypes.POINTER(gemv_options), vp]
             L.gemv_plan_create.argtypes = [ctypes.POINTER(gemv_proj), ctypes.c_int,
                                            ctypes.POINTER(vp)]
             L.gemv_plan_capture.argtypes = [vp, vp]
@@ -141,6 +152,31 @@ def gemv_bf16(W, x, y, N: int, K: int, B: int, ldw: int, stream=None, check: boo
     return _check(rc, "gemv_bf16") if check else rc
 
 
+def _options(rms_eps):
+    if rms_eps is None:
+        return None
+    return ctypes.byref(gemv_options(GEMV_FLAG_RMSNORM, float(rms_eps)))
+
+
+def gemv_bf16_ex(W, x, y, N: int, K: int, B: int, ldw: int, rms_eps=None, stream=None,
+                 check: bool = True, options=None) -> int:
+    """gemv_bf16 with options; ``rms_eps`` (not None) turns on the RMSNorm prologue.
+    ``options`` (a gemv_options) overrides ``rms_eps`` when given."""
+    opt = ctypes.byref(options) if options is not None else _options(rms_eps)
+    rc = lib().gemv_bf16_ex(_ptr(W), _ptr(x), _ptr(y), N, K, B, ldw, opt, _stream(stream))
+    return _check(rc, "gemv_bf16_ex") if check else rc
+
+
+def gemv_bf16_multi_ex(segments, x, K: int, B: int, rms_eps=None, stream=None, check: bool = True,
+                       options=None) -> int:
+    arr = (gemv_segment * max(1, len(segments)))()
+    for i, (W, y, N, ldw) in enumerate(segments):
+        arr[i] = gemv_segment(_ptr(W), _ptr(y), N, ldw)
+    opt = ctypes.byref(options) if options is not None else _options(rms_eps)
+    rc = lib().gemv_bf16_multi_ex(arr, len(segments), _ptr(x), K, B, opt, _stream(stream))
+    return _check(rc, "gemv_bf16_multi_ex") if check else rc
+
+
 def gemv_bf16_multi(segments, x, K: int, B: int, stream=None, check: bool = True) -> int:
     """``segments``: sequence of (W, y, N, ldw)."""
     arr = (gemv_segment * max(1, len(segments)))()
@@ -168,15 +204,21 @@ def gemv_probe_stream_read(src, nbytes: int, sink, stream=None) -> int:
 class Plan:
     """Owner of a gemv_plan handle (gemv_plan_create / capture / launch / destroy).
 
-    ``projections``: sequence of (W, x, y, N, K, ldw, B, fuse_group). The
-    tensors behind the pointers must outlive the plan; keep them referenced.
+    ``projections``: sequence of (W, x, y, N, K, ldw, B, fuse_group) or
+    (W, x, y, N, K, ldw, B, fuse_group, rms_eps) with rms_eps None for no
+    RMSNorm prologue. The tensors behind the pointers must outlive the plan;
+    keep them referenced.
     """
 
     def __init__(self, projections, keepalive=None):
         n = len(projections)
         arr = (gemv_proj * max(1, n))()
-        for i, (W, x, y, N, K, ldw, B, grp) in enumerate(projections):
-            arr[i] = gemv_proj(_ptr(W), _ptr(x), _ptr(y), N, K, ldw, B, grp)
+        for i, pr in enumerate(projections):
+            W, x, y, N, K, ldw, B, grp = pr[:8]
+            eps = pr[8] if len(pr) > 8 else None
+            flags = GEMV_FLAG_RMSNORM if eps is not None else 0
+            arr[i] = gemv_proj(_ptr(W), _ptr(x), _ptr(y), N, K, ldw, B, grp, flags,
+                               float(eps) if eps is not None else 0.0)
         handle = vp()
         _check(lib().gemv_plan_create(arr, n, ctypes.byref(handle)), "gemv_plan_create")
         self._h = handle

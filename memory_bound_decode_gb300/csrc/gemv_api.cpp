@@ -1,6 +1,7 @@
 // C-ABI front end of libgemv.so: argument checks, per-device set-up, fused
 // launches and the CUDA-graph decode-step plan. Every operation on data runs
 // in the kernels; this file only validates, plans and launches.
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -89,6 +90,19 @@ int check_matrix(const void* W, const float* y, int64_t N, int64_t K, int64_t ld
     return GEMV_OK;
 }
 
+int check_options(const gemv_options* opt, int* flags, float* eps) {
+    *flags = 0;
+    *eps = 0.f;
+    if (!opt) return GEMV_OK;
+    if (opt->flags & ~GEMV_FLAG_RMSNORM) return GEMV_ERR_INVALID;
+    if (opt->flags & GEMV_FLAG_RMSNORM) {
+        if (!std::isfinite(opt->rms_eps) || opt->rms_eps < 0.f) return GEMV_ERR_INVALID;
+        *eps = opt->rms_eps;
+    }
+    *flags = opt->flags;
+    return GEMV_OK;
+}
+
 // One prepared launch: parameters plus grid shape.
 struct Prepared {
     Params p;
@@ -97,8 +111,8 @@ struct Prepared {
 };
 
 // Validate a group of segments sharing x, K, B and plan one launch over them.
-int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B, int sm_count,
-            Prepared* out) {
+int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B, int flags, float eps,
+            int sm_count, Prepared* out) {
     if (!segs || nsegs < 1 || nsegs > GEMV_MAX_SEGMENTS) return GEMV_ERR_INVALID;
     int rc = check_common(x, K, B);
     if (rc != GEMV_OK) return rc;
@@ -135,6 +149,8 @@ int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B
     p.xstride = l.xstride;
     p.batch = B;
     p.nbuf = l.nbuf;
+    p.flags = (flags & GEMV_FLAG_RMSNORM) ? gemv::kFlagRmsNorm : 0;
+    p.rms_eps = eps;
     out->p = p;
     out->l = l;
     out->B = B;
@@ -157,31 +173,47 @@ struct gemv_plan {
 
 extern "C" {
 
-int gemv_bf16(const void* W, const void* x, float* y, int64_t N, int64_t K, int B, int64_t ldw,
-              void* stream) {
+int gemv_bf16_ex(const void* W, const void* x, float* y, int64_t N, int64_t K, int B, int64_t ldw,
+                 const gemv_options* opt, void* stream) {
     gemv_segment seg{W, y, N, ldw};
+    int flags = 0;
+    float eps = 0.f;
     int rc = check_common(x, K, B);
     if (rc != GEMV_OK) return rc;
     if ((rc = check_matrix(W, y, N, K, ldw)) != GEMV_OK) return rc;
+    if ((rc = check_options(opt, &flags, &eps)) != GEMV_OK) return rc;
     int sm_count = 0;
     if ((rc = device_state(&sm_count)) != GEMV_OK) return rc;
     Prepared pr;
-    if ((rc = prepare(&seg, 1, x, K, B, sm_count, &pr)) != GEMV_OK) return rc;
+    if ((rc = prepare(&seg, 1, x, K, B, flags, eps, sm_count, &pr)) != GEMV_OK) return rc;
     return run(pr, static_cast<cudaStream_t>(stream));
 }
 
-int gemv_bf16_multi(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B,
-                    void* stream) {
+int gemv_bf16(const void* W, const void* x, float* y, int64_t N, int64_t K, int B, int64_t ldw,
+              void* stream) {
+    return gemv_bf16_ex(W, x, y, N, K, B, ldw, nullptr, stream);
+}
+
+int gemv_bf16_multi_ex(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B,
+                       const gemv_options* opt, void* stream) {
     if (!segs || nsegs < 1 || nsegs > GEMV_MAX_SEGMENTS) return GEMV_ERR_INVALID;
     int rc = check_common(x, K, B);
     if (rc != GEMV_OK) return rc;
     for (int i = 0; i < nsegs; ++i)
         if ((rc = check_matrix(segs[i].W, segs[i].y, segs[i].N, K, segs[i].ldw)) != GEMV_OK) return rc;
+    int flags = 0;
+    float eps = 0.f;
+    if ((rc = check_options(opt, &flags, &eps)) != GEMV_OK) return rc;
     int sm_count = 0;
     if ((rc = device_state(&sm_count)) != GEMV_OK) return rc;
     Prepared pr;
-    if ((rc = prepare(segs, nsegs, x, K, B, sm_count, &pr)) != GEMV_OK) return rc;
+    if ((rc = prepare(segs, nsegs, x, K, B, flags, eps, sm_count, &pr)) != GEMV_OK) return rc;
     return run(pr, static_cast<cudaStream_t>(stream));
+}
+
+int gemv_bf16_multi(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B,
+                    void* stream) {
+    return gemv_bf16_multi_ex(segs, nsegs, x, K, B, nullptr, stream);
 }
 
 int gemv_plan_create(const gemv_proj* projs, int nproj, gemv_plan** out) {
@@ -195,6 +227,10 @@ int gemv_plan_create(const gemv_proj* projs, int nproj, gemv_plan** out) {
         if ((rc = check_matrix(projs[i].W, projs[i].y, projs[i].N, projs[i].K, projs[i].ldw)) != GEMV_OK)
             return rc;
         if (projs[i].fuse_group < 0) return GEMV_ERR_INVALID;
+        gemv_options o{projs[i].flags, projs[i].rms_eps};
+        int f = 0;
+        float e = 0.f;
+        if ((rc = check_options(&o, &f, &e)) != GEMV_OK) return rc;
     }
     int sm_count = 0;
     int rc = device_state(&sm_count);
@@ -209,13 +245,15 @@ int gemv_plan_create(const gemv_proj* projs, int nproj, gemv_plan** out) {
             int j = i + 1;
             if (a.fuse_group > 0) {
                 while (j < nproj && j - i < GEMV_MAX_SEGMENTS && projs[j].fuse_group == a.fuse_group &&
-                       projs[j].x == a.x && projs[j].K == a.K && projs[j].B == a.B)
+                       projs[j].x == a.x && projs[j].K == a.K && projs[j].B == a.B &&
+                       projs[j].flags == a.flags && projs[j].rms_eps == a.rms_eps)
                     ++j;
             }
             gemv_segment segs[GEMV_MAX_SEGMENTS];
             for (int q = i; q < j; ++q) segs[q - i] = gemv_segment{projs[q].W, projs[q].y, projs[q].N, projs[q].ldw};
             Prepared pr;
-            if ((rc = prepare(segs, j - i, a.x, a.K, a.B, sm_count, &pr)) != GEMV_OK) {
+            const float eps = (a.flags & GEMV_FLAG_RMSNORM) ? a.rms_eps : 0.f;
+            if ((rc = prepare(segs, j - i, a.x, a.K, a.B, a.flags, eps, sm_count, &pr)) != GEMV_OK) {
                 delete plan;
                 return rc;
             }

@@ -136,6 +136,37 @@ __device__ __forceinline__ Chunk chunk_at(int64_t c0, int64_t k1, int64_t kchunk
     return c;
 }
 
+// Sum of squares of the staged x rows (the RMSNorm statistic), from the chunk
+// in xbuf: every thread takes vectors tid, tid + kThreads, ...; lanes combine by
+// xor butterfly, warps in index order. The CTA total for row b goes to
+// misc[kWarps * kMaxBatch + b] (first chunk: assigned, later chunks: added).
+// Called by every thread of the CTA; zero-filled columns >= K add nothing.
+__device__ __forceinline__ void xsq_accumulate(const uint16_t* xbuf, int xstride, int B, int nv,
+                                               float* misc, bool first) {
+    float* wsum = misc;
+    float* xsq = misc + kWarps * kMaxBatch;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    for (int b = 0; b < B; ++b) {
+        float s = 0.f;
+        for (int i = threadIdx.x; i < nv; i += kThreads) {
+            float f[8];
+            unpack8(*reinterpret_cast<const uint4*>(xbuf + b * xstride + 8 * i), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s = fmaf(f[e], f[e], s);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        if (lane == 0) wsum[warp * kMaxBatch + b] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x < B) {
+        float t = wsum[threadIdx.x];
+        for (int w = 1; w < kWarps; ++w) t += wsum[w * kMaxBatch + threadIdx.x];
+        xsq[threadIdx.x] = first ? t : xsq[threadIdx.x] + t;
+    }
+}
+
 // Where warp kq of a row group puts its partial sum of (row_local, b): rows
 // of B + 1 floats, so that the lanes of a warp writing neighbouring rows do
 // not fall on the same shared-memory bank.
@@ -145,31 +176,48 @@ __device__ __forceinline__ int red_index(int kq, int rows_per_cta, int row_local
 
 // After every warp has written its partial sums with red_index: sum them over
 // kq in order, then (with a cluster along K) over the CTAs of the cluster in
-// rank order, and store each output once.
-__device__ __forceinline__ void combine_and_store(const float* red, float* cpart, int rows_per_cta, int B,
-                                                  int kw, int S, int split, int64_t n_base, int64_t N,
-                                                  float* __restrict__ y) {
+// rank order, scale by the RMSNorm factor of the batch row when asked (its sum
+// of squares combined over the cluster in rank order as well), and store each
+// output once.
+__device__ __forceinline__ void combine_and_store(const float* red, float* cpart, float* misc, int rows_per_cta,
+                                                  int B, int kw, int S, int split, int64_t n_base, int64_t N,
+                                                  float* __restrict__ y, bool norm, int64_t K, float eps) {
+    float* xsq = misc + kWarps * kMaxBatch;
+    float* rsc = xsq + kMaxBatch;
     __syncthreads();
+    if (norm && S == 1) {
+        if (threadIdx.x < B) rsc[threadIdx.x] = 1.0f / sqrtf(xsq[threadIdx.x] / static_cast<float>(K) + eps);
+        __syncthreads();
+    }
     const int nout = rows_per_cta * B;   // index i = row_local * B + b
     for (int i = threadIdx.x; i < nout; i += kThreads) {
         const int rl = i / B, b = i - (i / B) * B;
         float s = red[red_index(0, rows_per_cta, rl, B, b)];
         for (int q = 1; q < kw; ++q) s += red[red_index(q, rows_per_cta, rl, B, b)];
         if (S == 1) {
-            const int64_t n = n_base + i / B;
-            if (n < N) y[static_cast<int64_t>(i % B) * N + n] = s;
+            const int64_t n = n_base + rl;
+            if (n < N) y[static_cast<int64_t>(b) * N + n] = norm ? s * rsc[b] : s;
         } else {
             cpart[i] = s;
         }
     }
     if (S > 1) {
         cluster_sync_all();   // every CTA of the cluster has its partials in shared memory
+        if (norm) {
+            if (threadIdx.x < B) {
+                float t = ld_dsmem(&xsq[threadIdx.x], 0);
+                for (int q = 1; q < S; ++q) t += ld_dsmem(&xsq[threadIdx.x], static_cast<uint32_t>(q));
+                rsc[threadIdx.x] = 1.0f / sqrtf(t / static_cast<float>(K) + eps);
+            }
+            __syncthreads();
+        }
         for (int i = threadIdx.x; i < nout; i += kThreads) {
             if (i % S != split) continue;   // outputs are shared out over the ranks
             float s = ld_dsmem(&cpart[i], 0);
             for (int q = 1; q < S; ++q) s += ld_dsmem(&cpart[i], static_cast<uint32_t>(q));
-            const int64_t n = n_base + i / B;
-            if (n < N) y[static_cast<int64_t>(i % B) * N + n] = s;
+            const int rl = i / B, b = i - (i / B) * B;
+            const int64_t n = n_base + rl;
+            if (n < N) y[static_cast<int64_t>(b) * N + n] = norm ? s * rsc[b] : s;
         }
         cluster_sync_all();   // no CTA leaves while another still reads its shared memory
     }

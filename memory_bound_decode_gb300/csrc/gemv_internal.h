@@ -36,7 +36,17 @@ struct Params {
     int32_t xstride;  // shared-memory elements per staged x row (>= kchunk)
     int32_t batch;    // B
     int32_t nbuf;     // x buffers (2 when the K-range takes more than one chunk)
+    int32_t flags;    // kFlagRmsNorm
+    float rms_eps;    // epsilon of the RMSNorm prologue
 };
+
+// Scale each output row b by (mean_k x[b][k]^2 + rms_eps)^(-1/2) (RMSNorm
+// prologue; the norm's elementwise weight is folded into W).
+constexpr int32_t kFlagRmsNorm = 1;
+
+// Shared floats after the partial sums: per-warp sums of squares of x
+// [kWarps][kMaxBatch], the CTA's sums [kMaxBatch] and the row scales [kMaxBatch].
+constexpr int kMiscFloats = kWarps * kMaxBatch + 2 * kMaxBatch;
 
 // Kernel families.
 enum Path : int32_t {

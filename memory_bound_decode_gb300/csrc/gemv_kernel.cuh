@@ -144,6 +144,8 @@ gemv_bf16_kernel(const __grid_constant__ Params p) {
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem_raw);
     float* red = reinterpret_cast<float*>(smem_raw + static_cast<size_t>(p.nbuf) * xbuf * 2);
     float* cpart = red + rows_per_cta * (B + 1) * kw;
+    float* misc = cpart + rows_per_cta * B;
+    const bool norm = (p.flags & kFlagRmsNorm) != 0;
 
     const int64_t K = p.K;
     const int64_t k0 = static_cast<int64_t>(split) * p.kslice;
@@ -207,6 +209,7 @@ gemv_bf16_kernel(const __grid_constant__ Params p) {
             consume_batch<B, RPW, UJ, true>(acc, wv, ok, xl, xstride);
             advance();
         }
+        if (norm) xsq_accumulate(xcur, xstride, B, ch.nv, misc, c == 0);
         if (!more) break;
 
         // The next chunk's first weight batch goes out before the barrier that
@@ -238,7 +241,8 @@ gemv_bf16_kernel(const __grid_constant__ Params p) {
 #pragma unroll
             for (int b = 0; b < B; ++b) red[red_index(kq, rows_per_cta, g * RPW + r, B, b)] = acc[r][b];
     }
-    combine_and_store(red, cpart, rows_per_cta, B, kw, S, split, sg.tile_local * rows_per_cta, sg.N, sg.y);
+    combine_and_store(red, cpart, misc, rows_per_cta, B, kw, S, split, sg.tile_local * rows_per_cta, sg.N, sg.y,
+                      norm, K, p.rms_eps);
 }
 
 template <int B>

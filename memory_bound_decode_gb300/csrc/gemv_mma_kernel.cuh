@@ -169,6 +169,8 @@ gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem_raw);
     float* red = reinterpret_cast<float*>(smem_raw + static_cast<size_t>(p.nbuf) * xbuf * 2);
     float* cpart = red + rows_per_cta * (B + 1) * kw;
+    float* misc = cpart + rows_per_cta * B;
+    const bool norm = (p.flags & kFlagRmsNorm) != 0;
 
     const int64_t K = p.K;
     const int64_t k0 = static_cast<int64_t>(split) * p.kslice;
@@ -227,6 +229,7 @@ gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
             mma_consume<NB, UJ, true>(acc, w0, w1, ok, xrow0, xstride, v, g, B);
             advance();
         }
+        if (norm) xsq_accumulate(xs + (c & 1) * xbuf, xstride, B, ch.nv, misc, c == 0);
         if (!more) break;
 
         ch = nch;
@@ -250,7 +253,8 @@ gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
             if (b < B) red[red_index(kq, rows_per_cta, rl, B, b)] = acc[nb][i];
         }
     }
-    combine_and_store(red, cpart, rows_per_cta, B, kw, S, split, sg.tile_local * rows_per_cta, sg.N, sg.y);
+    combine_and_store(red, cpart, misc, rows_per_cta, B, kw, S, split, sg.tile_local * rows_per_cta, sg.N, sg.y,
+                      norm, K, p.rms_eps);
 }
 
 template <int NB>

@@ -157,3 +157,17 @@ def test_planner_rejects(L):
         binding.gemv_query_launch(8, 8, 17, GB300_SMS)
     with pytest.raises(binding.GemvError):
         binding.gemv_query_launch(8, 8, 1, 0)
+
+
+def test_options_rejected_before_launch(L):
+    ok = dict(stream=0, check=False)
+    bad_flags = binding.gemv_options(4, 0.0)
+    assert binding.gemv_bf16_ex(A16, A16, A16, 8, 8, 1, 8, options=bad_flags, **ok) == binding.GEMV_ERR_INVALID
+    for eps in (-1.0, float("nan"), float("inf")):
+        assert binding.gemv_bf16_ex(A16, A16, A16, 8, 8, 1, 8, rms_eps=eps, **ok) == binding.GEMV_ERR_INVALID
+        assert binding.gemv_bf16_multi_ex([(A16, A16, 8, 8)], A16, 8, 1, rms_eps=eps, **ok) == binding.GEMV_ERR_INVALID
+    with pytest.raises(binding.GemvError) as e:
+        binding.Plan([(A16, A16, A16, 8, 8, 8, 1, 0, -1.0)])
+    assert e.value.status == binding.GEMV_ERR_INVALID
+    # argument checks still come first
+    assert binding.gemv_bf16_ex(0, A16, A16, 8, 8, 1, 8, rms_eps=1e-5, **ok) == binding.GEMV_ERR_INVALID
