@@ -90,3 +90,51 @@ def from_bits(a: np.ndarray, device="cpu") -> torch.Tensor:
     """A BF16 tensor holding the given uint16 bit patterns."""
     a = np.ascontiguousarray(a, dtype=np.uint16)
     return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16).to(device)
+
+
+# ----------------------------------------------------------------------------- INT4 weights
+#
+# Layout of a group-quantised INT4 weight (group of W4_GROUP consecutive k per
+# row, one BF16 scale each; the value of an element is (u - 8) * scale with u
+# its 4-bit code):
+#   Wq : uint8 [N, ldq], ldq >= K / 2, ldq % 16 == 0. Row n, 32-bit word w
+#        (bytes 4w .. 4w+3, little endian) holds k = 8w .. 8w+7: the code of
+#        k = 8w + 2j sits in bits 4j .. 4j+3 and that of k = 8w + 2j + 1 in bits
+#        16 + 4j .. 16 + 4j + 3 (j = 0..3): even k in the low half-word, odd k in
+#        the high half-word.
+#   S  : BF16 [N, lds], lds >= K / W4_GROUP; S[n][g] scales k in [g*W4_GROUP, (g+1)*W4_GROUP).
+W4_GROUP = 128
+
+
+def w4_pack(u: np.ndarray, ldq: int | None = None) -> np.ndarray:
+    """Pack 4-bit codes u (uint8 in [0, 15], [N, K], K % 8 == 0) into the layout above."""
+    u = np.asarray(u, dtype=np.uint32)
+    N, K = u.shape
+    assert K % 8 == 0 and u.max(initial=0) < 16
+    ldq = K // 2 if ldq is None else int(ldq)
+    g = u.reshape(N, K // 8, 4, 2)               # [n, word, j, parity]
+    shifts = (4 * np.arange(4, dtype=np.uint32))[None, None, :]
+    words = ((g[..., 0] << shifts) | (g[..., 1] << (shifts + 16))).sum(axis=2, dtype=np.uint64).astype(np.uint32)
+    out = np.zeros((N, ldq), dtype=np.uint8)
+    out[:, : K // 2] = words.view(np.uint8).reshape(N, K // 2)
+    return out
+
+
+def w4_weight(N: int, K: int, ldq: int | None = None, lds: int | None = None, *, seed: int = 0,
+              index: int = 0, scale_lo: float = 0.002, scale_hi: float = 0.006, codes=None,
+              scales=None):
+    """(Wq uint8 [N, ldq], S bf16 [N, lds], u uint8 [N, K]) on the host: random codes
+    (or ``codes``) and scales uniform in [scale_lo, scale_hi] rounded to BF16 (or
+    ``scales``, float [N, K / W4_GROUP])."""
+    assert K % W4_GROUP == 0
+    ldq = (K // 2 + 15) // 16 * 16 if ldq is None else int(ldq)
+    G = K // W4_GROUP
+    lds = G if lds is None else int(lds)
+    g = generator(seed, index, "cpu")
+    if codes is None:
+        codes = torch.randint(0, 16, (N, K), generator=g, dtype=torch.int32).numpy().astype(np.uint8)
+    if scales is None:
+        scales = (torch.rand((N, G), generator=g, dtype=torch.float32) * (scale_hi - scale_lo) + scale_lo)
+    S = torch.zeros((N, lds), dtype=torch.bfloat16)
+    S[:, :G] = torch.as_tensor(scales, dtype=torch.float32).to(torch.bfloat16)
+    return w4_pack(codes, ldq), S, np.asarray(codes, dtype=np.uint8)

@@ -134,3 +134,50 @@ int oracle_gemv_rmsnorm_f64(const uint16_t *W, const uint16_t *x,
     }
     return 0;
 }
+
+/*
+ * The GEMV with group-quantised INT4 weights ("Decode GEMV at half of HBM
+ * bandwidth", "What interviewers probe next": with INT4 weights the bytes fall
+ * four times). Element (n, k) of W is (u - 8) * scale, u its 4-bit code and
+ * scale = S[n][k / group] (BF16). Codes are packed eight to a little-endian
+ * 32-bit word per row, word w of row n at byte n*ldq + 4w holding
+ * k = 8w .. 8w+7: k = 8w + 2j in bits 4j..4j+3, k = 8w + 2j + 1 in bits
+ * 16+4j..16+4j+3. Rows [n0, n1); FP64; the same y and tolerance scale s as
+ * oracle_gemv_f64. Returns 0, or -1 on a bad argument.
+ */
+static double w4_element(const uint8_t *Wq, const uint16_t *S, int64_t ldq, int64_t lds,
+                         int64_t group, int64_t n, int64_t k)
+{
+    const uint8_t *p = Wq + n * ldq + 4 * (k / 8);
+    uint32_t word = (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+    int64_t i = k % 8;
+    int shift = (i % 2 == 0) ? (int)(4 * (i / 2)) : (int)(16 + 4 * (i / 2));
+    int code = (int)((word >> shift) & 0xFu);
+    return (double)(code - 8) * bf16_to_double(S[n * lds + k / group]);
+}
+
+int oracle_gemv_w4_f64(const uint8_t *Wq, const uint16_t *S, const uint16_t *x,
+                       int64_t N, int64_t K, int64_t B, int64_t ldq, int64_t lds, int64_t group,
+                       int64_t n0, int64_t n1, double *y, double *s)
+{
+    if (!Wq || !S || !x || !y || !s) return -1;
+    if (N < 1 || K < 1 || B < 1 || group < 1 || K % 8 != 0) return -1;
+    if (ldq < K / 2 || lds < (K + group - 1) / group) return -1;
+    if (n0 < 0 || n1 > N || n0 > n1) return -1;
+
+    for (int64_t b = 0; b < B; ++b) {
+        const uint16_t *xrow = x + b * K;
+        for (int64_t n = n0; n < n1; ++n) {
+            double dot = 0.0;
+            double absdot = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double t = w4_element(Wq, S, ldq, lds, group, n, k) * bf16_to_double(xrow[k]);
+                dot += t;
+                absdot += fabs(t);
+            }
+            y[b * N + n] = dot;
+            s[b * N + n] = absdot;
+        }
+    }
+    return 0;
+}

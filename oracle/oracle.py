@@ -79,6 +79,9 @@ class OracleLib:
         h = self._lib.oracle_gemv_rmsnorm_f64
         h.restype = ctypes.c_int
         h.argtypes = [vp, vp, i64, i64, i64, i64, ctypes.c_double, i64, i64, vp, vp, vp]
+        q = self._lib.oracle_gemv_w4_f64
+        q.restype = ctypes.c_int
+        q.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64, vp, vp]
 
     def gemv(self, W: np.ndarray, x: np.ndarray, K: int | None = None,
              threads: int | None = None) -> tuple[np.ndarray, np.ndarray]:
@@ -135,6 +138,41 @@ class OracleLib:
         r[:] = rs[0]
         return y, s, r
 
+    def gemv_w4(self, Wq: np.ndarray, S: np.ndarray, x: np.ndarray, K: int, group: int = 128,
+                threads: int | None = None) -> tuple[np.ndarray, np.ndarray]:
+        """(y_ref, scale) of the INT4 GEMV. Wq uint8 [N, ldq], S uint16 [N, lds]
+        (BF16 bits), x uint16 [B, K]."""
+        if Wq.dtype != np.uint8 or S.dtype != np.uint16 or x.dtype != np.uint16:
+            raise TypeError("Wq uint8, S and x BF16 bits as uint16")
+        if x.ndim == 1:
+            x = x[None, :]
+        Wq = np.ascontiguousarray(Wq)
+        S = np.ascontiguousarray(S)
+        x = np.ascontiguousarray(x)
+        N, ldq = Wq.shape
+        lds = S.shape[1]
+        B = x.shape[0]
+        if x.shape[1] != K or S.shape[0] != N:
+            raise ValueError("shapes disagree")
+        y = np.empty((B, N), dtype=np.float64)
+        s = np.empty((B, N), dtype=np.float64)
+        threads = max(1, min(threads or 1, N))
+        bounds = np.linspace(0, N, threads + 1).astype(np.int64)
+
+        def run(i: int) -> int:
+            return self._lib.oracle_gemv_w4_f64(
+                Wq.ctypes.data, S.ctypes.data, x.ctypes.data, N, K, B, ldq, lds, group,
+                int(bounds[i]), int(bounds[i + 1]), y.ctypes.data, s.ctypes.data)
+
+        if threads == 1:
+            rcs = [run(0)]
+        else:
+            with ThreadPoolExecutor(max_workers=threads) as ex:
+                rcs = list(ex.map(run, range(threads)))
+        if any(rc != 0 for rc in rcs):
+            raise ValueError("oracle rejected its arguments")
+        return y, s
+
     def gemv_one(self, W: np.ndarray, x: np.ndarray, b: int, n: int,
                  K: int | None = None) -> tuple[float, float]:
         """Return (y_ref[b, n], scale[b, n]) for a single output element."""
@@ -183,6 +221,11 @@ def gemv(W: np.ndarray, x: np.ndarray, K: int | None = None,
 def gemv_rmsnorm(W: np.ndarray, x: np.ndarray, eps: float, K: int | None = None,
                  threads: int | None = None):
     return load().gemv_rmsnorm(W, x, eps, K, threads)
+
+
+def gemv_w4(Wq: np.ndarray, S: np.ndarray, x: np.ndarray, K: int, group: int = 128,
+            threads: int | None = None):
+    return load().gemv_w4(Wq, S, x, K, group, threads)
 
 
 def gemv_one(W: np.ndarray, x: np.ndarray, b: int, n: int, K: int | None = None):

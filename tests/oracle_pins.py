@@ -17,6 +17,15 @@ What pins what:
   batch_rows          row b of a batch equals a single-row call on x[b]
   padding_unread      NaN in the ldw padding never reaches y
   float64_matmul      random BF16 data against numpy float64 matmul
+  single_element      the one-element entry point equals the full computation
+  rms_constant_x      RMSNorm prologue: x = c gives r = (c^2 + eps)^(-1/2), y = r*c*rowsum
+  rms_scale_free      RMSNorm prologue with eps = 0: y(4x) = y(x) bitwise
+  rms_independent     r from numpy's own mean and sqrt; y and scale = r * the plain GEMV
+  w4_integer_exact    INT4 weights, power-of-two group scales, integer x: y exact
+                      against numpy int64 arithmetic on the codes the packer was given
+  w4_one_hot          INT4: one-hot x at every position of a word and across a group
+                      boundary selects (u - 8) * scale
+  w4_dense            INT4 against numpy float64 on weights dequantised from the codes
 """
 from __future__ import annotations
 
@@ -223,10 +232,59 @@ def rms_independent(lib):
         raise AssertionError("negative eps accepted")
 
 
+def _w4_case(N, K, B, seed, ldq=None, lds=None, pow2_scales=False):
+    G = K // inputs.W4_GROUP
+    scales = None
+    if pow2_scales:
+        scales = np.array([[2.0 ** ((n + g) % 5 - 2) for g in range(G)] for n in range(N)])
+    Wq, S, u = inputs.w4_weight(N, K, ldq, lds, seed=seed, scales=scales)
+    return Wq, inputs.bits(S), u
+
+
+def w4_integer_exact(lib):
+    for (N, K, B, ldq, lds) in [(5, 256, 2, 144, 3), (9, 1024, 3, 512, 8), (3, 128, 1, 64, 1)]:
+        Wq, S, u = _w4_case(N, K, B, seed=N + K, ldq=ldq, lds=lds, pow2_scales=True)
+        x = inputs.bits(inputs.int_activations(B, K, lo=-3, hi=3, seed=N))
+        y, sc = lib.gemv_w4(Wq, S, x, K)
+        G = K // inputs.W4_GROUP
+        s4 = (_decode(S[:, :G]) * 4).astype(np.int64)                 # 4 * scale is an integer
+        w4 = (u.astype(np.int64) - 8) * np.repeat(s4, inputs.W4_GROUP, axis=1)
+        xi = _decode(x).astype(np.int64)
+        assert np.array_equal(y * 4, (xi @ w4.T).astype(np.float64)), (N, K)
+        assert np.array_equal(sc * 4, (np.abs(xi) @ np.abs(w4).T).astype(np.float64))
+
+
+def w4_one_hot(lib):
+    N, K = 6, 384
+    Wq, S, u = _w4_case(N, K, 1, seed=31)
+    Sd = _decode(S)
+    for k in list(range(8)) + [127, 128, 129, 255, 383]:
+        x = np.zeros((1, K), dtype=np.uint16)
+        x[0, k] = 0x3F80
+        y, _ = lib.gemv_w4(Wq, S, x, K)
+        want = (u[:, k].astype(np.float64) - 8) * Sd[:, k // inputs.W4_GROUP]
+        assert np.array_equal(y[0], want), k
+
+
+def w4_dense(lib):
+    N, K, B = 40, 1024, 4
+    Wq, S, u = _w4_case(N, K, B, seed=32)
+    x = inputs.bits(inputs.activations(B, K, seed=33))
+    y, sc = lib.gemv_w4(Wq, S, x, K)
+    Wd = (u.astype(np.float64) - 8) * np.repeat(_decode(S), inputs.W4_GROUP, axis=1)
+    xd = _decode(x)
+    assert np.all(np.abs(y - xd @ Wd.T) <= 4 * K * EPS64 * sc)
+    assert np.allclose(sc, np.abs(xd) @ np.abs(Wd).T, rtol=1e-12, atol=0)
+    zero = inputs.w4_pack(np.full((N, K), 8, dtype=np.uint8))
+    y0, s0 = lib.gemv_w4(zero, S, x, K)
+    assert np.array_equal(y0, np.zeros_like(y0)) and np.array_equal(s0, np.zeros_like(s0))
+
+
 ALL_PINS = [exact_rational, integer_matmul, ones_row_sums, one_hot_column,
             identity_padded, scaling_exact, linearity, row_permutation,
             batch_rows, padding_unread, float64_matmul, single_element,
-            rms_constant_x, rms_scale_free, rms_independent]
+            rms_constant_x, rms_scale_free, rms_independent,
+            w4_integer_exact, w4_one_hot, w4_dense]
 
 
 def failures(lib) -> list[str]:

@@ -39,6 +39,15 @@ MUTATIONS = {
     "rms_abs_not_square": ("            sq += v * v;", "            sq += v < 0.0 ? -v : v;"),
     "rms_scale_unscaled": ("            s[b * N + n] *= rb;\n", ""),
     "rms_mean_over_ldw": ("1.0 / sqrt(sq / (double)K + eps)", "1.0 / sqrt(sq / (double)ldw + eps)"),
+    "w4_odd_even_swapped": ("int shift = (i % 2 == 0) ? (int)(4 * (i / 2)) : (int)(16 + 4 * (i / 2));",
+                            "int shift = (i % 2 == 1) ? (int)(4 * (i / 2)) : (int)(16 + 4 * (i / 2));"),
+    "w4_no_zero_point": ("return (double)(code - 8) *", "return (double)(code) *"),
+    "w4_group_64": ("bf16_to_double(S[n * lds + k / group]);", "bf16_to_double(S[n * lds + k / 64]);"),
+    "w4_row_stride_half_k": ("const uint8_t *p = Wq + n * ldq + 4 * (k / 8);",
+                             "const uint8_t *p = Wq + n * (lds * 64) + 4 * (k / 8);"),
+    "w4_scale_row_0": ("bf16_to_double(S[n * lds + k / group]);", "bf16_to_double(S[k / group]);"),
+    "w4_big_endian": ("uint32_t word = (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);",
+                      "uint32_t word = (uint32_t)p[3] | ((uint32_t)p[2] << 8) | ((uint32_t)p[1] << 16) | ((uint32_t)p[0] << 24);"),
 }
 
 
