@@ -166,10 +166,22 @@ def split_norm(workload: str) -> tuple[str, float | None]:
     return workload, None
 
 
+W4_PREFIX = "w4:"
+
+
+def split_w4(workload: str) -> tuple[str, bool]:
+    """A workload name may start with "w4:": the same shapes with group-quantised
+    INT4 weights (128-column groups, BF16 scales)."""
+    if workload.startswith(W4_PREFIX):
+        return workload[len(W4_PREFIX):], True
+    return workload, False
+
+
 def describe(workload: str):
     """(kind, N-list, K, B) of a named workload."""
     from memory_bound_decode_gb300 import workloads as wl
     workload, _ = split_norm(workload)
+    workload, _ = split_w4(workload)
     if workload in ("down_proj", "k_proj", "o_proj", "lm_head"):
         N, K = wl.SHAPES[workload]
         return "single", [N], K, 1
@@ -191,18 +203,31 @@ def describe(workload: str):
 class GemvWorkload:
     """Rotating device-resident weight copies for one (possibly fused) GEMV."""
 
-    def __init__(self, kind, rows, K, B, device, l2_bytes, rms_eps=None):
+    def __init__(self, kind, rows, K, B, device, l2_bytes, rms_eps=None, w4=False):
         import torch
         from memory_bound_decode_gb300 import inputs, roofline
         self.kind, self.rows, self.K, self.B = kind, rows, K, B
         self.rms_eps = rms_eps
-        self.ldw = inputs.padded_ldw(K)
+        self.w4 = w4
         self.N = sum(rows)
-        self.bytes_per_step = roofline.algorithmic_bytes(self.N, K, B)
-        wbytes = 2 * self.N * self.ldw
+        if w4:
+            if kind != "single":
+                raise SystemExit("INT4 weights: single-matrix workloads only")
+            self.ldq = (K // 2 + 15) // 16 * 16
+            self.lds = K // inputs.W4_GROUP
+            self.bytes_per_step = roofline.algorithmic_bytes_w4(self.N, K, B)
+            wbytes = self.N * (self.ldq + 2 * self.lds)
+        else:
+            self.ldw = inputs.padded_ldw(K)
+            self.bytes_per_step = roofline.algorithmic_bytes(self.N, K, B)
+            wbytes = 2 * self.N * self.ldw
         self.copies = max(1, min(64, math.ceil(3 * l2_bytes / wbytes)))
-        self.Ws = [[inputs.weight(n, K, self.ldw, seed=0, index=10 * c + i, device=device)
-                    for i, n in enumerate(rows)] for c in range(self.copies)]
+        if w4:
+            self.Ws = [[inputs.w4_weight_device(self.N, K, self.ldq, self.lds, seed=0, index=10 * c,
+                                                device=device)] for c in range(self.copies)]
+        else:
+            self.Ws = [[inputs.weight(n, K, self.ldw, seed=0, index=10 * c + i, device=device)
+                        for i, n in enumerate(rows)] for c in range(self.copies)]
         self.x = inputs.activations(B, K, seed=0, index=1000, device=device)
         self.ys = [torch.empty((B, n), dtype=torch.float32, device=device) for n in rows]
         self.launches_per_step = 1
@@ -212,7 +237,11 @@ class GemvWorkload:
         from memory_bound_decode_gb300 import binding
         Ws = self.Ws[i % self.copies]
         x = self.x if x is None else x
-        if self.kind == "single" and self.rms_eps is None:
+        if self.w4:
+            Wq, S = Ws[0]
+            binding.gemv_w4_bf16(Wq, S, x, self.ys[0], self.N, self.K, self.B, self.ldq, self.lds,
+                                 rms_eps=self.rms_eps, stream=stream)
+        elif self.kind == "single" and self.rms_eps is None:
             binding.gemv_bf16(Ws[0], x, self.ys[0], self.N, self.K, self.B, self.ldw, stream)
         elif self.kind == "single":
             binding.gemv_bf16_ex(Ws[0], x, self.ys[0], self.N, self.K, self.B, self.ldw,
@@ -227,8 +256,10 @@ class GemvWorkload:
     def config(self) -> dict:
         shape = "+".join(str(n) for n in self.rows)
         norm = f", RMSNorm prologue eps={self.rms_eps}" if self.rms_eps is not None else ""
-        return {"workload": f"{self.kind} BF16 GEMV N={shape} K={self.K} B={self.B}{norm}",
-                "N": self.N, "K": self.K, "B": self.B, "ldw": self.ldw,
+        wt = "INT4-weight (128-col groups, BF16 scales)" if self.w4 else "BF16"
+        return {"workload": f"{self.kind} {wt} GEMV N={shape} K={self.K} B={self.B}{norm}",
+                "N": self.N, "K": self.K, "B": self.B,
+                "ldw": self.ldq if self.w4 else self.ldw,
                 "segments": len(self.rows),
                 "l2": f"inputs larger than L2: {self.copies} rotating weight copies, "
                       f"{self.rotating_bytes / 1e6:.0f} MB"}
@@ -307,8 +338,9 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
 
     kind, rows, K, B = describe(args.workload)
     _, rms_eps = split_norm(args.workload)
+    _, w4 = split_w4(split_norm(args.workload)[0])
     wk = StepWorkload(device, torch.cuda.Stream(), rms_eps) if kind == "step" else \
-        GemvWorkload(kind, rows, K, B, device, l2, rms_eps)
+        GemvWorkload(kind, rows, K, B, device, l2, rms_eps, w4)
     torch.cuda.synchronize()
 
     def barrier():
@@ -390,7 +422,9 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_kind": f"{peak_kind} copy (MEASURED_PEAKS hbm_gbs, burst)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "kernel": "gemv_bf16_kernel (CUDA cores)" if wk.B == 1 else "gemv_bf16_mma_kernel (BF16 tensor cores)",
+                     "kernel": ("gemv_w4_kernel (INT4 codes, BF16 tensor cores)" if getattr(wk, "w4", False)
+                                else "gemv_bf16_kernel (CUDA cores)" if wk.B == 1
+                                else "gemv_bf16_mma_kernel (BF16 tensor cores)"),
                      "kernel_source_hash": src_hash},
         "ceilings": {"copy_gbs": peak,
                      "read_probe_gbs": round(read_ceiling, 1) if read_ceiling else None,

@@ -202,13 +202,40 @@ typedef struct {
     int32_t rows_per_warp;   /* rows one warp streams together (16: tensor-core tile) */
     int32_t unroll;          /* loads per lane per row in flight before any is used */
     int32_t smem_bytes;      /* dynamic shared memory per CTA                     */
-    int32_t path;            /* 0: CUDA-core FP32 FMA (batch 1), 1: BF16 tensor-core MMA */
+    int32_t path;            /* 0: CUDA-core FP32 FMA (batch 1), 1: BF16 tensor-core MMA,
+                                2: INT4 weights on the BF16 tensor cores */
     int32_t xstride;         /* shared-memory elements per staged x row           */
     int32_t nbuf;            /* x buffers: 2 when the K-range is staged in chunks */
 } gemv_launch_info;
 
 int gemv_query_launch(int64_t N, int64_t K, int B, int sm_count,
                       gemv_launch_info *out);
+
+/*
+ * y = W·x with group-quantised INT4 weights ("Decode GEMV at half of HBM
+ * bandwidth", "What interviewers probe next": with INT4 weights the bytes fall
+ * four times; the codes are unpacked in registers while the next loads are in
+ * flight). Element (n, k) of W is (u - 8) * S[n][k / 128], u the 4-bit code:
+ *   Wq : N rows of ldq bytes (ldq >= K/2, ldq % 16 == 0, Wq 16-byte aligned).
+ *        Row n, little-endian 32-bit word w (bytes 4w..4w+3) holds the codes of
+ *        k = 8w..8w+7: k = 8w + 2j in bits 4j..4j+3 and k = 8w + 2j + 1 in bits
+ *        16+4j..16+4j+3 (j = 0..3), i.e. even k in the low half-word and odd k
+ *        in the high half-word.
+ *   S  : N rows of lds BF16 scales (lds >= K/128), S[n][g] for k in
+ *        [128 g, 128 g + 128).
+ *   x, y, B and the options as for gemv_bf16_ex; K must be a multiple of 128.
+ * The contraction runs on the BF16 tensor cores with FP32 accumulation for
+ * every B (dequantised codes are exact in BF16; each 128-column group is summed
+ * and then scaled). Accuracy bound and tolerance as for gemv_bf16, with
+ * |W[n][k]| = |u - 8| * S[n][k/128].
+ */
+int gemv_w4_bf16(const void *Wq, const void *S, const void *x, float *y,
+                 int64_t N, int64_t K, int B, int64_t ldq, int64_t lds,
+                 const gemv_options *opt, void *stream);
+
+/* gemv_query_launch for the INT4-weight GEMV (K a multiple of 128). */
+int gemv_w4_query_launch(int64_t N, int64_t K, int B, int sm_count,
+                         gemv_launch_info *out);
 
 /*
  * Read-only bandwidth probe: streams `bytes` (a multiple of 16, >= 16) from the

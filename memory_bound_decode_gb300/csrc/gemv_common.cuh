@@ -230,6 +230,8 @@ struct SegView {
     int64_t N;
     int64_t ldw;
     int64_t tile_local;
+    const uint16_t* S;   // INT4 weights: group scales
+    int64_t lds;
 };
 
 __device__ __forceinline__ SegView segment_of(const Params& p, int64_t tile) {
@@ -243,6 +245,8 @@ __device__ __forceinline__ SegView segment_of(const Params& p, int64_t tile) {
     s.N = p.seg[si].N;
     s.ldw = p.seg[si].ldw;
     s.tile_local = tile - p.seg[si].tile_begin;
+    s.S = p.seg[si].S;
+    s.lds = p.seg[si].lds;
     return s;
 }
 

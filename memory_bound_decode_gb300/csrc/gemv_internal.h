@@ -16,11 +16,13 @@ constexpr int kMaxSplits = 8;             // CTAs along K: one portable cluster
 // One weight matrix of a launch. Row tiles of all segments are numbered
 // consecutively; tile_begin is the first tile of this segment.
 struct Seg {
-    const uint16_t* W;
+    const uint16_t* W;     // BF16 weights, or packed INT4 codes (then ldw is in bytes)
     float* y;
     int64_t N;
     int64_t ldw;
     int64_t tile_begin;
+    const uint16_t* S;     // INT4 weights: BF16 group scales [N, lds]; unused otherwise
+    int64_t lds;
 };
 
 // Everything one launch needs; passed by value as a __grid_constant__.
@@ -52,7 +54,16 @@ constexpr int kMiscFloats = kWarps * kMaxBatch + 2 * kMaxBatch;
 enum Path : int32_t {
     kPathFma = 0,   // CUDA-core FP32 multiply-adds, one warp streams RPW whole rows
     kPathMma = 1,   // BF16 tensor-core mma.sync, one warp streams a 16-row tile
+    kPathW4 = 2,    // INT4 weights dequantised to BF16 in registers, tensor-core mma.sync
 };
+
+// Weight formats the planner knows.
+enum WeightKind : int32_t {
+    kWeightBf16 = 0,
+    kWeightInt4 = 1,   // 128-column groups, BF16 scales
+};
+constexpr int kW4Group = 128;
+constexpr int kW4Unroll = 4;      // 128-column groups in flight per lane (2 x 16 B each)
 
 // Compile-time shape of the CUDA-core kernel instance for batch B.
 struct Variant {
@@ -89,7 +100,7 @@ struct Launch {
 };
 
 // Returns 0 and fills `out`, or a negative GEMV_ERR_* code.
-int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out);
+int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind = kWeightBf16);
 
 // Largest dynamic shared memory any plan requests (set as the kernel attribute).
 constexpr int32_t kMaxDynSmem = 112 * 1024;

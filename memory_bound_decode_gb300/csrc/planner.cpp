@@ -35,9 +35,10 @@ int64_t round_up(int64_t a, int64_t m) { return cdiv(a, m) * m; }
 
 }  // namespace
 
-int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out) {
+int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind) {
     if (!out || N < 1 || K < 1 || B < 1 || B > kMaxBatch || sm_count < 1) return GEMV_ERR_INVALID;
-    const Path path = path_for(B);
+    if (weight_kind != kWeightBf16 && weight_kind != kWeightInt4) return GEMV_ERR_INVALID;
+    const Path path = weight_kind == kWeightInt4 ? kPathW4 : path_for(B);
     int group_rows, unroll, xpad;
     int64_t batch_cols, warp_inflight;
     bool cluster_first;
@@ -49,11 +50,18 @@ int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out) {
         warp_inflight = 32LL * 16 * v.unroll * v.rows_per_warp;
         cluster_first = false;
         xpad = 0;
-    } else {
+    } else if (path == kPathMma) {
         group_rows = kMmaRows;
         unroll = kMmaUnroll;
         batch_cols = 32LL * kMmaUnroll;    // 4 lanes x 8 columns per load and row
         warp_inflight = 32LL * 16 * kMmaUnroll * 2;
+        cluster_first = true;
+        xpad = kMmaXPad;
+    } else {
+        group_rows = kMmaRows;
+        unroll = kW4Unroll;
+        batch_cols = static_cast<int64_t>(kW4Group) * kW4Unroll;   // one group per slot
+        warp_inflight = 32LL * 16 * kW4Unroll * 2;
         cluster_first = true;
         xpad = kMmaXPad;
     }

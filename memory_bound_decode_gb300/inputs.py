@@ -138,3 +138,27 @@ def w4_weight(N: int, K: int, ldq: int | None = None, lds: int | None = None, *,
     S = torch.zeros((N, lds), dtype=torch.bfloat16)
     S[:, :G] = torch.as_tensor(scales, dtype=torch.float32).to(torch.bfloat16)
     return w4_pack(codes, ldq), S, np.asarray(codes, dtype=np.uint8)
+
+
+def w4_weight_device(N: int, K: int, ldq: int | None = None, lds: int | None = None, *, seed: int = 0,
+                     index: int = 0, device="cuda", scale_lo: float = 0.002, scale_hi: float = 0.006):
+    """Random INT4 weight in the layout above, drawn and packed on the device
+    (for workloads too large to pack on the host): (Wq uint8 [N, ldq], S bf16 [N, lds])."""
+    assert K % W4_GROUP == 0
+    ldq = (K // 2 + 15) // 16 * 16 if ldq is None else int(ldq)
+    G = K // W4_GROUP
+    lds = G if lds is None else int(lds)
+    g = generator(seed, index, device)
+    Wq = torch.zeros((N, ldq), dtype=torch.uint8, device=device)
+    rows = max(1, (1 << 26) // K)
+    for r0 in range(0, N, rows):
+        r1 = min(N, r0 + rows)
+        u = torch.randint(0, 16, (r1 - r0, K // 8, 4, 2), generator=g, device=device, dtype=torch.int64)
+        shifts = 4 * torch.arange(4, device=device, dtype=torch.int64)
+        words = ((u[..., 0] << shifts) | (u[..., 1] << (shifts + 16))).sum(dim=2)
+        words = torch.where(words >= 2 ** 31, words - 2 ** 32, words).to(torch.int32)
+        Wq[r0:r1, : K // 2] = words.contiguous().view(torch.uint8).view(r1 - r0, K // 2)
+    S = torch.zeros((N, lds), dtype=torch.bfloat16, device=device)
+    sc = torch.rand((N, G), generator=g, device=device, dtype=torch.float32) * (scale_hi - scale_lo) + scale_lo
+    S[:, :G] = sc.to(torch.bfloat16)
+    return Wq, S

@@ -19,6 +19,13 @@ def algorithmic_bytes(N: int, K: int, B: int = 1) -> int:
     return 2 * N * K + 2 * B * K + 4 * B * N
 
 
+def algorithmic_bytes_w4(N: int, K: int, B: int = 1, group: int = 128) -> int:
+    """The same for INT4 weights: N*K/2 bytes of codes plus N*K/group BF16 scales
+    ("Decode GEMV at half of HBM bandwidth", "What interviewers probe next": with
+    INT4 weights the bytes fall four times)."""
+    return N * K // 2 + 2 * N * (K // group) + 2 * B * K + 4 * B * N
+
+
 def flops(N: int, K: int, B: int = 1) -> int:
     """One multiply and one add per weight element per batch row."""
     return 2 * B * N * K

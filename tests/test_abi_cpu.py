@@ -171,3 +171,30 @@ def test_options_rejected_before_launch(L):
     assert e.value.status == binding.GEMV_ERR_INVALID
     # argument checks still come first
     assert binding.gemv_bf16_ex(0, A16, A16, 8, 8, 1, 8, rms_eps=1e-5, **ok) == binding.GEMV_ERR_INVALID
+
+
+def test_w4_rejects_before_launch(L):
+    ok = dict(stream=0, check=False)
+    f = binding.gemv_w4_bf16
+    assert f(0, A16, A16, A16, 8, 128, 1, 64, 1, **ok) == binding.GEMV_ERR_INVALID          # Wq NULL
+    assert f(A16, 0, A16, A16, 8, 128, 1, 64, 1, **ok) == binding.GEMV_ERR_INVALID          # S NULL
+    assert f(A16, A16, A16, A16, 8, 100, 1, 64, 1, **ok) == binding.GEMV_ERR_INVALID        # K % 128
+    assert f(A16, A16, A16, A16, 8, 256, 1, 64, 2, **ok) == binding.GEMV_ERR_INVALID        # ldq < K/2
+    assert f(A16, A16, A16, A16, 8, 256, 1, 128, 1, **ok) == binding.GEMV_ERR_INVALID       # lds < K/128
+    assert f(A16, A16, A16, A16, 8, 256, 17, 128, 2, **ok) == binding.GEMV_ERR_INVALID      # B > 16
+    assert f(A16, A16, A16, A16, 8, 256, 1, 136, 2, **ok) == binding.GEMV_ERR_ALIGN         # ldq % 16
+    assert f(A16 + 8, A16, A16, A16, 8, 256, 1, 128, 2, **ok) == binding.GEMV_ERR_ALIGN     # Wq alignment
+    assert f(A16, A16 + 1, A16, A16, 8, 256, 1, 128, 2, **ok) == binding.GEMV_ERR_ALIGN     # S alignment
+    assert f(A16, A16, A16, A16, 8, 256, 1, 128, 2, rms_eps=-1.0, **ok) == binding.GEMV_ERR_INVALID
+
+
+@pytest.mark.parametrize("B", [1, 8, 16])
+@pytest.mark.parametrize("N,K", [(4096, 14336), (128256, 4096), (7, 128), (33, 65536)])
+def test_w4_plan_covers_the_problem(L, N, K, B):
+    q = binding.gemv_w4_query_launch(N, K, B, GB300_SMS)
+    assert q["path"] == 2 and q["rows_per_warp"] == 16
+    assert q["row_tiles"] * q["rows_per_cta"] >= N
+    assert q["splits"] * q["kslice"] >= K > (q["splits"] - 1) * q["kslice"]
+    assert q["kslice"] % 128 == 0 and q["kchunk"] % 128 == 0      # groups never straddle
+    with pytest.raises(binding.GemvError):
+        binding.gemv_w4_query_launch(N, 100, B, GB300_SMS)
