@@ -87,10 +87,17 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // Copy x[b][c0 .. c0 + 8*nv) for b < B into shared memory (row stride
-// xstride), zero-filling columns >= K. Aligned 16-byte pieces go out as
+// xstride; with SWZ, vector i of a row at position xswz(i)), zero-filling
+// columns >= K. Aligned 16-byte pieces go out as
 // asynchronous copies, all in flight at once and holding no registers;
 // misaligned ones (rows of x start at 2-byte offsets when K % 8 != 0) are
 // loaded element by element. Commits one copy group.
+// Position of x vector i in a swizzled row: bit 1 flips with bit 3, so the
+// four 64-byte-apart vectors that the lanes of an INT4 row team read at once
+// fall on distinct banks (with rows 16 bytes apart mod 128).
+__device__ __forceinline__ int xswz(int i) { return i ^ (((i >> 3) & 1) << 1); }
+
+template <bool SWZ = false>
 __device__ __forceinline__ void stage_x(uint16_t* xs, int xstride, const uint16_t* __restrict__ x,
                                         int B, int64_t K, int64_t c0, int nv) {
     const int items = B * nv;
@@ -100,7 +107,7 @@ __device__ __forceinline__ void stage_x(uint16_t* xs, int xstride, const uint16_
         const int i = it - b * nv;
         const int64_t col = c0 + 8 * static_cast<int64_t>(i);
         const uint16_t* src = x + static_cast<int64_t>(b) * K + col;
-        uint16_t* dst = xs + static_cast<int64_t>(b) * xstride + 8 * i;
+        uint16_t* dst = xs + static_cast<int64_t>(b) * xstride + 8 * (SWZ ? xswz(i) : i);
         if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
             cp_async16(dst, src, (col + 8 <= K) ? 16 : static_cast<int>(K - col) * 2);
         } else {

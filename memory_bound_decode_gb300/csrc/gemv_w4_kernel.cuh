@@ -21,7 +21,8 @@
 // 32-bit word) sum exactly one group, which is then scaled by the row's
 // S[n][group] and added to the running FP32 tile. As in the BF16 tensor-core
 // kernel, a fixed permutation of k pairs each lane's dequantised codes with the
-// x values in the same columns (one 16-byte shared-memory read of x per word),
+// x values in the same columns (one 16-byte shared-memory read of x per word;
+// x rows are swizzled so the four lanes of a row team hit distinct banks),
 // x is staged per CTA with asynchronous copies, the first batch of loads goes
 // out before the programmatic-dependent-launch wait, and partial sums combine
 // in a fixed order over warps and cluster CTAs.
@@ -141,7 +142,7 @@ gemv_w4_kernel(const __grid_constant__ Params p) {
 #pragma unroll
     for (int u = 0; u < UJ; ++u) issue(u, ch.c0, rg.j_begin + u, u < rg.my_groups);
     pdl_wait_prerequisites();
-    stage_x(xs, xstride, p.x, B, K, ch.c0, ch.nv);
+    stage_x<true>(xs, xstride, p.x, B, K, ch.c0, ch.nv);
 
 #pragma unroll 1
     for (int c = 0;; ++c) {
@@ -151,7 +152,7 @@ gemv_w4_kernel(const __grid_constant__ Params p) {
         Chunk nch{};
         if (more) {
             nch = chunk_at(next_c0, k1, p.kchunk, K);
-            stage_x(xs + ((c + 1) & 1) * xbuf, xstride, p.x, B, K, nch.c0, nch.nv);
+            stage_x<true>(xs + ((c + 1) & 1) * xbuf, xstride, p.x, B, K, nch.c0, nch.nv);
             cp_async_wait<1>();
         } else {
             cp_async_wait<0>();
@@ -184,7 +185,7 @@ gemv_w4_kernel(const __grid_constant__ Params p) {
 #pragma unroll
                     for (int nb = 0; nb < NB; ++nb) {
                         const int b = (nb * 8 + g < B) ? nb * 8 + g : B - 1;
-                        const uint4 xr = *reinterpret_cast<const uint4*>(xbuf0 + b * xstride + 8 * (vb + m));
+                        const uint4 xr = *reinterpret_cast<const uint4*>(xbuf0 + b * xstride + 8 * xswz(vb + m));
                         mma_bf16_16816(d[nb], A[0], Bq[0], A[1], Bq[1], xr.x, xr.y);
                         mma_bf16_16816(d[nb], A[2], Bq[2], A[3], Bq[3], xr.z, xr.w);
                     }

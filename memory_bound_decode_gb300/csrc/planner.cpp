@@ -29,6 +29,7 @@ constexpr int64_t kTargetInflightPerSm = 64 * 1024;
 constexpr int64_t kXBudgetBytes = 80 * 1024;   // staged x per CTA, all buffers
 constexpr int64_t kSliceGrain = 256;           // K-slices and chunks are multiples of this
 constexpr int kMmaXPad = 32;                   // per-row padding of x: conflict-free fragment reads
+constexpr int kW4XPad = 8;                     // INT4: rows 16 bytes apart mod 128 (with the swizzle)
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t m) { return cdiv(a, m) * m; }
@@ -58,12 +59,15 @@ int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weig
         cluster_first = true;
         xpad = kMmaXPad;
     } else {
+        // INT4: each byte carries four weights of dequantisation and MMA work, so
+        // the kernel is bound by the integer pipe, not by loads in flight; it asks
+        // for half the warps (counted as 8 KB each) and so fewer K-splits.
         group_rows = kMmaRows;
         unroll = kW4Unroll;
         batch_cols = static_cast<int64_t>(kW4Group) * kW4Unroll;   // one group per slot
-        warp_inflight = 32LL * 16 * kW4Unroll * 2;
+        warp_inflight = 2 * 32LL * 16 * kW4Unroll * 2;
         cluster_first = true;
-        xpad = kMmaXPad;
+        xpad = kW4XPad;
     }
     const int64_t target_warps = static_cast<int64_t>(sm_count) * kTargetInflightPerSm / warp_inflight;
     auto warps_for = [&](int kw, int splits) {
