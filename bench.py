@@ -68,13 +68,29 @@ def load_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+KERNEL_FILES = {   # the sources that make up each kernel family's launches
+    "fma": ("gemv_internal.h", "gemv_common.cuh", "gemv_kernel.cuh", "gemv_fma_instances.cu",
+            "gemv_dispatch.cu"),
+    "mma": ("gemv_internal.h", "gemv_common.cuh", "gemv_mma_kernel.cuh", "gemv_mma_instances_nb1.cu",
+            "gemv_mma_instances_nb2.cu", "gemv_dispatch.cu"),
+    "w4": ("gemv_internal.h", "gemv_common.cuh", "gemv_mma_kernel.cuh", "gemv_w4_kernel.cuh",
+           "gemv_w4_instances.cu", "gemv_dispatch.cu"),
+}
+
+
+def kernel_source_hash(family: str, launch: dict | None = None) -> str:
+    """Hash of one kernel family's sources and of the launch configuration the
+    planner picks for the workload (grid, splits, K slices, chunks): together
+    they decide the bytes a launch moves. Without a launch configuration (fused
+    and multi-launch workloads) the planner's source stands in for it."""
     csrc = os.path.join(ROOT, "memory_bound_decode_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".cpp", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    names = KERNEL_FILES[family] + (() if launch else ("planner.cpp",))
+    for name in names:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    if launch:
+        h.update(json.dumps(launch, sort_keys=True).encode())
     return h.hexdigest()[:16]
 
 
@@ -371,27 +387,34 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
     value = total_bytes / seconds / 1e9
     per_launch_s = seconds / (steps * wk.launches_per_step)
 
-    # end to end through the public call: pinned x in, GEMV, y out, synchronized
+    # end to end through the public call: pinned host x in, GEMV, host y out,
+    # synchronized, every step (gemv_bf16_host_io for single BF16 matrices)
     e2e = None
     if not args.no_e2e and kind != "step":
         x_host = wk.x.cpu().pin_memory()
         y_host = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in wk.ys]
         x_dev = torch.empty_like(wk.x)
         e2e_steps = max(10, min(steps, 2000))
+        host_io = kind == "single" and not getattr(wk, "w4", False)
+        sh = stream.cuda_stream
+
+        def e2e_step(i):
+            if host_io:
+                binding.gemv_bf16_host_io(wk.Ws[i % wk.copies][0], x_host, y_host[0], x_dev, wk.ys[0],
+                                          wk.N, wk.K, wk.B, wk.ldw, rms_eps=wk.rms_eps, stream=sh)
+            else:
+                x_dev.copy_(x_host, non_blocking=True)
+                wk.step(i, stream, x_dev)
+                for yh, yd in zip(y_host, wk.ys):
+                    yh.copy_(yd, non_blocking=True)
+                stream.synchronize()
+
         for i in range(5):
-            x_dev.copy_(x_host, non_blocking=True)
-            wk.step(i, stream, x_dev)
-            for yh, yd in zip(y_host, wk.ys):
-                yh.copy_(yd, non_blocking=True)
-            stream.synchronize()
+            e2e_step(i)
         barrier()
         t0 = time.perf_counter()
         for i in range(e2e_steps):
-            x_dev.copy_(x_host, non_blocking=True)
-            wk.step(i, stream, x_dev)
-            for yh, yd in zip(y_host, wk.ys):
-                yh.copy_(yd, non_blocking=True)
-            stream.synchronize()
+            e2e_step(i)
         e2e_s = max_over_ranks(time.perf_counter() - t0, dist, device)
         e2e = {"value": round(wk.bytes_per_step * e2e_steps * world / e2e_s / 1e9, 2), "unit": UNIT,
                "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
@@ -407,7 +430,13 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
     peak, peak_kind = load_peaks()
     achieved = wk.bytes_per_step / (seconds / steps) / 1e9 if kind == "step" else \
         wk.bytes_per_step / per_launch_s / 1e9
-    src_hash = kernel_source_hash()
+    family = "w4" if getattr(wk, "w4", False) else "fma" if wk.B == 1 else "mma"
+    launch = None
+    if kind == "single":
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        query = binding.gemv_w4_query_launch if family == "w4" else binding.gemv_query_launch
+        launch = query(wk.N, wk.K, wk.B, sms)
+    src_hash = kernel_source_hash(family, launch)
     traffic = profiled_traffic(args.workload, src_hash)
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,

@@ -108,6 +108,20 @@ int gemv_bf16_ex(const void *W, const void *x, float *y,
                  const gemv_options *opt, void *stream);
 
 /*
+ * gemv_bf16_ex for a caller whose activations live in host memory: copies x
+ * from x_host (B*K BF16, pinned memory recommended) to the device buffer x_dev,
+ * runs the GEMV into the device buffer y_dev, copies y back to y_host (B*N
+ * floats) and waits for the stream, so y_host holds the result on return. The
+ * device buffers are the caller's (x_dev B*K BF16, 16-byte aligned; y_dev B*N
+ * floats); the library allocates nothing. This is the whole host-to-host path
+ * of one decode-step projection, timed end to end by the benchmark.
+ */
+int gemv_bf16_host_io(const void *W, const void *x_host, float *y_host,
+                      void *x_dev, float *y_dev,
+                      int64_t N, int64_t K, int B, int64_t ldw,
+                      const gemv_options *opt, void *stream);
+
+/*
  * One weight matrix of a fused launch: y_i = W_i · x, W_i [N_i, ldw_i], y_i
  * [B, N_i] (row stride N_i).
  */

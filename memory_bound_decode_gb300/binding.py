@@ -30,7 +30,8 @@ GEMV_MAX_SEGMENTS = 8
 GEMV_FLAG_RMSNORM = 1
 
 EXPORTED = [
-    "gemv_bf16", "gemv_bf16_ex", "gemv_bf16_multi", "gemv_bf16_multi_ex", "gemv_plan_create", "gemv_plan_capture",
+    "gemv_bf16", "gemv_bf16_ex", "gemv_bf16_host_io", "gemv_bf16_multi", "gemv_bf16_multi_ex",
+    "gemv_plan_create", "gemv_plan_capture",
     "gemv_plan_launch", "gemv_plan_num_launches", "gemv_plan_destroy",
     "gemv_query_launch", "gemv_w4_bf16", "gemv_w4_query_launch",
     "gemv_probe_stream_read", "gemv_probe_sink_words",
@@ -95,6 +96,8 @@ def lib() -> ctypes.CDLL:
                                        ctypes.POINTER(gemv_options), vp]
             L.gemv_bf16_multi_ex.argtypes = [ctypes.POINTER(gemv_segment), ctypes.c_int, vp, i64,
                                              ctypes.c_int, ctypes.POINTER(gemv_options), vp]
+            L.gemv_bf16_host_io.argtypes = [vp, vp, vp, vp, vp, i64, i64, ctypes.c_int, i64,
+                                            ctypes.POINTER(gemv_options), vp]
             L.gemv_plan_create.argtypes = [ctypes.POINTER(gemv_proj), ctypes.c_int,
                                            ctypes.POINTER(vp)]
             L.gemv_plan_capture.argtypes = [vp, vp]
@@ -170,6 +173,14 @@ def gemv_bf16_ex(W, x, y, N: int, K: int, B: int, ldw: int, rms_eps=None, stream
     opt = ctypes.byref(options) if options is not None else _options(rms_eps)
     rc = lib().gemv_bf16_ex(_ptr(W), _ptr(x), _ptr(y), N, K, B, ldw, opt, _stream(stream))
     return _check(rc, "gemv_bf16_ex") if check else rc
+
+
+def gemv_bf16_host_io(W, x_host, y_host, x_dev, y_dev, N: int, K: int, B: int, ldw: int, rms_eps=None,
+                      stream=None, check: bool = True) -> int:
+    """Host x in, host y out, synchronous (see gemv.h)."""
+    rc = lib().gemv_bf16_host_io(_ptr(W), _ptr(x_host), _ptr(y_host), _ptr(x_dev), _ptr(y_dev), N, K, B, ldw,
+                                 _options(rms_eps), _stream(stream))
+    return _check(rc, "gemv_bf16_host_io") if check else rc
 
 
 def gemv_bf16_multi_ex(segments, x, K: int, B: int, rms_eps=None, stream=None, check: bool = True,

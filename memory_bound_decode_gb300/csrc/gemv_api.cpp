@@ -234,6 +234,26 @@ int gemv_bf16_ex(const void* W, const void* x, float* y, int64_t N, int64_t K, i
     return run(pr, static_cast<cudaStream_t>(stream));
 }
 
+int gemv_bf16_host_io(const void* W, const void* x_host, float* y_host, void* x_dev, float* y_dev,
+                      int64_t N, int64_t K, int B, int64_t ldw, const gemv_options* opt, void* stream) {
+    if (!x_host || !y_host) return GEMV_ERR_INVALID;
+    int rc = check_common(x_dev, K, B);
+    if (rc != GEMV_OK) return rc;
+    if ((rc = check_matrix(W, y_dev, N, K, ldw)) != GEMV_OK) return rc;
+    int flags = 0;
+    float eps = 0.f;
+    if ((rc = check_options(opt, &flags, &eps)) != GEMV_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t xbytes = static_cast<size_t>(B) * static_cast<size_t>(K) * 2;
+    const size_t ybytes = static_cast<size_t>(B) * static_cast<size_t>(N) * 4;
+    cudaError_t e = cudaMemcpyAsync(x_dev, x_host, xbytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if ((rc = gemv_bf16_ex(W, x_dev, y_dev, N, K, B, ldw, opt, stream)) != GEMV_OK) return rc;
+    if ((e = cudaMemcpyAsync(y_host, y_dev, ybytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e);
+    return GEMV_OK;
+}
+
 int gemv_bf16(const void* W, const void* x, float* y, int64_t N, int64_t K, int B, int64_t ldw,
               void* stream) {
     return gemv_bf16_ex(W, x, y, N, K, B, ldw, nullptr, stream);

@@ -6,7 +6,8 @@
 // registers while the next loads are outstanding. Unpacking four bits into an
 // FP32 multiply-add costs more issue slots per weight byte than the CUDA cores
 // have at HBM speed, so every batch size (1..16) runs the contraction on the
-// BF16 tensor cores; the dequantisation is two instructions per pair of codes.
+// BF16 tensor cores; the dequantisation is a shift, one three-input logic
+// operation and one BF16 subtraction per pair of codes.
 //
 // Weight layout (see include/gemv.h): per row, 32-bit words of eight codes,
 // even k in the low half-word, odd k in the high half-word, so that
@@ -43,11 +44,14 @@ __device__ __forceinline__ uint16_t ld_stream_u16(const uint16_t* p) {
 }
 
 // Four BF16 pairs (u - 8) from one word of eight codes: out[j] holds the codes
-// of columns 8w + 2j (low half) and 8w + 2j + 1 (high half).
+// of columns 8w + 2j (low half) and 8w + 2j + 1 (high half). The mask and the
+// exponent bits go in one three-input logic operation ((a & b) | c, truth table
+// 0xEA); written as two C++ operators after a shift they cost two.
 __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&out)[4]) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const uint32_t biased = ((w >> (4 * j)) & 0x000F000Fu) | 0x43004300u;   // 128 + u
+        uint32_t biased;   // 128 + u, both halves
+        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(biased) : "r"(w >> (4 * j)), "r"(0x000F000Fu), "r"(0x43004300u));
         uint32_t q;
         asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(q) : "r"(biased), "r"(0x43084308u));  // - 136
         out[j] = q;
@@ -97,10 +101,12 @@ gemv_w4_kernel(const __grid_constant__ Params p) {
     int64_t n0 = tile_row0 + g, n1 = tile_row0 + g + 8;
     n0 = n0 < sg.N ? n0 : sg.N - 1;   // rows past N stream a valid row; results dropped
     n1 = n1 < sg.N ? n1 : sg.N - 1;
-    const uint8_t* q0row = Wq + n0 * sg.ldw;   // ldw is the row stride in bytes here
-    const uint8_t* q1row = Wq + n1 * sg.ldw;
-    const uint16_t* s0row = Sseg + n0 * lds;
-    const uint16_t* s1row = Sseg + n1 * lds;
+    // This lane's 16-byte slice (columns 32t .. 32t+31 of a group) of rows n0 and
+    // n1 at column 0; ldw is the row stride in bytes here.
+    const uint8_t* q0p = Wq + n0 * sg.ldw + 16 * t;
+    const uint8_t* q1p = Wq + n1 * sg.ldw + 16 * t;
+    const uint16_t* s0p = Sseg + n0 * lds;
+    const uint16_t* s1p = Sseg + n1 * lds;
 
     const int xstride = p.xstride;
     const int xbuf = B * xstride;
@@ -109,6 +115,18 @@ gemv_w4_kernel(const __grid_constant__ Params p) {
     float* cpart = red + rows_per_cta * (B + 1) * kw;
     float* misc = cpart + rows_per_cta * B;
     const bool norm = (p.flags & kFlagRmsNorm) != 0;
+
+    // Byte offset, within one staged x buffer, of the 8 columns that word m of
+    // this lane's slice multiplies in group 0: batch row b, vector 4t + m at its
+    // swizzled place xswz(16 j + 4t + m) = 16 j + 4t + (m ^ (t & 2)). Group j
+    // adds 256 bytes.
+    uint32_t xo[NB][4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        const int b = (nb * 8 + g < B) ? nb * 8 + g : B - 1;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) xo[nb][m] = 2u * static_cast<uint32_t>(b * xstride + 8 * (4 * t + (m ^ (t & 2))));
+    }
 
     const int64_t K = p.K;
     const int64_t k0 = static_cast<int64_t>(split) * p.kslice;
@@ -122,31 +140,83 @@ gemv_w4_kernel(const __grid_constant__ Params p) {
 
     uint4 qa[UJ], qb[UJ];
     uint16_t sa[UJ], sb[UJ];
-    bool ok[UJ];
+    int rg_begin = 0;   // first group of this warp's range in the current chunk
 
-    // Issue slot u: group j of the chunk starting at column c0. Loads are never
-    // conditional: an out-of-range slot reads the row's first group and is
-    // dropped when consumed.
-    auto issue = [&](int u, int64_t c0, int j, bool in_range) {
-        ok[u] = in_range;
-        const int64_t col = in_range ? c0 + 128LL * j : 0;
-        qa[u] = ld_stream16(reinterpret_cast<const uint16_t*>(q0row + col / 2 + 16 * t));
-        qb[u] = ld_stream16(reinterpret_cast<const uint16_t*>(q1row + col / 2 + 16 * t));
-        sa[u] = ld_stream_u16(s0row + col / 128);
-        sb[u] = ld_stream_u16(s1row + col / 128);
+    // Issue the slots of groups jr .. jr+UJ-1 of this warp's range (chunk at c0).
+    // A full batch addresses its slots by immediate offsets; the last, partial
+    // batch repeats its last group in the unused slots, which are not consumed.
+    auto issue = [&](int64_t c0, int jr, int my) {
+        const int rem = my - jr;
+        if (rem <= 0) return;
+        const int64_t col0 = c0 + 128LL * (rg_begin + jr);
+        const uint8_t* a0 = q0p + (col0 >> 1);
+        const uint8_t* a1 = q1p + (col0 >> 1);
+        const uint16_t* z0 = s0p + (col0 >> 7);
+        const uint16_t* z1 = s1p + (col0 >> 7);
+        if (rem >= UJ) {
+#pragma unroll
+            for (int u = 0; u < UJ; ++u) {
+                qa[u] = ld_stream16(reinterpret_cast<const uint16_t*>(a0 + 64 * u));
+                qb[u] = ld_stream16(reinterpret_cast<const uint16_t*>(a1 + 64 * u));
+                sa[u] = ld_stream_u16(z0 + u);
+                sb[u] = ld_stream_u16(z1 + u);
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < UJ; ++u) {
+                const int uu = u < rem ? u : rem - 1;
+                qa[u] = ld_stream16(reinterpret_cast<const uint16_t*>(a0 + 64 * uu));
+                qb[u] = ld_stream16(reinterpret_cast<const uint16_t*>(a1 + 64 * uu));
+                sa[u] = ld_stream_u16(z0 + uu);
+                sb[u] = ld_stream_u16(z1 + uu);
+            }
+        }
+    };
+
+    // Contract slot u (one 128-column group of rows n0, n1) with x at xg (the
+    // staged x of this batch's first group) and add it, scaled, to acc.
+    auto consume = [&](int u, const unsigned char* xg) {
+        float d[NB][4];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d[nb][i] = 0.f;
+        const uint32_t wa[4] = {qa[u].x, qa[u].y, qa[u].z, qa[u].w};
+        const uint32_t wb[4] = {qb[u].x, qb[u].y, qb[u].z, qb[u].w};
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            uint32_t A[4], Bq[4];
+            dequant_word(wa[m], A);
+            dequant_word(wb[m], Bq);
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+                const uint4 xr = *reinterpret_cast<const uint4*>(xg + xo[nb][m] + 256 * u);
+                mma_bf16_16816(d[nb], A[0], Bq[0], A[1], Bq[1], xr.x, xr.y);
+                mma_bf16_16816(d[nb], A[2], Bq[2], A[3], Bq[3], xr.z, xr.w);
+            }
+        }
+        const float s_a = __uint_as_float(static_cast<uint32_t>(sa[u]) << 16);
+        const float s_b = __uint_as_float(static_cast<uint32_t>(sb[u]) << 16);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            acc[nb][0] = fmaf(d[nb][0], s_a, acc[nb][0]);
+            acc[nb][1] = fmaf(d[nb][1], s_a, acc[nb][1]);
+            acc[nb][2] = fmaf(d[nb][2], s_b, acc[nb][2]);
+            acc[nb][3] = fmaf(d[nb][3], s_b, acc[nb][3]);
+        }
     };
 
     Chunk ch = chunk_at(k0, k1, p.kchunk, K);
     int ngroups = (ch.nv + 15) >> 4;
     W4Range rg = w4_range(ngroups, kw, kq);
-#pragma unroll
-    for (int u = 0; u < UJ; ++u) issue(u, ch.c0, rg.j_begin + u, u < rg.my_groups);
+    rg_begin = rg.j_begin;
+    issue(ch.c0, 0, rg.my_groups);
     pdl_wait_prerequisites();
     stage_x<true>(xs, xstride, p.x, B, K, ch.c0, ch.nv);
 
 #pragma unroll 1
     for (int c = 0;; ++c) {
-        const uint16_t* xbuf0 = xs + (c & 1) * xbuf;
+        const unsigned char* xsb = reinterpret_cast<const unsigned char*>(xs + (c & 1) * xbuf);
         const int64_t next_c0 = ch.c0 + p.kchunk;
         const bool more = CHUNKED && next_c0 < k1;
         Chunk nch{};
@@ -159,58 +229,29 @@ gemv_w4_kernel(const __grid_constant__ Params p) {
         }
         __syncthreads();
 
+        const int my = rg.my_groups;
 #pragma unroll 1
-        for (int j0 = 0; j0 < rg.my_groups; j0 += UJ) {
-            if (j0 > 0) {
+        for (int j0 = 0; j0 < my; j0 += UJ) {
+            if (j0 > 0) issue(ch.c0, j0, my);
+            const unsigned char* xg = xsb + 256 * (rg_begin + j0);
+            const int rem = my - j0;
+            if (rem >= UJ) {
+#pragma unroll
+                for (int u = 0; u < UJ; ++u) consume(u, xg);
+            } else {
 #pragma unroll
                 for (int u = 0; u < UJ; ++u)
-                    issue(u, ch.c0, rg.j_begin + j0 + u, j0 + u < rg.my_groups);
-            }
-#pragma unroll
-            for (int u = 0; u < UJ; ++u) {
-                const int j = rg.j_begin + j0 + u;
-                const int vb = ok[u] ? 16 * j + 4 * t : 0;   // vector of x at column 128 j + 32 t
-                float d[NB][4];
-#pragma unroll
-                for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) d[nb][i] = 0.f;
-                const uint32_t wa[4] = {qa[u].x, qa[u].y, qa[u].z, qa[u].w};
-                const uint32_t wb[4] = {qb[u].x, qb[u].y, qb[u].z, qb[u].w};
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    uint32_t A[4], Bq[4];
-                    dequant_word(wa[m], A);
-                    dequant_word(wb[m], Bq);
-#pragma unroll
-                    for (int nb = 0; nb < NB; ++nb) {
-                        const int b = (nb * 8 + g < B) ? nb * 8 + g : B - 1;
-                        const uint4 xr = *reinterpret_cast<const uint4*>(xbuf0 + b * xstride + 8 * xswz(vb + m));
-                        mma_bf16_16816(d[nb], A[0], Bq[0], A[1], Bq[1], xr.x, xr.y);
-                        mma_bf16_16816(d[nb], A[2], Bq[2], A[3], Bq[3], xr.z, xr.w);
-                    }
-                }
-                if (ok[u]) {
-                    const float s_a = __uint_as_float(static_cast<uint32_t>(sa[u]) << 16);
-                    const float s_b = __uint_as_float(static_cast<uint32_t>(sb[u]) << 16);
-#pragma unroll
-                    for (int nb = 0; nb < NB; ++nb) {
-                        acc[nb][0] = fmaf(d[nb][0], s_a, acc[nb][0]);
-                        acc[nb][1] = fmaf(d[nb][1], s_a, acc[nb][1]);
-                        acc[nb][2] = fmaf(d[nb][2], s_b, acc[nb][2]);
-                        acc[nb][3] = fmaf(d[nb][3], s_b, acc[nb][3]);
-                    }
-                }
+                    if (u < rem) consume(u, xg);
             }
         }
-        if (norm) xsq_accumulate(xbuf0, xstride, B, ch.nv, misc, c == 0);
+        if (norm) xsq_accumulate(reinterpret_cast<const uint16_t*>(xsb), xstride, B, ch.nv, misc, c == 0);
         if (!more) break;
 
         ch = nch;
         ngroups = (ch.nv + 15) >> 4;
         rg = w4_range(ngroups, kw, kq);
-#pragma unroll
-        for (int u = 0; u < UJ; ++u) issue(u, ch.c0, rg.j_begin + u, u < rg.my_groups);
+        rg_begin = rg.j_begin;
+        issue(ch.c0, 0, rg.my_groups);
         __syncthreads();
     }
 

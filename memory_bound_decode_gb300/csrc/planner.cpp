@@ -59,13 +59,10 @@ int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weig
         cluster_first = true;
         xpad = kMmaXPad;
     } else {
-        // INT4: each byte carries four weights of dequantisation and MMA work, so
-        // the kernel is bound by the integer pipe, not by loads in flight; it asks
-        // for half the warps (counted as 8 KB each) and so fewer K-splits.
         group_rows = kMmaRows;
         unroll = kW4Unroll;
         batch_cols = static_cast<int64_t>(kW4Group) * kW4Unroll;   // one group per slot
-        warp_inflight = 2 * 32LL * 16 * kW4Unroll * 2;
+        warp_inflight = 32LL * 16 * kW4Unroll * 2;
         cluster_first = true;
         xpad = kW4XPad;
     }
@@ -79,7 +76,20 @@ int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weig
     };
 
     int kw = 1, splits = 1;
-    if (cluster_first) {
+    if (path == kPathW4 && B == 1) {
+        // INT4, one activation row: two warps along K first, then CTAs along K
+        // (measured best on the decode shapes).
+        while (kw < 2 && warps_for(kw, splits) < target_warps && room(kw, splits)) kw *= 2;
+        while (splits < 4 && warps_for(kw, splits) < target_warps && room(kw, splits)) splits *= 2;
+        while (kw < kWarps && warps_for(kw, splits) < target_warps && room(kw, splits)) kw *= 2;
+        while (splits < kMaxSplits && warps_for(kw, splits) < target_warps && room(kw, splits)) splits *= 2;
+    } else if (path == kPathW4) {
+        // INT4, several rows: warps along K would each re-read the CTA's B rows
+        // of x from shared memory for fewer weight rows, so only CTAs along K;
+        // from 8 rows on, at least two, which halves each CTA's staged x.
+        while (splits < kMaxSplits && warps_for(kw, splits) < target_warps && room(kw, splits)) splits *= 2;
+        if (B >= 8 && splits == 1 && room(kw, splits)) splits = 2;
+    } else if (cluster_first) {
         while (splits < 4 && warps_for(kw, splits) < target_warps && room(kw, splits)) splits *= 2;
         while (kw < kWarps && warps_for(kw, splits) < target_warps && room(kw, splits)) kw *= 2;
         while (splits < kMaxSplits && warps_for(kw, splits) < target_warps && room(kw, splits)) splits *= 2;

@@ -198,3 +198,12 @@ def test_w4_plan_covers_the_problem(L, N, K, B):
     assert q["kslice"] % 128 == 0 and q["kchunk"] % 128 == 0      # groups never straddle
     with pytest.raises(binding.GemvError):
         binding.gemv_w4_query_launch(N, 100, B, GB300_SMS)
+
+
+def test_host_io_rejects(L):
+    ok = dict(stream=0, check=False)
+    f = binding.gemv_bf16_host_io
+    assert f(A16, 0, A16, A16, A16, 8, 8, 1, 8, **ok) == binding.GEMV_ERR_INVALID        # x_host NULL
+    assert f(A16, A16, 0, A16, A16, 8, 8, 1, 8, **ok) == binding.GEMV_ERR_INVALID        # y_host NULL
+    assert f(A16, A16, A16, 0, A16, 8, 8, 1, 8, **ok) == binding.GEMV_ERR_INVALID        # x_dev NULL
+    assert f(A16, A16, A16, A16, A16 + 2, 8, 8, 1, 8, **ok) == binding.GEMV_ERR_ALIGN    # y_dev

@@ -192,3 +192,19 @@ def test_probe_stream_read_runs():
     binding.gemv_probe_stream_read(src, nbytes, sink)
     torch.cuda.synchronize()
     assert torch.isfinite(sink[:152]).all()
+
+
+def test_host_io_round_trip():
+    N, K, B = 4096, 14336, 2
+    W, x, ldw = make(N, K, B, seed=12)
+    x_host = x.cpu().pin_memory()
+    y_host = torch.full((B, N), float("nan")).pin_memory()
+    x_dev = torch.empty_like(x)
+    y_dev = torch.empty((B, N), device=DEV)
+    s = torch.cuda.Stream()
+    binding.gemv_bf16_host_io(W, x_host, y_host, x_dev, y_dev, N, K, B, ldw, stream=s)
+    # synchronous: the host buffer already holds the result
+    y_ref, sc = gu.reference(W, x, K)
+    gu.assert_parity(y_host.numpy(), y_ref, sc)
+    binding.gemv_bf16_host_io(W, x_host, y_host, x_dev, y_dev, N, K, B, ldw, rms_eps=1e-5, stream=s)
+    assert np.isfinite(y_host.numpy()).all()
