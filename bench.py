@@ -75,6 +75,8 @@ KERNEL_FILES = {   # the sources that make up each kernel family's launches
             "gemv_mma_instances_nb2.cu", "gemv_dispatch.cu"),
     "w4": ("gemv_internal.h", "gemv_common.cuh", "gemv_mma_kernel.cuh", "gemv_w4_kernel.cuh",
            "gemv_w4_instances.cu", "gemv_dispatch.cu"),
+    "sk": ("gemv_internal.h", "gemv_common.cuh", "gemv_kernel.cuh", "gemv_streamk_kernel.cuh",
+           "gemv_streamk_instances.cu", "gemv_dispatch.cu"),
 }
 
 
@@ -193,10 +195,22 @@ def split_w4(workload: str) -> tuple[str, bool]:
     return workload, False
 
 
+SK_PREFIX = "sk:"
+
+
+def split_sk(workload: str) -> tuple[str, bool]:
+    """A workload name may start with "sk:": the same BF16 batch-1 projections
+    through the stream-K kernel (GEMV_FLAG_STREAMK)."""
+    if workload.startswith(SK_PREFIX):
+        return workload[len(SK_PREFIX):], True
+    return workload, False
+
+
 def describe(workload: str):
     """(kind, N-list, K, B) of a named workload."""
     from memory_bound_decode_gb300 import workloads as wl
     workload, _ = split_norm(workload)
+    workload, _ = split_sk(workload)
     workload, _ = split_w4(workload)
     if workload in ("down_proj", "k_proj", "o_proj", "lm_head"):
         N, K = wl.SHAPES[workload]
@@ -219,12 +233,15 @@ def describe(workload: str):
 class GemvWorkload:
     """Rotating device-resident weight copies for one (possibly fused) GEMV."""
 
-    def __init__(self, kind, rows, K, B, device, l2_bytes, rms_eps=None, w4=False):
+    def __init__(self, kind, rows, K, B, device, l2_bytes, rms_eps=None, w4=False, streamk=False):
         import torch
         from memory_bound_decode_gb300 import inputs, roofline
         self.kind, self.rows, self.K, self.B = kind, rows, K, B
         self.rms_eps = rms_eps
         self.w4 = w4
+        self.streamk = streamk
+        if streamk and (w4 or B != 1):
+            raise SystemExit("stream-K: BF16 batch-1 workloads only")
         self.N = sum(rows)
         if w4:
             if kind != "single":
@@ -257,23 +274,25 @@ class GemvWorkload:
             Wq, S = Ws[0]
             binding.gemv_w4_bf16(Wq, S, x, self.ys[0], self.N, self.K, self.B, self.ldq, self.lds,
                                  rms_eps=self.rms_eps, stream=stream)
-        elif self.kind == "single" and self.rms_eps is None:
+        elif self.kind == "single" and self.rms_eps is None and not self.streamk:
             binding.gemv_bf16(Ws[0], x, self.ys[0], self.N, self.K, self.B, self.ldw, stream)
         elif self.kind == "single":
             binding.gemv_bf16_ex(Ws[0], x, self.ys[0], self.N, self.K, self.B, self.ldw,
-                                 rms_eps=self.rms_eps, stream=stream)
-        elif self.rms_eps is None:
+                                 rms_eps=self.rms_eps, stream=stream, streamk=self.streamk)
+        elif self.rms_eps is None and not self.streamk:
             binding.gemv_bf16_multi([(W, y, n, self.ldw) for W, y, n in zip(Ws, self.ys, self.rows)],
                                     x, self.K, self.B, stream)
         else:
             binding.gemv_bf16_multi_ex([(W, y, n, self.ldw) for W, y, n in zip(Ws, self.ys, self.rows)],
-                                       x, self.K, self.B, rms_eps=self.rms_eps, stream=stream)
+                                       x, self.K, self.B, rms_eps=self.rms_eps, stream=stream,
+                                       streamk=self.streamk)
 
     def config(self) -> dict:
         shape = "+".join(str(n) for n in self.rows)
         norm = f", RMSNorm prologue eps={self.rms_eps}" if self.rms_eps is not None else ""
         wt = "INT4-weight (128-col groups, BF16 scales)" if self.w4 else "BF16"
-        return {"workload": f"{self.kind} {wt} GEMV N={shape} K={self.K} B={self.B}{norm}",
+        sk = ", stream-K one-wave grid" if self.streamk else ""
+        return {"workload": f"{self.kind} {wt} GEMV N={shape} K={self.K} B={self.B}{norm}{sk}",
                 "N": self.N, "K": self.K, "B": self.B,
                 "ldw": self.ldq if self.w4 else self.ldw,
                 "segments": len(self.rows),
@@ -284,12 +303,13 @@ class GemvWorkload:
 class StepWorkload:
     """The full decode-step projection set replayed as one CUDA graph."""
 
-    def __init__(self, device, stream, rms_eps=None):
+    def __init__(self, device, stream, rms_eps=None, streamk=False):
         from memory_bound_decode_gb300 import workloads as wl
         self.spec = wl.decode_step_spec()
         self.data = wl.DecodeStep(self.spec, seed=0, device=device)
         self.rms_eps = rms_eps
-        self.plan = self.data.plan(rms_eps=rms_eps)
+        self.streamk = streamk
+        self.plan = self.data.plan(rms_eps=rms_eps, streamk=streamk)
         self.plan.capture(stream)
         self.bytes_per_step = wl.step_bytes_formula(self.spec)
         self.launches_per_step = self.plan.num_launches()
@@ -354,9 +374,10 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
 
     kind, rows, K, B = describe(args.workload)
     _, rms_eps = split_norm(args.workload)
-    _, w4 = split_w4(split_norm(args.workload)[0])
-    wk = StepWorkload(device, torch.cuda.Stream(), rms_eps) if kind == "step" else \
-        GemvWorkload(kind, rows, K, B, device, l2, rms_eps, w4)
+    base, streamk = split_sk(split_norm(args.workload)[0])
+    _, w4 = split_w4(base)
+    wk = StepWorkload(device, torch.cuda.Stream(), rms_eps, streamk) if kind == "step" else \
+        GemvWorkload(kind, rows, K, B, device, l2, rms_eps, w4, streamk)
     torch.cuda.synchronize()
 
     def barrier():
@@ -396,12 +417,14 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
         x_dev = torch.empty_like(wk.x)
         e2e_steps = max(10, min(steps, 2000))
         host_io = kind == "single" and not getattr(wk, "w4", False)
+        sk = getattr(wk, "streamk", False)
         sh = stream.cuda_stream
 
         def e2e_step(i):
             if host_io:
                 binding.gemv_bf16_host_io(wk.Ws[i % wk.copies][0], x_host, y_host[0], x_dev, wk.ys[0],
-                                          wk.N, wk.K, wk.B, wk.ldw, rms_eps=wk.rms_eps, stream=sh)
+                                          wk.N, wk.K, wk.B, wk.ldw, rms_eps=wk.rms_eps, stream=sh,
+                                          streamk=sk)
             else:
                 x_dev.copy_(x_host, non_blocking=True)
                 wk.step(i, stream, x_dev)
@@ -430,12 +453,16 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
     peak, peak_kind = load_peaks()
     achieved = wk.bytes_per_step / (seconds / steps) / 1e9 if kind == "step" else \
         wk.bytes_per_step / per_launch_s / 1e9
-    family = "w4" if getattr(wk, "w4", False) else "fma" if wk.B == 1 else "mma"
+    family = ("w4" if getattr(wk, "w4", False) else "sk" if getattr(wk, "streamk", False)
+              else "fma" if wk.B == 1 else "mma")
     launch = None
     if kind == "single":
         sms = torch.cuda.get_device_properties(device).multi_processor_count
-        query = binding.gemv_w4_query_launch if family == "w4" else binding.gemv_query_launch
-        launch = query(wk.N, wk.K, wk.B, sms)
+        if family == "w4":
+            launch = binding.gemv_w4_query_launch(wk.N, wk.K, wk.B, sms)
+        else:
+            launch = binding.gemv_query_launch_ex(wk.N, wk.K, wk.B, sms,
+                                                  binding.GEMV_FLAG_STREAMK if family == "sk" else 0)
     src_hash = kernel_source_hash(family, launch)
     traffic = profiled_traffic(args.workload, src_hash)
     result = {
@@ -451,7 +478,8 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_kind": f"{peak_kind} copy (MEASURED_PEAKS hbm_gbs, burst)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "kernel": ("gemv_w4_kernel (INT4 codes, BF16 tensor cores)" if getattr(wk, "w4", False)
+                     "kernel": ("gemv_w4_kernel (INT4 codes, BF16 tensor cores)" if family == "w4"
+                                else "gemv_streamk_kernel (CUDA cores, one-wave grid)" if family == "sk"
                                 else "gemv_bf16_kernel (CUDA cores)" if wk.B == 1
                                 else "gemv_bf16_mma_kernel (BF16 tensor cores)"),
                      "kernel_source_hash": src_hash},

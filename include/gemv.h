@@ -97,6 +97,26 @@ int gemv_bf16(const void *W, const void *x, float *y,
  */
 #define GEMV_FLAG_RMSNORM 1
 
+/*
+ * GEMV_FLAG_STREAMK: batch 1 only (x row of at most 24,576 columns). Run the
+ * stream-K kernel ("GPU performance chains", "Wave quantization"; "Decode GEMV
+ * at half of HBM bandwidth", cause 1): a grid of exactly one wave; rows that
+ * fill whole rounds of its warps go one per warp, the rest are cut into
+ * (row, 2,048-column) units shared out in equal, contiguous ranges; a row cut
+ * between warps is finished by the last of its warps to arrive, which adds
+ * their partial sums in warp order (results are bitwise reproducible; they may
+ * differ in the last bits from the default kernel, which cuts K differently).
+ * It needs a workspace of 8 bytes per warp of the grid plus 4 bytes per output
+ * row. Direct calls use a workspace the library owns per device: it is
+ * allocated (cudaMalloc, then zeroed; the call waits for the device) the first
+ * time a call needs more than it has, which must not happen while a stream is
+ * capturing (GEMV_ERR_CAPTURE), and it is freed by gemv_workspace_release.
+ * All direct stream-K calls on one device share it, so they must not run
+ * concurrently: issue them on one stream. A plan owns its own workspace.
+ * Combined with a batch of more than 1 or a longer x row: GEMV_ERR_UNSUPPORTED.
+ */
+#define GEMV_FLAG_STREAMK 2
+
 typedef struct {
     int flags;
     float rms_eps;
@@ -113,7 +133,8 @@ int gemv_bf16_ex(const void *W, const void *x, float *y,
  * runs the GEMV into the device buffer y_dev, copies y back to y_host (B*N
  * floats) and waits for the stream, so y_host holds the result on return. The
  * device buffers are the caller's (x_dev B*K BF16, 16-byte aligned; y_dev B*N
- * floats); the library allocates nothing. This is the whole host-to-host path
+ * floats); the library allocates nothing (but the stream-K workspace, see
+ * GEMV_FLAG_STREAMK). This is the whole host-to-host path
  * of one decode-step projection, timed end to end by the benchmark.
  */
 int gemv_bf16_host_io(const void *W, const void *x_host, float *y_host,
@@ -217,13 +238,30 @@ typedef struct {
     int32_t unroll;          /* loads per lane per row in flight before any is used */
     int32_t smem_bytes;      /* dynamic shared memory per CTA                     */
     int32_t path;            /* 0: CUDA-core FP32 FMA (batch 1), 1: BF16 tensor-core MMA,
-                                2: INT4 weights on the BF16 tensor cores */
+                                2: INT4 weights on the BF16 tensor cores,
+                                3: stream-K, batch 1 (CUDA cores, one-wave grid) */
     int32_t xstride;         /* shared-memory elements per staged x row           */
     int32_t nbuf;            /* x buffers: 2 when the K-range is staged in chunks */
+    /* stream-K (path 3) only; zero otherwise: */
+    int64_t units;           /* (row, 2,048-column) units of the split part       */
+    int64_t warps;           /* warps that take split-part units (equal ranges)   */
+    int32_t chunks;          /* units per row                                     */
+    int32_t ctas_per_sm;     /* resident CTAs per SM the one-wave grid assumes    */
+    int32_t dp_rounds;       /* rounds of whole rows, one per warp of the grid,
+                                taken before the split part                       */
 } gemv_launch_info;
 
 int gemv_query_launch(int64_t N, int64_t K, int B, int sm_count,
                       gemv_launch_info *out);
+
+/* gemv_query_launch for a call with option flags (GEMV_FLAG_STREAMK selects
+ * path 3; GEMV_ERR_UNSUPPORTED where that kernel does not apply). */
+int gemv_query_launch_ex(int64_t N, int64_t K, int B, int sm_count, int flags,
+                         gemv_launch_info *out);
+
+/* Free the stream-K workspace the library holds for the current device. No
+ * stream-K call on that device may be in flight. Returns GEMV_OK. */
+int gemv_workspace_release(void);
 
 /*
  * y = W·x with group-quantised INT4 weights ("Decode GEMV at half of HBM

@@ -28,12 +28,14 @@ GEMV_MAX_BATCH = 16
 GEMV_MAX_SEGMENTS = 8
 
 GEMV_FLAG_RMSNORM = 1
+GEMV_FLAG_STREAMK = 2
 
 EXPORTED = [
     "gemv_bf16", "gemv_bf16_ex", "gemv_bf16_host_io", "gemv_bf16_multi", "gemv_bf16_multi_ex",
     "gemv_plan_create", "gemv_plan_capture",
     "gemv_plan_launch", "gemv_plan_num_launches", "gemv_plan_destroy",
-    "gemv_query_launch", "gemv_w4_bf16", "gemv_w4_query_launch",
+    "gemv_query_launch", "gemv_query_launch_ex", "gemv_workspace_release",
+    "gemv_w4_bf16", "gemv_w4_query_launch",
     "gemv_probe_stream_read", "gemv_probe_sink_words",
     "gemv_status_string", "gemv_last_cuda_error",
 ]
@@ -61,7 +63,9 @@ class gemv_launch_info(ctypes.Structure):
                 ("kchunk", i64), ("warps_per_cta", ctypes.c_int32), ("warps_per_row", ctypes.c_int32),
                 ("splits", ctypes.c_int32), ("rows_per_warp", ctypes.c_int32),
                 ("unroll", ctypes.c_int32), ("smem_bytes", ctypes.c_int32), ("path", ctypes.c_int32),
-                ("xstride", ctypes.c_int32), ("nbuf", ctypes.c_int32)]
+                ("xstride", ctypes.c_int32), ("nbuf", ctypes.c_int32),
+                ("units", i64), ("warps", i64), ("chunks", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
+                ("dp_rounds", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -107,6 +111,9 @@ def lib() -> ctypes.CDLL:
             L.gemv_plan_destroy.restype = None
             L.gemv_query_launch.argtypes = [i64, i64, ctypes.c_int, ctypes.c_int,
                                             ctypes.POINTER(gemv_launch_info)]
+            L.gemv_query_launch_ex.argtypes = [i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.POINTER(gemv_launch_info)]
+            L.gemv_workspace_release.argtypes = []
             L.gemv_w4_bf16.argtypes = [vp, vp, vp, vp, i64, i64, ctypes.c_int, i64, i64,
                                        ctypes.POINTER(gemv_options), vp]
             L.gemv_w4_query_launch.argtypes = [i64, i64, ctypes.c_int, ctypes.c_int,
@@ -160,35 +167,36 @@ def gemv_bf16(W, x, y, N: int, K: int, B: int, ldw: int, stream=None, check: boo
     return _check(rc, "gemv_bf16") if check else rc
 
 
-def _options(rms_eps):
-    if rms_eps is None:
+def _options(rms_eps, streamk: bool = False):
+    if rms_eps is None and not streamk:
         return None
-    return ctypes.byref(gemv_options(GEMV_FLAG_RMSNORM, float(rms_eps)))
+    flags = (GEMV_FLAG_RMSNORM if rms_eps is not None else 0) | (GEMV_FLAG_STREAMK if streamk else 0)
+    return ctypes.byref(gemv_options(flags, float(rms_eps) if rms_eps is not None else 0.0))
 
 
 def gemv_bf16_ex(W, x, y, N: int, K: int, B: int, ldw: int, rms_eps=None, stream=None,
-                 check: bool = True, options=None) -> int:
-    """gemv_bf16 with options; ``rms_eps`` (not None) turns on the RMSNorm prologue.
-    ``options`` (a gemv_options) overrides ``rms_eps`` when given."""
-    opt = ctypes.byref(options) if options is not None else _options(rms_eps)
+                 check: bool = True, options=None, streamk: bool = False) -> int:
+    """gemv_bf16 with options; ``rms_eps`` (not None) turns on the RMSNorm prologue,
+    ``streamk`` the stream-K kernel. ``options`` (a gemv_options) overrides both."""
+    opt = ctypes.byref(options) if options is not None else _options(rms_eps, streamk)
     rc = lib().gemv_bf16_ex(_ptr(W), _ptr(x), _ptr(y), N, K, B, ldw, opt, _stream(stream))
     return _check(rc, "gemv_bf16_ex") if check else rc
 
 
 def gemv_bf16_host_io(W, x_host, y_host, x_dev, y_dev, N: int, K: int, B: int, ldw: int, rms_eps=None,
-                      stream=None, check: bool = True) -> int:
+                      stream=None, check: bool = True, streamk: bool = False) -> int:
     """Host x in, host y out, synchronous (see gemv.h)."""
     rc = lib().gemv_bf16_host_io(_ptr(W), _ptr(x_host), _ptr(y_host), _ptr(x_dev), _ptr(y_dev), N, K, B, ldw,
-                                 _options(rms_eps), _stream(stream))
+                                 _options(rms_eps, streamk), _stream(stream))
     return _check(rc, "gemv_bf16_host_io") if check else rc
 
 
 def gemv_bf16_multi_ex(segments, x, K: int, B: int, rms_eps=None, stream=None, check: bool = True,
-                       options=None) -> int:
+                       options=None, streamk: bool = False) -> int:
     arr = (gemv_segment * max(1, len(segments)))()
     for i, (W, y, N, ldw) in enumerate(segments):
         arr[i] = gemv_segment(_ptr(W), _ptr(y), N, ldw)
-    opt = ctypes.byref(options) if options is not None else _options(rms_eps)
+    opt = ctypes.byref(options) if options is not None else _options(rms_eps, streamk)
     rc = lib().gemv_bf16_multi_ex(arr, len(segments), _ptr(x), K, B, opt, _stream(stream))
     return _check(rc, "gemv_bf16_multi_ex") if check else rc
 
@@ -206,6 +214,16 @@ def gemv_query_launch(N: int, K: int, B: int, sm_count: int) -> dict:
     info = gemv_launch_info()
     _check(lib().gemv_query_launch(N, K, B, sm_count, ctypes.byref(info)), "gemv_query_launch")
     return info.as_dict()
+
+
+def gemv_query_launch_ex(N: int, K: int, B: int, sm_count: int, flags: int) -> dict:
+    info = gemv_launch_info()
+    _check(lib().gemv_query_launch_ex(N, K, B, sm_count, flags, ctypes.byref(info)), "gemv_query_launch_ex")
+    return info.as_dict()
+
+
+def gemv_workspace_release() -> int:
+    return _check(lib().gemv_workspace_release(), "gemv_workspace_release")
 
 
 def gemv_w4_bf16(Wq, S, x, y, N: int, K: int, B: int, ldq: int, lds: int, rms_eps=None,
@@ -233,10 +251,10 @@ def gemv_probe_stream_read(src, nbytes: int, sink, stream=None) -> int:
 class Plan:
     """Owner of a gemv_plan handle (gemv_plan_create / capture / launch / destroy).
 
-    ``projections``: sequence of (W, x, y, N, K, ldw, B, fuse_group) or
+    ``projections``: sequence of (W, x, y, N, K, ldw, B, fuse_group),
     (W, x, y, N, K, ldw, B, fuse_group, rms_eps) with rms_eps None for no
-    RMSNorm prologue. The tensors behind the pointers must outlive the plan;
-    keep them referenced.
+    RMSNorm prologue, or (..., rms_eps, streamk) with streamk a bool. The
+    tensors behind the pointers must outlive the plan; keep them referenced.
     """
 
     def __init__(self, projections, keepalive=None):
@@ -245,7 +263,8 @@ class Plan:
         for i, pr in enumerate(projections):
             W, x, y, N, K, ldw, B, grp = pr[:8]
             eps = pr[8] if len(pr) > 8 else None
-            flags = GEMV_FLAG_RMSNORM if eps is not None else 0
+            sk = bool(pr[9]) if len(pr) > 9 else False
+            flags = (GEMV_FLAG_RMSNORM if eps is not None else 0) | (GEMV_FLAG_STREAMK if sk else 0)
             arr[i] = gemv_proj(_ptr(W), _ptr(x), _ptr(y), N, K, ldw, B, grp, flags,
                                float(eps) if eps is not None else 0.0)
         handle = vp()

@@ -28,10 +28,20 @@ int cuda_fail(cudaError_t e) {
 
 constexpr int kMaxDevices = 64;
 
+// Device memory of the stream-K kernel: partial sums and per-row counters
+// (zero between launches).
+struct Workspace {
+    float* part = nullptr;
+    int32_t* ticket = nullptr;
+    int64_t part_cap = 0;
+    int64_t ticket_cap = 0;
+};
+
 struct DeviceState {
     bool ready = false;
     int status = GEMV_OK;
     int sm_count = 0;
+    Workspace ws;   // shared by direct stream-K calls on this device
 };
 
 std::mutex g_dev_mutex;
@@ -94,7 +104,7 @@ int check_options(const gemv_options* opt, int* flags, float* eps) {
     *flags = 0;
     *eps = 0.f;
     if (!opt) return GEMV_OK;
-    if (opt->flags & ~GEMV_FLAG_RMSNORM) return GEMV_ERR_INVALID;
+    if (opt->flags & ~(GEMV_FLAG_RMSNORM | GEMV_FLAG_STREAMK)) return GEMV_ERR_INVALID;
     if (opt->flags & GEMV_FLAG_RMSNORM) {
         if (!std::isfinite(opt->rms_eps) || opt->rms_eps < 0.f) return GEMV_ERR_INVALID;
         *eps = opt->rms_eps;
@@ -103,12 +113,84 @@ int check_options(const gemv_options* opt, int* flags, float* eps) {
     return GEMV_OK;
 }
 
-// One prepared launch: parameters plus grid shape.
+// One prepared launch: parameters plus grid shape (one of the two kinds).
 struct Prepared {
     Params p;
     Launch l;
     int B;
+    bool sk = false;
+    gemv::SkParams skp;
+    gemv::SkLaunch skl;
 };
+
+void ws_free(Workspace& ws) {
+    if (ws.part) cudaFree(ws.part);
+    if (ws.ticket) cudaFree(ws.ticket);
+    ws = Workspace{};
+}
+
+// Make ws hold at least part_floats partial sums and `tickets` zeroed counters.
+// Growing waits for the device (the old buffers may still be in use) and is
+// refused while `s` is capturing.
+int ws_reserve(Workspace& ws, int64_t part_floats, int64_t tickets, cudaStream_t s) {
+    if (ws.part_cap >= part_floats && ws.ticket_cap >= tickets) return GEMV_OK;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (cs != cudaStreamCaptureStatusNone) return GEMV_ERR_CAPTURE;
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e);
+    const int64_t np = part_floats > ws.part_cap ? part_floats : ws.part_cap;
+    const int64_t nt = tickets > ws.ticket_cap ? tickets : ws.ticket_cap;
+    ws_free(ws);
+    if (cudaMalloc(&ws.part, static_cast<size_t>(np) * sizeof(float)) != cudaSuccess ||
+        cudaMalloc(&ws.ticket, static_cast<size_t>(nt) * sizeof(int32_t)) != cudaSuccess) {
+        cudaGetLastError();
+        ws_free(ws);
+        return GEMV_ERR_NOMEM;
+    }
+    if ((e = cudaMemset(ws.ticket, 0, static_cast<size_t>(nt) * sizeof(int32_t))) != cudaSuccess ||
+        (e = cudaDeviceSynchronize()) != cudaSuccess) {
+        ws_free(ws);
+        return cuda_fail(e);
+    }
+    ws.part_cap = np;
+    ws.ticket_cap = nt;
+    return GEMV_OK;
+}
+
+// Stream-K launch over the segments (batch 1; see gemv_streamk_kernel.cuh).
+int prepare_streamk(const gemv_segment* segs, int nsegs, int64_t total, const void* x, int64_t K, int flags,
+                    float eps, int sm_count, Prepared* out) {
+    gemv::SkLaunch l;
+    int rc = gemv::plan_streamk(total, K, 1, sm_count, &l);
+    if (rc != GEMV_OK) return rc;
+    gemv::SkParams p;
+    std::memset(&p, 0, sizeof p);
+    int64_t row = 0;
+    for (int i = 0; i < nsegs; ++i) {
+        p.seg[i].W = static_cast<const uint16_t*>(segs[i].W);
+        p.seg[i].y = segs[i].y;
+        p.seg[i].N = segs[i].N;
+        p.seg[i].ldw = segs[i].ldw;
+        p.seg[i].tile_begin = row;
+        row += segs[i].N;
+    }
+    p.x = static_cast<const uint16_t*>(x);
+    p.K = K;
+    p.units = l.units;
+    p.warps = l.warps;
+    p.chunks = l.chunks;
+    p.dp_rounds = l.dp_rounds;
+    p.nseg = nsegs;
+    p.xstride = l.xstride;
+    p.flags = (flags & GEMV_FLAG_RMSNORM) ? gemv::kFlagRmsNorm : 0;
+    p.rms_eps = eps;
+    out->sk = true;
+    out->skp = p;
+    out->skl = l;
+    out->B = 1;
+    return GEMV_OK;
+}
 
 // Validate a group of segments sharing x, K, B and plan one launch over them.
 int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B, int flags, float eps,
@@ -122,6 +204,13 @@ int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B
         total += segs[i].N;
         if (total > 0x7fffffffLL) return GEMV_ERR_INVALID;
     }
+    if (flags & GEMV_FLAG_STREAMK) {
+        if (B != 1) return GEMV_ERR_UNSUPPORTED;
+        return prepare_streamk(segs, nsegs, total, x, K, flags, eps, sm_count, out);
+    }
+    if (B == 1 && gemv::prefer_streamk(total, K, B, sm_count) &&
+        prepare_streamk(segs, nsegs, total, x, K, flags, eps, sm_count, out) == GEMV_OK)
+        return GEMV_OK;
     Launch l;
     if ((rc = gemv::plan_launch(total, K, B, sm_count, &l)) != GEMV_OK) return rc;
 
@@ -202,8 +291,30 @@ int check_w4(const void* Wq, const void* S, const void* x, const float* y, int64
     return GEMV_OK;
 }
 
-int run(const Prepared& pr, cudaStream_t s) {
-    cudaError_t e = gemv::launch_gemv(pr.B, pr.p, pr.l, s, pdl_enabled());
+// Launch a prepared GEMV; a stream-K launch takes its workspace from `ws`
+// (the plan's), or from the device's when ws is null.
+int run(const Prepared& pr, cudaStream_t s, Workspace* ws = nullptr) {
+    cudaError_t e;
+    if (pr.sk) {
+        gemv::SkParams p = pr.skp;
+        if (ws) {
+            if (ws->part_cap < pr.skl.part_floats || ws->ticket_cap < pr.skl.tickets) return GEMV_ERR_INVALID;
+            p.part = ws->part;
+            p.ticket = ws->ticket;
+        } else {
+            int dev = 0;
+            if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
+            std::lock_guard<std::mutex> lock(g_dev_mutex);
+            Workspace& dws = g_dev[dev].ws;
+            int rc = ws_reserve(dws, pr.skl.part_floats, pr.skl.tickets, s);
+            if (rc != GEMV_OK) return rc;
+            p.part = dws.part;
+            p.ticket = dws.ticket;
+        }
+        e = gemv::launch_streamk(p, pr.skl, s, pdl_enabled());
+    } else {
+        e = gemv::launch_gemv(pr.B, pr.p, pr.l, s, pdl_enabled());
+    }
     if (e != cudaSuccess) return cuda_fail(e);
     return GEMV_OK;
 }
@@ -214,6 +325,7 @@ struct gemv_plan {
     std::vector<Prepared> launches;
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
+    Workspace ws;   // stream-K launches of this plan (run one after another)
 };
 
 extern "C" {
@@ -329,6 +441,16 @@ int gemv_plan_create(const gemv_proj* projs, int nproj, gemv_plan** out) {
         delete plan;
         return GEMV_ERR_NOMEM;
     }
+    int64_t need_part = 0, need_tickets = 0;
+    for (const Prepared& pr : plan->launches) {
+        if (!pr.sk) continue;
+        if (pr.skl.part_floats > need_part) need_part = pr.skl.part_floats;
+        if (pr.skl.tickets > need_tickets) need_tickets = pr.skl.tickets;
+    }
+    if (need_part > 0 && (rc = ws_reserve(plan->ws, need_part, need_tickets, nullptr)) != GEMV_OK) {
+        delete plan;
+        return rc;
+    }
     *out = plan;
     return GEMV_OK;
 }
@@ -344,7 +466,7 @@ int gemv_plan_capture(gemv_plan* plan, void* stream) {
     if ((e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal)) != cudaSuccess) return cuda_fail(e);
     int rc = GEMV_OK;
     for (const Prepared& pr : plan->launches) {
-        if ((rc = run(pr, s)) != GEMV_OK) break;
+        if ((rc = run(pr, s, &plan->ws)) != GEMV_OK) break;
     }
     cudaGraph_t g = nullptr;
     e = cudaStreamEndCapture(s, &g);
@@ -386,11 +508,56 @@ void gemv_plan_destroy(gemv_plan* plan) {
     if (!plan) return;
     if (plan->exec) cudaGraphExecDestroy(plan->exec);
     if (plan->graph) cudaGraphDestroy(plan->graph);
+    ws_free(plan->ws);
     delete plan;
+}
+
+int gemv_workspace_release(void) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return GEMV_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    ws_free(g_dev[dev].ws);
+    return GEMV_OK;
+}
+
+int gemv_query_launch_ex(int64_t N, int64_t K, int B, int sm_count, int flags, gemv_launch_info* out) {
+    if (!out) return GEMV_ERR_INVALID;
+    if (flags & ~(GEMV_FLAG_RMSNORM | GEMV_FLAG_STREAMK)) return GEMV_ERR_INVALID;
+    const bool sk = (flags & GEMV_FLAG_STREAMK) ||
+                    (B == 1 && gemv::prefer_streamk(N, K, B, sm_count));
+    if (!sk) return gemv_query_launch(N, K, B, sm_count, out);
+    gemv::SkLaunch l;
+    int rc = gemv::plan_streamk(N, K, B, sm_count, &l);
+    if (rc != GEMV_OK) {
+        if (flags & GEMV_FLAG_STREAMK) return rc;
+        return gemv_query_launch(N, K, B, sm_count, out);
+    }
+    std::memset(out, 0, sizeof *out);
+    out->grid = l.grid;
+    out->kslice = gemv::kSkUnitCols;
+    out->kchunk = K;
+    out->warps_per_cta = gemv::kWarps;
+    out->warps_per_row = 1;
+    out->splits = 1;
+    out->rows_per_warp = 1;
+    out->unroll = gemv::kSkUnroll;
+    out->smem_bytes = l.smem_bytes;
+    out->path = gemv::kPathStreamK;
+    out->xstride = l.xstride;
+    out->nbuf = 1;
+    out->units = l.units;
+    out->warps = l.warps;
+    out->chunks = l.chunks;
+    out->ctas_per_sm = l.ctas_per_sm;
+    out->dp_rounds = l.dp_rounds;
+    return GEMV_OK;
 }
 
 int gemv_query_launch(int64_t N, int64_t K, int B, int sm_count, gemv_launch_info* out) {
     if (!out) return GEMV_ERR_INVALID;
+    std::memset(out, 0, sizeof *out);
     Launch l;
     int rc = gemv::plan_launch(N, K, B, sm_count, &l);
     if (rc != GEMV_OK) return rc;
@@ -418,6 +585,7 @@ int gemv_w4_bf16(const void* Wq, const void* S, const void* x, float* y, int64_t
     int flags = 0;
     float eps = 0.f;
     if ((rc = check_options(opt, &flags, &eps)) != GEMV_OK) return rc;
+    if (flags & GEMV_FLAG_STREAMK) return GEMV_ERR_UNSUPPORTED;
     int sm_count = 0;
     if ((rc = device_state(&sm_count)) != GEMV_OK) return rc;
     Prepared pr;

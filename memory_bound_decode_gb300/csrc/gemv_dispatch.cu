@@ -27,6 +27,7 @@ cudaError_t prepare_kernels(int /*device: attributes apply to the current device
     if ((e = prepare_fma_all()) != cudaSuccess) return e;
     if ((e = prepare_mma_nb1()) != cudaSuccess) return e;
     if ((e = prepare_w4_all()) != cudaSuccess) return e;
+    if ((e = prepare_streamk()) != cudaSuccess) return e;
     return prepare_mma_nb2();
 }
 

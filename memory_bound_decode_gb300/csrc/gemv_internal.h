@@ -52,9 +52,10 @@ constexpr int kMiscFloats = kWarps * kMaxBatch + 2 * kMaxBatch;
 
 // Kernel families.
 enum Path : int32_t {
-    kPathFma = 0,   // CUDA-core FP32 multiply-adds, one warp streams RPW whole rows
-    kPathMma = 1,   // BF16 tensor-core mma.sync, one warp streams a 16-row tile
-    kPathW4 = 2,    // INT4 weights dequantised to BF16 in registers, tensor-core mma.sync
+    kPathFma = 0,       // CUDA-core FP32 multiply-adds, one warp streams RPW whole rows
+    kPathMma = 1,       // BF16 tensor-core mma.sync, one warp streams a 16-row tile
+    kPathW4 = 2,        // INT4 weights dequantised to BF16 in registers, tensor-core mma.sync
+    kPathStreamK = 3,   // batch 1, one wave of CTAs, warps take balanced ranges of (row, K-unit)
 };
 
 // Weight formats the planner knows.
@@ -102,11 +103,60 @@ struct Launch {
 // Returns 0 and fills `out`, or a negative GEMV_ERR_* code.
 int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind = kWeightBf16);
 
+// Stream-K launch (batch 1): the grid is one wave of GW warps. Rows (of all
+// segments, numbered consecutively) that fill whole rounds of GW are taken
+// one per warp: row r * GW + w in round r < dp_rounds. The rest, cut into
+// units of kSkUnitCols columns and numbered row-major, are split evenly: warp
+// w takes units [w * units / warps, (w + 1) * units / warps). A row whose units
+// belong to more than one warp is finished by the last of them to arrive
+// (per-row counter), which adds the warps' partial sums in warp order.
+constexpr int kSkUnroll = 8;                          // 16-byte loads per lane per unit
+constexpr int kSkUnitCols = 32 * 8 * kSkUnroll;       // 2,048 columns per unit
+constexpr int kSkMaxCtasPerSm = 4;
+constexpr int64_t kSkMaxXBytes = 48 * 1024;           // whole x row staged per CTA
+
+struct SkParams {
+    Seg seg[kMaxSegs];    // tile_begin holds the segment's first global row
+    const uint16_t* x;
+    int64_t K;
+    int64_t units;        // units of the split part: (rows - dp_rounds * grid warps) * chunks
+    int64_t warps;        // warps that take split-part units (<= units, <= grid * kWarps)
+    float* part;          // [warps][2] partial sums (a warp's first and last split row)
+    int32_t* ticket;      // [split-part rows] arrival counters, zero between launches
+    int32_t chunks;       // units per row
+    int32_t dp_rounds;    // rounds of whole rows, one per warp of the grid
+    int32_t nseg;
+    int32_t xstride;      // staged x elements (whole vectors up to K)
+    int32_t flags;        // kFlagRmsNorm
+    float rms_eps;
+};
+
+struct SkLaunch {
+    int64_t grid;         // CTAs (one wave)
+    int64_t warps;        // split-part warps
+    int64_t units;        // split-part units
+    int32_t dp_rounds;
+    int32_t chunks;
+    int32_t smem_bytes;
+    int32_t ctas_per_sm;
+    int32_t xstride;
+    int64_t part_floats;  // workspace the launch needs
+    int64_t tickets;
+};
+
+// Returns 0 and fills `out`, or a negative GEMV_ERR_* code (GEMV_ERR_UNSUPPORTED
+// when the shape does not fit the stream-K kernel: B > 1 or x too large).
+int plan_streamk(int64_t rows, int64_t K, int B, int sm_count, SkLaunch* out);
+// Whether the planner prefers the stream-K kernel for this batch-1 shape.
+bool prefer_streamk(int64_t rows, int64_t K, int B, int sm_count);
+
 // Largest dynamic shared memory any plan requests (set as the kernel attribute).
 constexpr int32_t kMaxDynSmem = 112 * 1024;
 
 // Kernel launchers, defined in the kernel translation units.
 cudaError_t launch_gemv(int B, const Params& p, const Launch& l, cudaStream_t s, bool pdl);
+cudaError_t launch_streamk(const SkParams& p, const SkLaunch& l, cudaStream_t s, bool pdl);
+cudaError_t prepare_streamk();
 cudaError_t prepare_kernels(int device);   // per-device function attributes
 cudaError_t launch_probe_read(const void* src, int64_t bytes, float* sink, int grid,
                               cudaStream_t s);

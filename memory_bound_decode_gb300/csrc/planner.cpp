@@ -148,4 +148,51 @@ int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weig
     return GEMV_OK;
 }
 
+// Stream-K (batch 1): one wave of CTAs, as many as fit on an SM by shared
+// memory (the whole x row) and registers (kSkMaxCtasPerSm for whole units,
+// one fewer for ragged K), and never more warps than units, so that every warp
+// takes at least one unit.
+int plan_streamk(int64_t rows, int64_t K, int B, int sm_count, SkLaunch* out) {
+    if (!out || rows < 1 || K < 1 || B < 1 || B > kMaxBatch || sm_count < 1) return GEMV_ERR_INVALID;
+    if (B != 1) return GEMV_ERR_UNSUPPORTED;
+    const int64_t nv = cdiv(K, 8);
+    const int64_t xbytes = 16 * nv;
+    if (xbytes > kSkMaxXBytes) return GEMV_ERR_UNSUPPORTED;
+    const int64_t chunks = cdiv(K, kSkUnitCols);
+    if (rows > 0x7fffffffLL) return GEMV_ERR_UNSUPPORTED;
+    const int64_t units = rows * chunks;
+    if (units > 0x7fffffffLL) return GEMV_ERR_UNSUPPORTED;   // 32-bit unit numbers in the kernel
+    const int64_t smem = xbytes + kMiscFloats * 4;
+    constexpr int64_t kSmemPerSm = 228 * 1024, kSmemReservedPerCta = 1024;
+    int64_t per_sm = kSmemPerSm / (smem + kSmemReservedPerCta);
+    // The ragged-K instance (predicated last unit) holds one CTA fewer by registers.
+    const int64_t reg_cap = (K % kSkUnitCols == 0) ? kSkMaxCtasPerSm : kSkMaxCtasPerSm - 1;
+    if (per_sm > reg_cap) per_sm = reg_cap;
+    const int64_t grid_warps = static_cast<int64_t>(sm_count) * per_sm * kWarps;
+    // Whole rounds of rows one per warp; the rest split evenly. With fewer rows
+    // than warps, every row is split; a grid with more warps than units is cut
+    // to the units (every warp takes at least one).
+    const int64_t rounds = rows / grid_warps;
+    const int64_t rest_units = (rows - rounds * grid_warps) * chunks;
+    int64_t grid = cdiv(grid_warps, kWarps);
+    int64_t warps = grid_warps < rest_units ? grid_warps : rest_units;
+    if (rounds == 0) grid = cdiv(warps, kWarps);
+    out->grid = grid;
+    out->warps = warps;
+    out->units = rest_units;
+    out->dp_rounds = static_cast<int32_t>(rounds);
+    out->chunks = static_cast<int32_t>(chunks);
+    out->smem_bytes = static_cast<int32_t>(smem);
+    out->ctas_per_sm = static_cast<int32_t>(per_sm);
+    out->xstride = static_cast<int32_t>(8 * nv);
+    out->part_floats = 2 * (warps > 0 ? warps : 1);
+    out->tickets = rows - rounds * grid_warps > 0 ? rows - rounds * grid_warps : 1;
+    return GEMV_OK;
+}
+
+bool prefer_streamk(int64_t rows, int64_t K, int B, int sm_count) {
+    (void)rows; (void)K; (void)B; (void)sm_count;
+    return false;
+}
+
 }  // namespace gemv

@@ -89,17 +89,18 @@ class DecodeStep:
         y = torch.empty((1, N), dtype=torch.float32, device=self.device)
         self.projs.append(Proj(name, W, x, y, N, K, ldw, group))
 
-    def plan(self, rms_eps: float | None = None) -> binding.Plan:
+    def plan(self, rms_eps: float | None = None, streamk: bool = False) -> binding.Plan:
         """The step as one plan. With rms_eps, the projections that read a
         normalised activation in the model (QKV, gate/up and the LM head) take
-        the RMSNorm prologue; o_proj and down read the raw one."""
+        the RMSNorm prologue; o_proj and down read the raw one. With streamk,
+        every launch runs the stream-K kernel."""
         def eps_of(p):
             if rms_eps is None:
                 return None
             return rms_eps if (p.name.endswith(("q_proj", "k_proj", "v_proj", "gate_proj", "up_proj"))
                                or p.name == "lm_head") else None
-        return binding.Plan([(p.W, p.x, p.y, p.N, p.K, p.ldw, 1, p.group, eps_of(p)) for p in self.projs],
-                            keepalive=self)
+        return binding.Plan([(p.W, p.x, p.y, p.N, p.K, p.ldw, 1, p.group, eps_of(p), streamk)
+                             for p in self.projs], keepalive=self)
 
     def outputs(self):
         return [p.y for p in self.projs]

@@ -45,9 +45,21 @@ def test_decode_step_bytes():
 def test_peaks_and_traffic_lookup(tmp_path, monkeypatch):
     peak, kind = bench.load_peaks()
     assert peak > 1000 and kind in ("measured", "fallback")
-    h = bench.kernel_source_hash()
+    from memory_bound_decode_gb300 import binding
+    launch = binding.gemv_query_launch(4096, 14336, 1, 152)
+    h = bench.kernel_source_hash("fma", launch)
     assert len(h) == 16
+    # the launch configuration and the kernel family are part of the hash
+    assert h != bench.kernel_source_hash("fma", binding.gemv_query_launch(1024, 4096, 1, 152))
+    assert h != bench.kernel_source_hash("mma", launch)
+    assert bench.kernel_source_hash("sk", None) != bench.kernel_source_hash("fma", None)
     assert bench.profiled_traffic("no_such_workload", h) is None
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "gemv_x_y.md").write_text(f"kernel_source_hash: {h}\ndram_bytes_per_launch: 1,234\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic("x:y", h) == 1234
+    assert bench.profiled_traffic("x:y", "0" * 16) is None
 
 
 def test_reference_arm_json_line():
