@@ -264,6 +264,39 @@ int gemv_query_launch_ex(int64_t N, int64_t K, int B, int sm_count, int flags,
 int gemv_workspace_release(void);
 
 /*
+ * gemv_bf16_ex with GEMV_FLAG_STREAMK for callers that must not allocate
+ * device memory: the same stream-K kernel (batch 1, same results bit for bit),
+ * with its partial sums and per-row counters in a fixed scratch area compiled
+ * into the library (80 KB of device memory per device, zero when the library
+ * is loaded, left at zero by every launch) instead of the workspace the
+ * library would allocate. The pages have no counterpart to this call; it
+ * exists for callers in which a cudaMalloc is not allowed or not wanted: a
+ * serving loop that has fixed its memory footprint at start-up, code that runs
+ * under another allocator's control (an out-of-memory handler, a caching
+ * allocator's own callbacks), or work that must not wait for the device
+ * synchronization an allocation implies.
+ *   - Same arguments as gemv_bf16_ex with B = 1 (opt may set
+ *     GEMV_FLAG_RMSNORM; GEMV_FLAG_STREAMK is implied). y[n] for n < N.
+ *   - Capacity: the split part of the launch (the rows left over after whole
+ *     rounds of one row per warp; on a 152-SM GB300 N mod 4,864 when K is a
+ *     multiple of 2,048, else N mod 3,648, and N itself when N is smaller)
+ *     must need at most 4,096 row counters, and the grid at most 8,192 warps.
+ *     A larger shape returns GEMV_ERR_UNSUPPORTED before any launch, as do a
+ *     batch above 1 and an x row longer than 24,576 columns.
+ *   - The first call on a device looks up the scratch's device address (with
+ *     that device current) and sets the library's kernels up on the device;
+ *     make that first call before any stream capture.
+ *   - All calls on one device share the one scratch area: calls whose
+ *     launches overlap (on different streams, or from several threads without
+ *     ordering) race on it and give undefined results. Issue them on one
+ *     stream, or order them. Its scratch is separate from the workspace of
+ *     GEMV_FLAG_STREAMK calls and of plans, so those may overlap with it.
+ */
+int gemv_bf16_streamk_noalloc(const void *W, const void *x, float *y,
+                              int64_t N, int64_t K, int64_t ldw,
+                              const gemv_options *opt, void *stream);
+
+/*
  * y = W·x with group-quantised INT4 weights ("Decode GEMV at half of HBM
  * bandwidth", "What interviewers probe next": with INT4 weights the bytes fall
  * four times; the codes are unpacked in registers while the next loads are in

@@ -34,7 +34,7 @@ EXPORTED = [
     "gemv_bf16", "gemv_bf16_ex", "gemv_bf16_host_io", "gemv_bf16_multi", "gemv_bf16_multi_ex",
     "gemv_plan_create", "gemv_plan_capture",
     "gemv_plan_launch", "gemv_plan_num_launches", "gemv_plan_destroy",
-    "gemv_query_launch", "gemv_query_launch_ex", "gemv_workspace_release",
+    "gemv_query_launch", "gemv_query_launch_ex", "gemv_workspace_release", "gemv_bf16_streamk_noalloc",
     "gemv_w4_bf16", "gemv_w4_query_launch",
     "gemv_probe_stream_read", "gemv_probe_sink_words",
     "gemv_status_string", "gemv_last_cuda_error",
@@ -114,6 +114,7 @@ def lib() -> ctypes.CDLL:
             L.gemv_query_launch_ex.argtypes = [i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                ctypes.POINTER(gemv_launch_info)]
             L.gemv_workspace_release.argtypes = []
+            L.gemv_bf16_streamk_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.POINTER(gemv_options), vp]
             L.gemv_w4_bf16.argtypes = [vp, vp, vp, vp, i64, i64, ctypes.c_int, i64, i64,
                                        ctypes.POINTER(gemv_options), vp]
             L.gemv_w4_query_launch.argtypes = [i64, i64, ctypes.c_int, ctypes.c_int,
@@ -220,6 +221,14 @@ def gemv_query_launch_ex(N: int, K: int, B: int, sm_count: int, flags: int) -> d
     info = gemv_launch_info()
     _check(lib().gemv_query_launch_ex(N, K, B, sm_count, flags, ctypes.byref(info)), "gemv_query_launch_ex")
     return info.as_dict()
+
+
+def gemv_bf16_streamk_noalloc(W, x, y, N: int, K: int, ldw: int, rms_eps=None, stream=None,
+                              check: bool = True) -> int:
+    """The stream-K GEMV (batch 1) with the library's fixed scratch: no allocation (see gemv.h)."""
+    rc = lib().gemv_bf16_streamk_noalloc(_ptr(W), _ptr(x), _ptr(y), N, K, ldw, _options(rms_eps),
+                                         _stream(stream))
+    return _check(rc, "gemv_bf16_streamk_noalloc") if check else rc
 
 
 def gemv_workspace_release() -> int:

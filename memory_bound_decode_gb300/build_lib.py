@@ -27,6 +27,7 @@ SOURCES = [
     "gemv_mma_instances_nb2.cu",
     "gemv_w4_instances.cu",
     "gemv_streamk_instances.cu",
+    "gemv_noalloc.cu",
     "gemv_dispatch.cu",
     "planner.cpp",
     "gemv_api.cpp",

@@ -522,6 +522,53 @@ int gemv_workspace_release(void) {
     return GEMV_OK;
 }
 
+int gemv_bf16_streamk_noalloc(const void* W, const void* x, float* y, int64_t N, int64_t K, int64_t ldw,
+                              const gemv_options* opt, void* stream) {
+    // Per-device addresses of the fixed scratch, looked up once per device
+    // with that device current.
+    static std::mutex scratch_mutex;
+    static float* scratch_part[kMaxDevices] = {};
+    static int32_t* scratch_ticket[kMaxDevices] = {};
+
+    int rc = check_common(x, K, 1);
+    if (rc != GEMV_OK) return rc;
+    if ((rc = check_matrix(W, y, N, K, ldw)) != GEMV_OK) return rc;
+    int flags = 0;
+    float eps = 0.f;
+    if ((rc = check_options(opt, &flags, &eps)) != GEMV_OK) return rc;
+    int sm_count = 0;
+    if ((rc = device_state(&sm_count)) != GEMV_OK) return rc;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    float* part = nullptr;
+    int32_t* ticket = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(scratch_mutex);
+        if (!scratch_part[dev]) {
+            if ((e = gemv::noalloc_scratch(&scratch_part[dev], &scratch_ticket[dev])) != cudaSuccess) {
+                scratch_part[dev] = nullptr;
+                scratch_ticket[dev] = nullptr;
+                return cuda_fail(e);
+            }
+        }
+        part = scratch_part[dev];
+        ticket = scratch_ticket[dev];
+    }
+    gemv_segment seg{W, y, N, ldw};
+    Prepared pr;
+    if ((rc = prepare_streamk(&seg, 1, N, x, K, flags | GEMV_FLAG_STREAMK, eps, sm_count, &pr)) != GEMV_OK)
+        return rc;
+    if (pr.skl.part_floats > gemv::kNoallocPartFloats || pr.skl.tickets > gemv::kNoallocTickets)
+        return GEMV_ERR_UNSUPPORTED;
+    gemv::SkParams p = pr.skp;
+    p.part = part;
+    p.ticket = ticket;
+    if ((e = gemv::launch_streamk(p, pr.skl, static_cast<cudaStream_t>(stream), pdl_enabled())) != cudaSuccess)
+        return cuda_fail(e);
+    return GEMV_OK;
+}
+
 int gemv_query_launch_ex(int64_t N, int64_t K, int B, int sm_count, int flags, gemv_launch_info* out) {
     if (!out) return GEMV_ERR_INVALID;
     if (flags & ~(GEMV_FLAG_RMSNORM | GEMV_FLAG_STREAMK)) return GEMV_ERR_INVALID;

@@ -144,6 +144,14 @@ struct SkLaunch {
     int64_t tickets;
 };
 
+// Capacity of the fixed scratch of gemv_bf16_streamk_noalloc (gemv_noalloc.cu):
+// partial sums for 8,192 warps (a one-wave grid of up to 256 SMs x 4 CTAs x 8
+// warps) and counters for 4,096 split-part rows. 80 KB of device memory.
+constexpr int64_t kNoallocPartFloats = 2 * 8192;
+constexpr int64_t kNoallocTickets = 4096;
+// Device addresses of that scratch for the current device.
+cudaError_t noalloc_scratch(float** part, int32_t** ticket);
+
 // Returns 0 and fills `out`, or a negative GEMV_ERR_* code (GEMV_ERR_UNSUPPORTED
 // when the shape does not fit the stream-K kernel: B > 1 or x too large).
 int plan_streamk(int64_t rows, int64_t K, int B, int sm_count, SkLaunch* out);

@@ -207,3 +207,12 @@ def test_host_io_rejects(L):
     assert f(A16, A16, 0, A16, A16, 8, 8, 1, 8, **ok) == binding.GEMV_ERR_INVALID        # y_host NULL
     assert f(A16, A16, A16, 0, A16, 8, 8, 1, 8, **ok) == binding.GEMV_ERR_INVALID        # x_dev NULL
     assert f(A16, A16, A16, A16, A16 + 2, 8, 8, 1, 8, **ok) == binding.GEMV_ERR_ALIGN    # y_dev
+
+
+def test_streamk_noalloc_rejects(L):
+    f = lambda *a: binding.gemv_bf16_streamk_noalloc(*a, stream=0, check=False)
+    assert f(0, A16, A16, 8, 8, 8) == binding.GEMV_ERR_INVALID            # W NULL
+    assert f(A16, A16, A16, 0, 8, 8) == binding.GEMV_ERR_INVALID          # N = 0
+    assert f(A16, A16, A16, 8, 8, 4) == binding.GEMV_ERR_INVALID          # ldw < K
+    assert f(A16, A16, A16 + 2, 8, 8, 8) == binding.GEMV_ERR_ALIGN        # y misaligned
+    assert f(A16 + 8, A16, A16, 8, 8, 8) == binding.GEMV_ERR_ALIGN        # W not 16-byte aligned
