@@ -162,3 +162,48 @@ def w4_weight_device(N: int, K: int, ldq: int | None = None, lds: int | None = N
     sc = torch.rand((N, G), generator=g, device=device, dtype=torch.float32) * (scale_hi - scale_lo) + scale_lo
     S[:, :G] = sc.to(torch.bfloat16)
     return Wq, S
+
+
+# ----------------------------------------------------------------------------- FP8 weights
+#
+# Layout of an FP8 weight: Wq uint8 [N, ldq], ldq >= K, ldq % 16 == 0, holding
+# E4M3 codes (sign, 4 exponent bits with bias 7, 3 mantissa bits; no infinities,
+# S.1111.111 is NaN), and S float32 [N], one scale per output row: element
+# (n, k) is e4m3(Wq[n][k]) * S[n]. Columns k in [K, ldq) are padding.
+FP8_PAD = 0x7F   # an E4M3 NaN: any use of padding shows up
+
+
+def fp8_quantize(Wf: torch.Tensor):
+    """Row-scaled E4M3 codes of a float weight: S[n] = max_k |W[n][k]| / 448 (1
+    for an all-zero row), codes = W / S rounded to E4M3 (round to nearest even,
+    by torch's conversion). Returns (codes uint8 [N, K], S float32 [N])."""
+    amax = Wf.abs().amax(dim=1)
+    S = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)).to(torch.float32)
+    codes = (Wf / S[:, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, S
+
+
+def fp8_weight(N: int, K: int, ldq: int | None = None, *, seed: int = 0, index: int = 0,
+               std: float = 0.02, device="cpu", pad: int | None = FP8_PAD):
+    """(Wq uint8 [N, ldq], S float32 [N]): W ~ N(0, std^2) drawn in FP32, then
+    quantised per row with fp8_quantize; padding columns hold an E4M3 NaN."""
+    ldq = (int(K) + 15) // 16 * 16 if ldq is None else int(ldq)
+    g = generator(seed, index, device)
+    Wq = torch.empty((N, ldq), dtype=torch.uint8, device=device)
+    S = torch.empty((N,), dtype=torch.float32, device=device)
+    rows = max(1, (1 << 26) // max(K, 1))
+    for r0 in range(0, N, rows):
+        r1 = min(N, r0 + rows)
+        part = torch.randn((r1 - r0, K), generator=g, dtype=torch.float32, device=device).mul_(std)
+        codes, sc = fp8_quantize(part)
+        Wq[r0:r1, :K] = codes
+        S[r0:r1] = sc
+    if pad is not None and ldq > K:
+        Wq[:, K:] = pad
+    return Wq, S
+
+
+def fp8_decode(codes) -> np.ndarray:
+    """E4M3 codes (uint8 array or tensor) to float64 by torch's float8_e4m3fn type."""
+    t = torch.as_tensor(np.ascontiguousarray(codes) if isinstance(codes, np.ndarray) else codes)
+    return t.cpu().view(torch.float8_e4m3fn).to(torch.float64).numpy()

@@ -181,3 +181,52 @@ int oracle_gemv_w4_f64(const uint8_t *Wq, const uint16_t *S, const uint16_t *x,
     }
     return 0;
 }
+
+/*
+ * The GEMV with FP8 weights ("Decode GEMV at half of HBM bandwidth", "What
+ * interviewers probe next": INT4, then FP8 weights, with the unpacking done in
+ * registers). Each weight is an 8-bit E4M3 code c: sign in bit 7, exponent
+ * field e in bits 3..6 with bias 7, mantissa m in bits 0..2. e = 0 encodes the
+ * subnormals (m / 8) * 2^-6; e = 15 with m = 7 is NaN; the format has no
+ * infinities, so e = 15 with m < 7 are finite (the largest is 448). Element
+ * (n, k) of W is e4m3(Wq[n * ldq + k]) * S[n], with S one FP32 scale per output
+ * row. Every product w * S * x is exact in FP64 (4 + 24 + 8 significant bits).
+ * Rows [n0, n1); FP64; the same y and tolerance scale s as oracle_gemv_f64.
+ * Returns 0, or -1 on a bad argument.
+ */
+static double e4m3_to_double(uint8_t c)
+{
+    int e8 = (c >> 3) & 0xF;
+    int m8 = c & 0x7;
+    double mag8;
+    if (e8 == 0xF && m8 == 0x7) return NAN;
+    if (e8 == 0) mag8 = ldexp((double)m8 / 8.0, -6);
+    else mag8 = ldexp(1.0 + (double)m8 / 8.0, e8 - 7);
+    return (c & 0x80) ? -mag8 : mag8;
+}
+
+int oracle_gemv_fp8_f64(const uint8_t *Wq, const float *S, const uint16_t *x,
+                        int64_t N, int64_t K, int64_t B, int64_t ldq,
+                        int64_t n0, int64_t n1, double *y, double *s)
+{
+    if (!Wq || !S || !x || !y || !s) return -1;
+    if (N < 1 || K < 1 || B < 1 || ldq < K) return -1;
+    if (n0 < 0 || n1 > N || n0 > n1) return -1;
+
+    for (int64_t b = 0; b < B; ++b) {
+        const uint16_t *xr8 = x + b * K;
+        for (int64_t n = n0; n < n1; ++n) {
+            const uint8_t *row8 = Wq + n * ldq;
+            double sum8 = 0.0;
+            double abs8 = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double t8 = e4m3_to_double(row8[k]) * (double)S[n] * bf16_to_double(xr8[k]);
+                sum8 += t8;
+                abs8 += fabs(t8);
+            }
+            y[b * N + n] = sum8;
+            s[b * N + n] = abs8;
+        }
+    }
+    return 0;
+}

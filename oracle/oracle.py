@@ -82,6 +82,9 @@ class OracleLib:
         q = self._lib.oracle_gemv_w4_f64
         q.restype = ctypes.c_int
         q.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64, vp, vp]
+        f8 = self._lib.oracle_gemv_fp8_f64
+        f8.restype = ctypes.c_int
+        f8.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp, vp]
 
     def gemv(self, W: np.ndarray, x: np.ndarray, K: int | None = None,
              threads: int | None = None) -> tuple[np.ndarray, np.ndarray]:
@@ -173,6 +176,40 @@ class OracleLib:
             raise ValueError("oracle rejected its arguments")
         return y, s
 
+    def gemv_fp8(self, Wq: np.ndarray, S: np.ndarray, x: np.ndarray, K: int,
+                 threads: int | None = None) -> tuple[np.ndarray, np.ndarray]:
+        """(y_ref, scale) of the FP8 (E4M3) GEMV. Wq uint8 [N, ldq] codes,
+        S float32 [N] row scales, x uint16 [B, K] (BF16 bits)."""
+        if Wq.dtype != np.uint8 or S.dtype != np.float32 or x.dtype != np.uint16:
+            raise TypeError("Wq uint8 codes, S float32, x BF16 bits as uint16")
+        if x.ndim == 1:
+            x = x[None, :]
+        Wq = np.ascontiguousarray(Wq)
+        S = np.ascontiguousarray(S.reshape(-1))
+        x = np.ascontiguousarray(x)
+        N, ldq = Wq.shape
+        B = x.shape[0]
+        if x.shape[1] != K or S.shape[0] != N:
+            raise ValueError("shapes disagree")
+        y = np.empty((B, N), dtype=np.float64)
+        s = np.empty((B, N), dtype=np.float64)
+        threads = max(1, min(threads or 1, N))
+        bounds = np.linspace(0, N, threads + 1).astype(np.int64)
+
+        def run(i: int) -> int:
+            return self._lib.oracle_gemv_fp8_f64(
+                Wq.ctypes.data, S.ctypes.data, x.ctypes.data, N, K, B, ldq,
+                int(bounds[i]), int(bounds[i + 1]), y.ctypes.data, s.ctypes.data)
+
+        if threads == 1:
+            rcs = [run(0)]
+        else:
+            with ThreadPoolExecutor(max_workers=threads) as ex:
+                rcs = list(ex.map(run, range(threads)))
+        if any(rc != 0 for rc in rcs):
+            raise ValueError("oracle rejected its arguments")
+        return y, s
+
     def gemv_one(self, W: np.ndarray, x: np.ndarray, b: int, n: int,
                  K: int | None = None) -> tuple[float, float]:
         """Return (y_ref[b, n], scale[b, n]) for a single output element."""
@@ -226,6 +263,10 @@ def gemv_rmsnorm(W: np.ndarray, x: np.ndarray, eps: float, K: int | None = None,
 def gemv_w4(Wq: np.ndarray, S: np.ndarray, x: np.ndarray, K: int, group: int = 128,
             threads: int | None = None):
     return load().gemv_w4(Wq, S, x, K, group, threads)
+
+
+def gemv_fp8(Wq: np.ndarray, S: np.ndarray, x: np.ndarray, K: int, threads: int | None = None):
+    return load().gemv_fp8(Wq, S, x, K, threads)
 
 
 def gemv_one(W: np.ndarray, x: np.ndarray, b: int, n: int, K: int | None = None):

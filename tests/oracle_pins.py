@@ -26,6 +26,12 @@ What pins what:
   w4_one_hot          INT4: one-hot x at every position of a word and across a group
                       boundary selects (u - 8) * scale
   w4_dense            INT4 against numpy float64 on weights dequantised from the codes
+  fp8_decode_table    FP8: every one of the 256 E4M3 codes against torch's float8_e4m3fn
+                      decode (NaN codes NaN) and closed forms (1, 448, 2^-6, 2^-9, -0)
+  fp8_integer_exact   FP8 codes of small integers, power-of-two row scales, integer x:
+                      y exact against numpy int64 arithmetic
+  fp8_dense           FP8 against numpy float64 on torch-decoded weights times row scales,
+                      with NaN codes in the ldq padding that must not reach y
 """
 from __future__ import annotations
 
@@ -280,11 +286,66 @@ def w4_dense(lib):
     assert np.array_equal(y0, np.zeros_like(y0)) and np.array_equal(s0, np.zeros_like(s0))
 
 
+def fp8_decode_table(lib):
+    N, K = 256, 1
+    Wq = np.arange(256, dtype=np.uint8).reshape(N, K)
+    S = np.ones(N, dtype=np.float32)
+    x = np.array([[0x3F80]], dtype=np.uint16)          # 1.0
+    y, sc = lib.gemv_fp8(Wq, S, x, K)
+    want = inputs.fp8_decode(Wq[:, 0])
+    nan = np.isnan(want)
+    assert set(np.flatnonzero(nan)) == {0x7F, 0xFF}
+    assert np.all(np.isnan(y[0, nan]))
+    assert np.array_equal(y[0, ~nan], want[~nan])
+    for code, value in ((0x38, 1.0), (0x7E, 448.0), (0x08, 2.0 ** -6), (0x01, 2.0 ** -9),
+                        (0x07, 7 * 2.0 ** -9), (0xB8, -1.0), (0x3C, 1.5), (0x00, 0.0)):
+        assert y[0, code] == value, hex(code)
+    assert y[0, 0x80] == 0.0 and sc[0, 0x80] == 0.0      # -0 (a sum from +0 loses its sign)
+
+
+def _fp8_codes_of(values: np.ndarray) -> np.ndarray:
+    return torch.as_tensor(values, dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def fp8_integer_exact(lib):
+    rng = np.random.default_rng(5)
+    for (N, K, B, ldq) in [(7, 64, 2, 64), (9, 300, 3, 304), (3, 17, 1, 32)]:
+        wi = rng.integers(-8, 9, size=(N, K))               # |w| <= 8: exact in E4M3
+        codes = np.zeros((N, ldq), dtype=np.uint8)
+        codes[:, :K] = _fp8_codes_of(wi.astype(np.float32))
+        shifts = (np.arange(N) % 4) - 1                       # row scales 2^-1 .. 2^2
+        S = (2.0 ** shifts).astype(np.float32)
+        x = inputs.bits(inputs.int_activations(B, K, lo=-3, hi=3, seed=N))
+        y, sc = lib.gemv_fp8(codes, S, x, K)
+        xi = _decode(x).astype(np.int64)
+        w2 = wi * (2 ** (shifts + 1))[:, None]                # 2 * w * S, an integer
+        assert np.array_equal(y * 2, (xi @ w2.T).astype(np.float64)), (N, K)
+        assert np.array_equal(sc * 2, (np.abs(xi) @ np.abs(w2).T).astype(np.float64))
+
+
+def fp8_dense(lib):
+    N, K, B, ldq = 33, 1000, 3, 1024
+    Wq, S = inputs.fp8_weight(N, K, ldq, seed=44)
+    Wq, S = Wq.numpy(), S.numpy()
+    assert np.all(Wq[:, K:] == inputs.FP8_PAD)
+    x = inputs.bits(inputs.activations(B, K, seed=45))
+    y, sc = lib.gemv_fp8(Wq, S, x, K)
+    Wd = inputs.fp8_decode(Wq[:, :K]) * S.astype(np.float64)[:, None]
+    xd = _decode(x)
+    assert np.all(np.isfinite(y))
+    assert np.all(np.abs(y - xd @ Wd.T) <= 4 * K * EPS64 * sc)
+    assert np.allclose(sc, np.abs(xd) @ np.abs(Wd).T, rtol=1e-12, atol=0)
+    # a sign flip of every code negates y
+    yn, _ = lib.gemv_fp8(Wq ^ np.uint8(0x80), S, x, K)
+    assert np.array_equal(yn, -y)
+
+
 ALL_PINS = [exact_rational, integer_matmul, ones_row_sums, one_hot_column,
             identity_padded, scaling_exact, linearity, row_permutation,
             batch_rows, padding_unread, float64_matmul, single_element,
             rms_constant_x, rms_scale_free, rms_independent,
-            w4_integer_exact, w4_one_hot, w4_dense]
+            w4_integer_exact, w4_one_hot, w4_dense,
+            fp8_decode_table, fp8_integer_exact, fp8_dense]
 
 
 def failures(lib) -> list[str]:

@@ -48,6 +48,21 @@ MUTATIONS = {
     "w4_scale_row_0": ("bf16_to_double(S[n * lds + k / group]);", "bf16_to_double(S[k / group]);"),
     "w4_big_endian": ("uint32_t word = (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);",
                       "uint32_t word = (uint32_t)p[3] | ((uint32_t)p[2] << 8) | ((uint32_t)p[1] << 16) | ((uint32_t)p[0] << 24);"),
+    "fp8_bias_8": ("else mag8 = ldexp(1.0 + (double)m8 / 8.0, e8 - 7);",
+                   "else mag8 = ldexp(1.0 + (double)m8 / 8.0, e8 - 8);"),
+    "fp8_subnormal_exponent": ("if (e8 == 0) mag8 = ldexp((double)m8 / 8.0, -6);",
+                               "if (e8 == 0) mag8 = ldexp((double)m8 / 8.0, -7);"),
+    "fp8_subnormal_implicit_one": ("if (e8 == 0) mag8 = ldexp((double)m8 / 8.0, -6);",
+                                   "if (e8 == 0) mag8 = ldexp(1.0 + (double)m8 / 8.0, -6);"),
+    "fp8_sign_dropped": ("return (c & 0x80) ? -mag8 : mag8;", "return mag8;"),
+    "fp8_mantissa_over_16": ("else mag8 = ldexp(1.0 + (double)m8 / 8.0, e8 - 7);",
+                             "else mag8 = ldexp(1.0 + (double)m8 / 16.0, e8 - 7);"),
+    "fp8_no_row_scale": ("e4m3_to_double(row8[k]) * (double)S[n] * bf16_to_double(xr8[k]);",
+                         "e4m3_to_double(row8[k]) * bf16_to_double(xr8[k]);"),
+    "fp8_scale_row_0": ("e4m3_to_double(row8[k]) * (double)S[n] * bf16_to_double(xr8[k]);",
+                        "e4m3_to_double(row8[k]) * (double)S[0] * bf16_to_double(xr8[k]);"),
+    "fp8_row_stride_K": ("const uint8_t *row8 = Wq + n * ldq;", "const uint8_t *row8 = Wq + n * K;"),
+    "fp8_nan_not_nan": ("if (e8 == 0xF && m8 == 0x7) return NAN;", "if (e8 == 0xF && m8 == 0x7) return 480.0;"),
 }
 
 
