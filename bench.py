@@ -75,6 +75,8 @@ KERNEL_FILES = {   # the sources that make up each kernel family's launches
             "gemv_mma_instances_nb2.cu", "gemv_dispatch.cu"),
     "w4": ("gemv_internal.h", "gemv_common.cuh", "gemv_mma_kernel.cuh", "gemv_w4_kernel.cuh",
            "gemv_w4_instances.cu", "gemv_dispatch.cu"),
+    "f8": ("gemv_internal.h", "gemv_common.cuh", "gemv_mma_kernel.cuh", "gemv_fp8_kernel.cuh",
+           "gemv_fp8_instances.cu", "gemv_dispatch.cu"),
     "sk": ("gemv_internal.h", "gemv_common.cuh", "gemv_kernel.cuh", "gemv_streamk_kernel.cuh",
            "gemv_streamk_instances.cu", "gemv_dispatch.cu"),
 }
@@ -196,6 +198,16 @@ def split_w4(workload: str) -> tuple[str, bool]:
 
 
 SK_PREFIX = "sk:"
+F8_PREFIX = "f8:"
+
+
+def split_f8(workload: str) -> tuple[str, bool]:
+    """A workload name may start with "f8:": the same shapes with FP8 (E4M3)
+    weights and FP32 row scales."""
+    if workload.startswith(F8_PREFIX):
+        return workload[len(F8_PREFIX):], True
+    return workload, False
+
 
 
 def split_sk(workload: str) -> tuple[str, bool]:
@@ -211,6 +223,7 @@ def describe(workload: str):
     from memory_bound_decode_gb300 import workloads as wl
     workload, _ = split_norm(workload)
     workload, _ = split_sk(workload)
+    workload, _ = split_f8(workload)
     workload, _ = split_w4(workload)
     if workload in ("down_proj", "k_proj", "o_proj", "lm_head"):
         N, K = wl.SHAPES[workload]
@@ -233,15 +246,18 @@ def describe(workload: str):
 class GemvWorkload:
     """Rotating device-resident weight copies for one (possibly fused) GEMV."""
 
-    def __init__(self, kind, rows, K, B, device, l2_bytes, rms_eps=None, w4=False, streamk=False):
+    def __init__(self, kind, rows, K, B, device, l2_bytes, rms_eps=None, w4=False, streamk=False, fp8=False):
         import torch
         from memory_bound_decode_gb300 import inputs, roofline
         self.kind, self.rows, self.K, self.B = kind, rows, K, B
         self.rms_eps = rms_eps
         self.w4 = w4
         self.streamk = streamk
-        if streamk and (w4 or B != 1):
+        self.fp8 = fp8
+        if streamk and (w4 or fp8 or B != 1):
             raise SystemExit("stream-K: BF16 batch-1 workloads only")
+        if fp8 and kind != "single":
+            raise SystemExit("FP8 weights: single-matrix workloads only")
         self.N = sum(rows)
         if w4:
             if kind != "single":
@@ -250,12 +266,19 @@ class GemvWorkload:
             self.lds = K // inputs.W4_GROUP
             self.bytes_per_step = roofline.algorithmic_bytes_w4(self.N, K, B)
             wbytes = self.N * (self.ldq + 2 * self.lds)
+        elif fp8:
+            self.ldq = (K + 15) // 16 * 16
+            self.bytes_per_step = roofline.algorithmic_bytes_fp8(self.N, K, B)
+            wbytes = self.N * (self.ldq + 4)
         else:
             self.ldw = inputs.padded_ldw(K)
             self.bytes_per_step = roofline.algorithmic_bytes(self.N, K, B)
             wbytes = 2 * self.N * self.ldw
         self.copies = max(1, min(64, math.ceil(3 * l2_bytes / wbytes)))
-        if w4:
+        if fp8:
+            self.Ws = [[inputs.fp8_weight(self.N, K, self.ldq, seed=0, index=10 * c, device=device)]
+                       for c in range(self.copies)]
+        elif w4:
             self.Ws = [[inputs.w4_weight_device(self.N, K, self.ldq, self.lds, seed=0, index=10 * c,
                                                 device=device)] for c in range(self.copies)]
         else:
@@ -270,7 +293,11 @@ class GemvWorkload:
         from memory_bound_decode_gb300 import binding
         Ws = self.Ws[i % self.copies]
         x = self.x if x is None else x
-        if self.w4:
+        if self.fp8:
+            Wq, S = Ws[0]
+            binding.gemv_fp8_bf16(Wq, S, x, self.ys[0], self.N, self.K, self.B, self.ldq,
+                                  rms_eps=self.rms_eps, stream=stream)
+        elif self.w4:
             Wq, S = Ws[0]
             binding.gemv_w4_bf16(Wq, S, x, self.ys[0], self.N, self.K, self.B, self.ldq, self.lds,
                                  rms_eps=self.rms_eps, stream=stream)
@@ -290,11 +317,12 @@ class GemvWorkload:
     def config(self) -> dict:
         shape = "+".join(str(n) for n in self.rows)
         norm = f", RMSNorm prologue eps={self.rms_eps}" if self.rms_eps is not None else ""
-        wt = "INT4-weight (128-col groups, BF16 scales)" if self.w4 else "BF16"
+        wt = ("INT4-weight (128-col groups, BF16 scales)" if self.w4 else
+              "FP8-weight (E4M3, FP32 row scales)" if self.fp8 else "BF16")
         sk = ", stream-K one-wave grid" if self.streamk else ""
         return {"workload": f"{self.kind} {wt} GEMV N={shape} K={self.K} B={self.B}{norm}{sk}",
                 "N": self.N, "K": self.K, "B": self.B,
-                "ldw": self.ldq if self.w4 else self.ldw,
+                "ldw": self.ldq if (self.w4 or self.fp8) else self.ldw,
                 "segments": len(self.rows),
                 "l2": f"inputs larger than L2: {self.copies} rotating weight copies, "
                       f"{self.rotating_bytes / 1e6:.0f} MB"}
@@ -375,9 +403,10 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
     kind, rows, K, B = describe(args.workload)
     _, rms_eps = split_norm(args.workload)
     base, streamk = split_sk(split_norm(args.workload)[0])
+    base, fp8 = split_f8(base)
     _, w4 = split_w4(base)
     wk = StepWorkload(device, torch.cuda.Stream(), rms_eps, streamk) if kind == "step" else \
-        GemvWorkload(kind, rows, K, B, device, l2, rms_eps, w4, streamk)
+        GemvWorkload(kind, rows, K, B, device, l2, rms_eps, w4, streamk, fp8)
     torch.cuda.synchronize()
 
     def barrier():
@@ -416,7 +445,7 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
         y_host = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in wk.ys]
         x_dev = torch.empty_like(wk.x)
         e2e_steps = max(10, min(steps, 2000))
-        host_io = kind == "single" and not getattr(wk, "w4", False)
+        host_io = kind == "single" and not getattr(wk, "w4", False) and not getattr(wk, "fp8", False)
         sk = getattr(wk, "streamk", False)
         sh = stream.cuda_stream
 
@@ -453,13 +482,15 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
     peak, peak_kind = load_peaks()
     achieved = wk.bytes_per_step / (seconds / steps) / 1e9 if kind == "step" else \
         wk.bytes_per_step / per_launch_s / 1e9
-    family = ("w4" if getattr(wk, "w4", False) else "sk" if getattr(wk, "streamk", False)
-              else "fma" if wk.B == 1 else "mma")
+    family = ("w4" if getattr(wk, "w4", False) else "f8" if getattr(wk, "fp8", False)
+              else "sk" if getattr(wk, "streamk", False) else "fma" if wk.B == 1 else "mma")
     launch = None
     if kind == "single":
         sms = torch.cuda.get_device_properties(device).multi_processor_count
         if family == "w4":
             launch = binding.gemv_w4_query_launch(wk.N, wk.K, wk.B, sms)
+        elif family == "f8":
+            launch = binding.gemv_fp8_query_launch(wk.N, wk.K, wk.B, sms)
         else:
             launch = binding.gemv_query_launch_ex(wk.N, wk.K, wk.B, sms,
                                                   binding.GEMV_FLAG_STREAMK if family == "sk" else 0)
@@ -471,7 +502,9 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
         "ms_per_step": round(seconds / steps * 1e3, 6),
         "us_per_call": round(per_launch_s * 1e6, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16 in, fp32 accumulate", "data": "synthetic (seeded N(0,0.02^2) weights, N(0,1) x)",
+        "dtype": {"w4": "u4 weights (bf16 group scales), bf16 x, fp32 accumulate",
+                  "f8": "e4m3 weights (fp32 row scales), bf16 x, fp32 accumulate"}.get(family, "bf16 in, fp32 accumulate"),
+        "data": "synthetic (seeded N(0,0.02^2) weights, N(0,1) x)",
         "config": dict(wk.config(), parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
                        pdl=os.environ.get("GEMV_PDL", "1") != "0"),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": UNIT,
@@ -479,6 +512,7 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
                      "peak_kind": f"{peak_kind} copy (MEASURED_PEAKS hbm_gbs, burst)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "kernel": ("gemv_w4_kernel (INT4 codes, BF16 tensor cores)" if family == "w4"
+                                else "gemv_fp8_kernel (E4M3 codes, BF16 tensor cores)" if family == "f8"
                                 else "gemv_streamk_kernel (CUDA cores, one-wave grid)" if family == "sk"
                                 else "gemv_bf16_kernel (CUDA cores)" if wk.B == 1
                                 else "gemv_bf16_mma_kernel (BF16 tensor cores)"),

@@ -239,7 +239,8 @@ typedef struct {
     int32_t smem_bytes;      /* dynamic shared memory per CTA                     */
     int32_t path;            /* 0: CUDA-core FP32 FMA (batch 1), 1: BF16 tensor-core MMA,
                                 2: INT4 weights on the BF16 tensor cores,
-                                3: stream-K, batch 1 (CUDA cores, one-wave grid) */
+                                3: stream-K, batch 1 (CUDA cores, one-wave grid),
+                                4: FP8 weights on the BF16 tensor cores */
     int32_t xstride;         /* shared-memory elements per staged x row           */
     int32_t nbuf;            /* x buffers: 2 when the K-range is staged in chunks */
     /* stream-K (path 3) only; zero otherwise: */
@@ -321,6 +322,30 @@ int gemv_w4_bf16(const void *Wq, const void *S, const void *x, float *y,
 /* gemv_query_launch for the INT4-weight GEMV (K a multiple of 128). */
 int gemv_w4_query_launch(int64_t N, int64_t K, int B, int sm_count,
                          gemv_launch_info *out);
+
+/*
+ * y = W·x with FP8 weights ("Decode GEMV at half of HBM bandwidth", "What
+ * interviewers probe next": INT4, then FP8 weights). Element (n, k) of W is
+ * e4m3(Wq[n][k]) * S[n]:
+ *   Wq : N rows of ldq bytes (ldq >= K, ldq % 16 == 0, Wq 16-byte aligned),
+ *        one E4M3 code per weight: sign in bit 7, exponent bits 3..6 with bias
+ *        7, mantissa bits 0..2, subnormals at exponent 0. The two NaN codes
+ *        (0x7F, 0xFF) must not occur in columns k < K (the kernel reads them
+ *        as 480); columns k >= K are never read.
+ *   S  : N FP32 scales, one per output row (4-byte aligned).
+ *   x, y, B and the options as for gemv_bf16_ex; K must be a multiple of 64.
+ * The codes are widened to BF16 exactly in registers and contracted on the
+ * BF16 tensor cores with FP32 accumulation for every B; each row's sum is
+ * multiplied by S[n] once at the end. Accuracy bound and tolerance as for
+ * gemv_bf16, with |W[n][k]| = |e4m3(Wq[n][k])| * S[n].
+ */
+int gemv_fp8_bf16(const void *Wq, const float *S, const void *x, float *y,
+                  int64_t N, int64_t K, int B, int64_t ldq,
+                  const gemv_options *opt, void *stream);
+
+/* gemv_query_launch for the FP8-weight GEMV (K a multiple of 64). */
+int gemv_fp8_query_launch(int64_t N, int64_t K, int B, int sm_count,
+                          gemv_launch_info *out);
 
 /*
  * Read-only bandwidth probe: streams `bytes` (a multiple of 16, >= 16) from the

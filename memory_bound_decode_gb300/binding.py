@@ -35,7 +35,7 @@ EXPORTED = [
     "gemv_plan_create", "gemv_plan_capture",
     "gemv_plan_launch", "gemv_plan_num_launches", "gemv_plan_destroy",
     "gemv_query_launch", "gemv_query_launch_ex", "gemv_workspace_release", "gemv_bf16_streamk_noalloc",
-    "gemv_w4_bf16", "gemv_w4_query_launch",
+    "gemv_w4_bf16", "gemv_w4_query_launch", "gemv_fp8_bf16", "gemv_fp8_query_launch",
     "gemv_probe_stream_read", "gemv_probe_sink_words",
     "gemv_status_string", "gemv_last_cuda_error",
 ]
@@ -119,6 +119,10 @@ def lib() -> ctypes.CDLL:
                                        ctypes.POINTER(gemv_options), vp]
             L.gemv_w4_query_launch.argtypes = [i64, i64, ctypes.c_int, ctypes.c_int,
                                                ctypes.POINTER(gemv_launch_info)]
+            L.gemv_fp8_bf16.argtypes = [vp, vp, vp, vp, i64, i64, ctypes.c_int, i64,
+                                        ctypes.POINTER(gemv_options), vp]
+            L.gemv_fp8_query_launch.argtypes = [i64, i64, ctypes.c_int, ctypes.c_int,
+                                                ctypes.POINTER(gemv_launch_info)]
             L.gemv_probe_stream_read.argtypes = [vp, i64, vp, vp]
             L.gemv_probe_sink_words.argtypes = []
             L.gemv_status_string.argtypes = [ctypes.c_int]
@@ -245,6 +249,20 @@ def gemv_w4_bf16(Wq, S, x, y, N: int, K: int, B: int, ldq: int, lds: int, rms_ep
 def gemv_w4_query_launch(N: int, K: int, B: int, sm_count: int) -> dict:
     info = gemv_launch_info()
     _check(lib().gemv_w4_query_launch(N, K, B, sm_count, ctypes.byref(info)), "gemv_w4_query_launch")
+    return info.as_dict()
+
+
+def gemv_fp8_bf16(Wq, S, x, y, N: int, K: int, B: int, ldq: int, rms_eps=None,
+                  stream=None, check: bool = True, options=None) -> int:
+    """FP8 (E4M3) weights with FP32 row scales S (see gemv.h)."""
+    opt = ctypes.byref(options) if options is not None else _options(rms_eps)
+    rc = lib().gemv_fp8_bf16(_ptr(Wq), _ptr(S), _ptr(x), _ptr(y), N, K, B, ldq, opt, _stream(stream))
+    return _check(rc, "gemv_fp8_bf16") if check else rc
+
+
+def gemv_fp8_query_launch(N: int, K: int, B: int, sm_count: int) -> dict:
+    info = gemv_launch_info()
+    _check(lib().gemv_fp8_query_launch(N, K, B, sm_count, ctypes.byref(info)), "gemv_fp8_query_launch")
     return info.as_dict()
 
 

@@ -279,6 +279,49 @@ int prepare_w4(const void* Wq, const void* S, const void* x, float* y, int64_t N
     return GEMV_OK;
 }
 
+int check_fp8(const void* Wq, const float* S, const void* x, const float* y, int64_t N, int64_t K, int B,
+              int64_t ldq) {
+    if (!Wq || !S || !x || !y) return GEMV_ERR_INVALID;
+    if (N < 1 || N > 0x7fffffffLL || K < gemv::kF8Slot || K > 0x7fffffffLL || K % gemv::kF8Slot != 0)
+        return GEMV_ERR_INVALID;
+    if (B < 1 || B > GEMV_MAX_BATCH || ldq < K) return GEMV_ERR_INVALID;
+    if (ldq % 16 != 0 || !aligned(Wq, 16) || !aligned(S, 4) || !aligned(x, 2) || !aligned(y, 4))
+        return GEMV_ERR_ALIGN;
+    return GEMV_OK;
+}
+
+// Validate and plan one FP8-weight GEMV.
+int prepare_fp8(const void* Wq, const float* S, const void* x, float* y, int64_t N, int64_t K, int B,
+                int64_t ldq, int flags, float eps, int sm_count, Prepared* out) {
+    Launch l;
+    int rc = gemv::plan_launch(N, K, B, sm_count, &l, gemv::kWeightFp8);
+    if (rc != GEMV_OK) return rc;
+    Params p;
+    std::memset(&p, 0, sizeof p);
+    p.seg[0].W = static_cast<const uint16_t*>(Wq);
+    p.seg[0].y = y;
+    p.seg[0].N = N;
+    p.seg[0].ldw = ldq;
+    p.seg[0].tile_begin = 0;
+    p.seg[0].rs = S;
+    p.x = static_cast<const uint16_t*>(x);
+    p.K = K;
+    p.kslice = l.kslice;
+    p.kchunk = l.kchunk;
+    p.nseg = 1;
+    p.splits = l.splits;
+    p.kw = l.kw;
+    p.xstride = l.xstride;
+    p.batch = B;
+    p.nbuf = l.nbuf;
+    p.flags = (flags & GEMV_FLAG_RMSNORM) ? gemv::kFlagRmsNorm : 0;
+    p.rms_eps = eps;
+    out->p = p;
+    out->l = l;
+    out->B = B;
+    return GEMV_OK;
+}
+
 int check_w4(const void* Wq, const void* S, const void* x, const float* y, int64_t N, int64_t K, int B,
              int64_t ldq, int64_t lds) {
     if (!Wq || !S || !x || !y) return GEMV_ERR_INVALID;
@@ -638,6 +681,45 @@ int gemv_w4_bf16(const void* Wq, const void* S, const void* x, float* y, int64_t
     Prepared pr;
     if ((rc = prepare_w4(Wq, S, x, y, N, K, B, ldq, lds, flags, eps, sm_count, &pr)) != GEMV_OK) return rc;
     return run(pr, static_cast<cudaStream_t>(stream));
+}
+
+int gemv_fp8_bf16(const void* Wq, const float* S, const void* x, float* y, int64_t N, int64_t K, int B,
+                  int64_t ldq, const gemv_options* opt, void* stream) {
+    int rc = check_fp8(Wq, S, x, y, N, K, B, ldq);
+    if (rc != GEMV_OK) return rc;
+    int flags = 0;
+    float eps = 0.f;
+    if ((rc = check_options(opt, &flags, &eps)) != GEMV_OK) return rc;
+    if (flags & GEMV_FLAG_STREAMK) return GEMV_ERR_UNSUPPORTED;
+    int sm_count = 0;
+    if ((rc = device_state(&sm_count)) != GEMV_OK) return rc;
+    Prepared pr;
+    if ((rc = prepare_fp8(Wq, S, x, y, N, K, B, ldq, flags, eps, sm_count, &pr)) != GEMV_OK) return rc;
+    return run(pr, static_cast<cudaStream_t>(stream));
+}
+
+int gemv_fp8_query_launch(int64_t N, int64_t K, int B, int sm_count, gemv_launch_info* out) {
+    if (!out) return GEMV_ERR_INVALID;
+    if (K < gemv::kF8Slot || K % gemv::kF8Slot != 0) return GEMV_ERR_INVALID;
+    std::memset(out, 0, sizeof *out);
+    Launch l;
+    int rc = gemv::plan_launch(N, K, B, sm_count, &l, gemv::kWeightFp8);
+    if (rc != GEMV_OK) return rc;
+    out->rows_per_cta = l.rows_per_cta;
+    out->row_tiles = l.row_tiles;
+    out->grid = l.grid;
+    out->kslice = l.kslice;
+    out->kchunk = l.kchunk;
+    out->warps_per_cta = gemv::kWarps;
+    out->warps_per_row = l.kw;
+    out->splits = l.splits;
+    out->rows_per_warp = l.rows_per_warp;
+    out->unroll = l.unroll;
+    out->smem_bytes = l.smem_bytes;
+    out->path = l.path;
+    out->xstride = l.xstride;
+    out->nbuf = l.nbuf;
+    return GEMV_OK;
 }
 
 int gemv_w4_query_launch(int64_t N, int64_t K, int B, int sm_count, gemv_launch_info* out) {

@@ -239,6 +239,7 @@ struct SegView {
     int64_t tile_local;
     const uint16_t* S;   // INT4 weights: group scales
     int64_t lds;
+    const float* rs;     // FP8 weights: row scales
 };
 
 __device__ __forceinline__ SegView segment_of(const Params& p, int64_t tile) {
@@ -254,6 +255,7 @@ __device__ __forceinline__ SegView segment_of(const Params& p, int64_t tile) {
     s.tile_local = tile - p.seg[si].tile_begin;
     s.S = p.seg[si].S;
     s.lds = p.seg[si].lds;
+    s.rs = p.seg[si].rs;
     return s;
 }
 

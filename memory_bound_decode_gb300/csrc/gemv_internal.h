@@ -23,6 +23,7 @@ struct Seg {
     int64_t tile_begin;
     const uint16_t* S;     // INT4 weights: BF16 group scales [N, lds]; unused otherwise
     int64_t lds;
+    const float* rs;       // FP8 weights: FP32 row scales [N]; unused otherwise
 };
 
 // Everything one launch needs; passed by value as a __grid_constant__.
@@ -56,15 +57,20 @@ enum Path : int32_t {
     kPathMma = 1,       // BF16 tensor-core mma.sync, one warp streams a 16-row tile
     kPathW4 = 2,        // INT4 weights dequantised to BF16 in registers, tensor-core mma.sync
     kPathStreamK = 3,   // batch 1, one wave of CTAs, warps take balanced ranges of (row, K-unit)
+    kPathFp8 = 4,       // FP8 (E4M3) weights widened to BF16 in registers, tensor-core mma.sync
 };
 
 // Weight formats the planner knows.
 enum WeightKind : int32_t {
     kWeightBf16 = 0,
     kWeightInt4 = 1,   // 128-column groups, BF16 scales
+    kWeightFp8 = 2,    // E4M3 codes, FP32 row scales
 };
 constexpr int kW4Group = 128;
 constexpr int kW4Unroll = 4;      // 128-column groups in flight per lane (2 x 16 B each)
+constexpr int kF8Slot = 64;       // FP8: columns of one slot (4 lanes x 16 codes); K is a multiple
+constexpr int kF8Unroll = 4;      // slots in flight per lane (2 x 16 B each)
+constexpr int kF8DeepUnroll = 8;  // the deep instance (up to 8 rows of x): 2 CTAs per SM
 
 // Compile-time shape of the CUDA-core kernel instance for batch B.
 struct Variant {

@@ -36,10 +36,36 @@ int64_t round_up(int64_t a, int64_t m) { return cdiv(a, m) * m; }
 
 }  // namespace
 
+namespace {
+int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind, int f8_unroll);
+}  // namespace
+
 int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind) {
+    // FP8 with up to 8 rows: the deep instance (kF8DeepUnroll slots in flight
+    // per lane; 2 CTAs per SM by registers) when its grid fits in one wave of
+    // it and spreads over the SMs at least as evenly as the kF8Unroll plan's:
+    // with CTAs of equal work the busiest SM sets the time, so the share of
+    // CTA places in use, grid / (SMs * ceil(grid / SMs)), is compared
+    // (measured per decode shape).
+    int rc = plan_with(N, K, B, sm_count, out, weight_kind, kF8Unroll);
+    if (rc != GEMV_OK || weight_kind != kWeightFp8 || B > 8) return rc;
+    Launch deep;
+    if (plan_with(N, K, B, sm_count, &deep, weight_kind, kF8DeepUnroll) != GEMV_OK) return rc;
+    auto balance = [&](int64_t grid) {
+        const int64_t per_sm = cdiv(grid, sm_count);
+        return static_cast<double>(grid) / static_cast<double>(per_sm * sm_count);
+    };
+    if (deep.grid <= 2LL * sm_count && balance(deep.grid) >= balance(out->grid)) *out = deep;
+    return GEMV_OK;
+}
+
+namespace {
+
+int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind, int f8_unroll) {
     if (!out || N < 1 || K < 1 || B < 1 || B > kMaxBatch || sm_count < 1) return GEMV_ERR_INVALID;
-    if (weight_kind != kWeightBf16 && weight_kind != kWeightInt4) return GEMV_ERR_INVALID;
-    const Path path = weight_kind == kWeightInt4 ? kPathW4 : path_for(B);
+    if (weight_kind != kWeightBf16 && weight_kind != kWeightInt4 && weight_kind != kWeightFp8)
+        return GEMV_ERR_INVALID;
+    const Path path = weight_kind == kWeightInt4 ? kPathW4 : weight_kind == kWeightFp8 ? kPathFp8 : path_for(B);
     int group_rows, unroll, xpad;
     int64_t batch_cols, warp_inflight;
     bool cluster_first;
@@ -58,13 +84,20 @@ int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weig
         warp_inflight = 32LL * 16 * kMmaUnroll * 2;
         cluster_first = true;
         xpad = kMmaXPad;
-    } else {
+    } else if (path == kPathW4) {
         group_rows = kMmaRows;
         unroll = kW4Unroll;
         batch_cols = static_cast<int64_t>(kW4Group) * kW4Unroll;   // one group per slot
         warp_inflight = 32LL * 16 * kW4Unroll * 2;
         cluster_first = true;
         xpad = kW4XPad;
+    } else {
+        group_rows = kMmaRows;
+        unroll = f8_unroll;
+        batch_cols = static_cast<int64_t>(kF8Slot) * f8_unroll;
+        warp_inflight = 32LL * 16 * f8_unroll * 2;
+        cluster_first = true;
+        xpad = kMmaXPad;
     }
     const int64_t target_warps = static_cast<int64_t>(sm_count) * kTargetInflightPerSm / warp_inflight;
     auto warps_for = [&](int kw, int splits) {
@@ -76,7 +109,22 @@ int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weig
     };
 
     int kw = 1, splits = 1;
-    if (path == kPathW4 && B == 1) {
+    if (path == kPathFp8 && B == 1) {
+        // FP8, one activation row (measured per decode shape): at least two
+        // warps along K, more warps along K while the grid lacks warps, CTAs
+        // along K only when even that leaves the GPU short of half of them.
+        if (room(kw, splits)) kw = 2;
+        while (kw < kWarps && warps_for(kw, splits) < target_warps && room(kw, splits)) kw *= 2;
+        while (splits < kMaxSplits && warps_for(kw, splits) < target_warps / 2 && room(kw, splits)) splits *= 2;
+    } else if (path == kPathFp8) {
+        // FP8, several rows: CTAs along K first (at most 4 for more than 8
+        // rows, whose staged x is twice as large), then warps along K up to half
+        // the target; from 8 rows on at least two CTAs, which halves the x each stages.
+        const int max_s = B > 8 ? 4 : kMaxSplits;
+        while (splits < max_s && warps_for(kw, splits) < target_warps && room(kw, splits)) splits *= 2;
+        while (kw < kWarps && warps_for(kw, splits) < target_warps / 2 && room(kw, splits)) kw *= 2;
+        if (B >= 8 && splits == 1 && room(kw, splits)) splits = 2;
+    } else if (path == kPathW4 && B == 1) {
         // INT4, one activation row: two warps along K first, then CTAs along K
         // (measured best on the decode shapes).
         while (kw < 2 && warps_for(kw, splits) < target_warps && room(kw, splits)) kw *= 2;
@@ -98,10 +146,11 @@ int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weig
         while (splits < kMaxSplits && warps_for(kw, splits) < target_warps && room(kw, splits)) splits *= 2;
     }
 
-    // On the tensor-core path, trade warps along K for CTAs along K while the
-    // CTA's x slice does not fit in one staged chunk (same warps, fewer x bytes
-    // per CTA, no chunk barriers).
-    if (cluster_first) {
+    // On the BF16 and INT4 tensor-core paths, trade warps along K for CTAs
+    // along K while the CTA's x slice does not fit in one staged chunk (same
+    // warps, fewer x bytes per CTA, no chunk barriers). The FP8 kernel measured
+    // faster with the chunks.
+    if (cluster_first && path != kPathFp8) {
         while (splits < kMaxSplits && kw > 1 &&
                static_cast<int64_t>(B) * (cdiv(K, splits) + xpad) * 2 > kXBudgetBytes) {
             splits *= 2;
@@ -147,6 +196,8 @@ int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weig
     out->nbuf = nbuf;
     return GEMV_OK;
 }
+
+}  // namespace
 
 // Stream-K (batch 1): one wave of CTAs, as many as fit on an SM by shared
 // memory (the whole x row) and registers (kSkMaxCtasPerSm for whole units,

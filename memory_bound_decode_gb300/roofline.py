@@ -26,6 +26,12 @@ def algorithmic_bytes_w4(N: int, K: int, B: int = 1, group: int = 128) -> int:
     return N * K // 2 + 2 * N * (K // group) + 2 * B * K + 4 * B * N
 
 
+def algorithmic_bytes_fp8(N: int, K: int, B: int = 1) -> int:
+    """The same for FP8 weights: N*K bytes of E4M3 codes plus N FP32 row scales
+    (the bytes fall two times against BF16)."""
+    return N * K + 4 * N + 2 * B * K + 4 * B * N
+
+
 def flops(N: int, K: int, B: int = 1) -> int:
     """One multiply and one add per weight element per batch row."""
     return 2 * B * N * K

@@ -216,3 +216,25 @@ def test_streamk_noalloc_rejects(L):
     assert f(A16, A16, A16, 8, 8, 4) == binding.GEMV_ERR_INVALID          # ldw < K
     assert f(A16, A16, A16 + 2, 8, 8, 8) == binding.GEMV_ERR_ALIGN        # y misaligned
     assert f(A16 + 8, A16, A16, 8, 8, 8) == binding.GEMV_ERR_ALIGN        # W not 16-byte aligned
+
+
+def test_fp8_argument_checks(L):
+    f = lambda Wq, S, x, y, N, K, B, ldq: binding.gemv_fp8_bf16(Wq, S, x, y, N, K, B, ldq, stream=0, check=False)
+    assert f(0, A16, A16, A16, 8, 64, 1, 64) == binding.GEMV_ERR_INVALID          # Wq NULL
+    assert f(A16, 0, A16, A16, 8, 64, 1, 64) == binding.GEMV_ERR_INVALID          # S NULL
+    assert f(A16, A16, A16, A16, 8, 96, 1, 96) == binding.GEMV_ERR_INVALID        # K % 64
+    assert f(A16, A16, A16, A16, 8, 64, 1, 48) == binding.GEMV_ERR_INVALID        # ldq < K
+    assert f(A16, A16, A16, A16, 8, 64, 17, 64) == binding.GEMV_ERR_INVALID       # B > 16
+    assert f(A16, A16, A16, A16, 8, 64, 1, 72) == binding.GEMV_ERR_ALIGN          # ldq % 16
+    assert f(A16 + 8, A16, A16, A16, 8, 64, 1, 64) == binding.GEMV_ERR_ALIGN      # Wq alignment
+    assert f(A16, A16 + 2, A16, A16, 8, 64, 1, 64) == binding.GEMV_ERR_ALIGN      # S alignment
+
+
+@pytest.mark.parametrize("N,K,B", [(4096, 14336, 1), (128256, 4096, 1), (4096, 14336, 16), (7, 64, 3)])
+def test_fp8_query(L, N, K, B):
+    q = binding.gemv_fp8_query_launch(N, K, B, 152)
+    assert q["path"] == 4 and q["rows_per_warp"] == 16
+    assert q["grid"] == q["row_tiles"] * q["splits"]
+    assert q["kslice"] % 64 == 0 and q["xstride"] >= q["kchunk"]
+    with pytest.raises(binding.GemvError):
+        binding.gemv_fp8_query_launch(N, 100, B, 152)
