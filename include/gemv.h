@@ -265,6 +265,18 @@ int gemv_query_launch_ex(int64_t N, int64_t K, int B, int sm_count, int flags,
 int gemv_workspace_release(void);
 
 /*
+ * Test support, not part of the method. In a library built with
+ * -DGEMV_DEBUG_WRITECOUNT every kernel store to an output element also adds 1
+ * to counts[element - y_base], or to counts[n] for a store outside
+ * [y_base, y_base + n), for every launch prepared (or plan created) after the
+ * call; counts = NULL turns it off. counts: n + 1 int32 on the device, zeroed
+ * by the caller. It checks that each output is written exactly once and
+ * nothing else is. Other builds return GEMV_ERR_UNSUPPORTED and never count.
+ * Not thread-safe.
+ */
+int gemv_debug_write_count(int32_t *counts, const float *y_base, int64_t n);
+
+/*
  * gemv_bf16_ex with GEMV_FLAG_STREAMK for callers that must not allocate
  * device memory: the same stream-K kernel (batch 1, same results bit for bit),
  * with its partial sums and per-row counters in a fixed scratch area compiled

@@ -10,6 +10,7 @@ current PyTorch stream).
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -35,6 +36,7 @@ EXPORTED = [
     "gemv_plan_create", "gemv_plan_capture",
     "gemv_plan_launch", "gemv_plan_num_launches", "gemv_plan_destroy",
     "gemv_query_launch", "gemv_query_launch_ex", "gemv_workspace_release", "gemv_bf16_streamk_noalloc",
+    "gemv_debug_write_count",
     "gemv_w4_bf16", "gemv_w4_query_launch", "gemv_fp8_bf16", "gemv_fp8_query_launch",
     "gemv_probe_stream_read", "gemv_probe_sink_words",
     "gemv_status_string", "gemv_last_cuda_error",
@@ -89,51 +91,73 @@ def lib() -> ctypes.CDLL:
     global _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(LIB_PATH):
-                raise RuntimeError(f"libgemv.so is not built ({LIB_PATH}); "
-                                   "run memory_bound_decode_gb300.build_lib.build()")
-            L = ctypes.CDLL(LIB_PATH)
-            L.gemv_bf16.argtypes = [vp, vp, vp, i64, i64, ctypes.c_int, i64, vp]
-            L.gemv_bf16_multi.argtypes = [ctypes.POINTER(gemv_segment), ctypes.c_int, vp, i64,
-                                          ctypes.c_int, vp]
-            L.gemv_bf16_ex.argtypes = [vp, vp, vp, i64, i64, ctypes.c_int, i64,
-                                       ctypes.POINTER(gemv_options), vp]
-            L.gemv_bf16_multi_ex.argtypes = [ctypes.POINTER(gemv_segment), ctypes.c_int, vp, i64,
-                                             ctypes.c_int, ctypes.POINTER(gemv_options), vp]
-            L.gemv_bf16_host_io.argtypes = [vp, vp, vp, vp, vp, i64, i64, ctypes.c_int, i64,
-                                            ctypes.POINTER(gemv_options), vp]
-            L.gemv_plan_create.argtypes = [ctypes.POINTER(gemv_proj), ctypes.c_int,
-                                           ctypes.POINTER(vp)]
-            L.gemv_plan_capture.argtypes = [vp, vp]
-            L.gemv_plan_launch.argtypes = [vp, vp]
-            L.gemv_plan_num_launches.argtypes = [vp]
-            L.gemv_plan_destroy.argtypes = [vp]
-            L.gemv_plan_destroy.restype = None
-            L.gemv_query_launch.argtypes = [i64, i64, ctypes.c_int, ctypes.c_int,
-                                            ctypes.POINTER(gemv_launch_info)]
-            L.gemv_query_launch_ex.argtypes = [i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                               ctypes.POINTER(gemv_launch_info)]
-            L.gemv_workspace_release.argtypes = []
-            L.gemv_bf16_streamk_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.POINTER(gemv_options), vp]
-            L.gemv_w4_bf16.argtypes = [vp, vp, vp, vp, i64, i64, ctypes.c_int, i64, i64,
-                                       ctypes.POINTER(gemv_options), vp]
-            L.gemv_w4_query_launch.argtypes = [i64, i64, ctypes.c_int, ctypes.c_int,
-                                               ctypes.POINTER(gemv_launch_info)]
-            L.gemv_fp8_bf16.argtypes = [vp, vp, vp, vp, i64, i64, ctypes.c_int, i64,
-                                        ctypes.POINTER(gemv_options), vp]
-            L.gemv_fp8_query_launch.argtypes = [i64, i64, ctypes.c_int, ctypes.c_int,
-                                                ctypes.POINTER(gemv_launch_info)]
-            L.gemv_probe_stream_read.argtypes = [vp, i64, vp, vp]
-            L.gemv_probe_sink_words.argtypes = []
-            L.gemv_status_string.argtypes = [ctypes.c_int]
-            L.gemv_status_string.restype = ctypes.c_char_p
-            L.gemv_last_cuda_error.argtypes = []
-            for name in EXPORTED:
-                f = getattr(L, name)
-                if name not in ("gemv_plan_destroy", "gemv_status_string"):
-                    f.restype = ctypes.c_int
-            _lib = L
+            _lib = _load(LIB_PATH)
         return _lib
+
+
+@contextlib.contextmanager
+def use_library(path: str):
+    """Route every call in the block to another build of the library (the
+    store-counting test build); the default library is restored afterwards."""
+    global _lib
+    other = _load(path)
+    with _lock:
+        saved = _lib
+        _lib = other
+    try:
+        yield other
+    finally:
+        with _lock:
+            _lib = saved
+
+
+def _load(path: str) -> ctypes.CDLL:
+    """Load one build of the library and declare its signatures."""
+    if not os.path.exists(path):
+        raise RuntimeError(f"libgemv.so is not built ({path}); "
+                           "run memory_bound_decode_gb300.build_lib.build()")
+    L = ctypes.CDLL(path)
+    L.gemv_bf16.argtypes = [vp, vp, vp, i64, i64, ctypes.c_int, i64, vp]
+    L.gemv_bf16_multi.argtypes = [ctypes.POINTER(gemv_segment), ctypes.c_int, vp, i64,
+                                  ctypes.c_int, vp]
+    L.gemv_bf16_ex.argtypes = [vp, vp, vp, i64, i64, ctypes.c_int, i64,
+                               ctypes.POINTER(gemv_options), vp]
+    L.gemv_bf16_multi_ex.argtypes = [ctypes.POINTER(gemv_segment), ctypes.c_int, vp, i64,
+                                     ctypes.c_int, ctypes.POINTER(gemv_options), vp]
+    L.gemv_bf16_host_io.argtypes = [vp, vp, vp, vp, vp, i64, i64, ctypes.c_int, i64,
+                                    ctypes.POINTER(gemv_options), vp]
+    L.gemv_plan_create.argtypes = [ctypes.POINTER(gemv_proj), ctypes.c_int,
+                                   ctypes.POINTER(vp)]
+    L.gemv_plan_capture.argtypes = [vp, vp]
+    L.gemv_plan_launch.argtypes = [vp, vp]
+    L.gemv_plan_num_launches.argtypes = [vp]
+    L.gemv_plan_destroy.argtypes = [vp]
+    L.gemv_plan_destroy.restype = None
+    L.gemv_query_launch.argtypes = [i64, i64, ctypes.c_int, ctypes.c_int,
+                                    ctypes.POINTER(gemv_launch_info)]
+    L.gemv_query_launch_ex.argtypes = [i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.POINTER(gemv_launch_info)]
+    L.gemv_workspace_release.argtypes = []
+    L.gemv_debug_write_count.argtypes = [vp, vp, i64]
+    L.gemv_bf16_streamk_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.POINTER(gemv_options), vp]
+    L.gemv_w4_bf16.argtypes = [vp, vp, vp, vp, i64, i64, ctypes.c_int, i64, i64,
+                               ctypes.POINTER(gemv_options), vp]
+    L.gemv_w4_query_launch.argtypes = [i64, i64, ctypes.c_int, ctypes.c_int,
+                                       ctypes.POINTER(gemv_launch_info)]
+    L.gemv_fp8_bf16.argtypes = [vp, vp, vp, vp, i64, i64, ctypes.c_int, i64,
+                                ctypes.POINTER(gemv_options), vp]
+    L.gemv_fp8_query_launch.argtypes = [i64, i64, ctypes.c_int, ctypes.c_int,
+                                        ctypes.POINTER(gemv_launch_info)]
+    L.gemv_probe_stream_read.argtypes = [vp, i64, vp, vp]
+    L.gemv_probe_sink_words.argtypes = []
+    L.gemv_status_string.argtypes = [ctypes.c_int]
+    L.gemv_status_string.restype = ctypes.c_char_p
+    L.gemv_last_cuda_error.argtypes = []
+    for name in EXPORTED:
+        f = getattr(L, name)
+        if name not in ("gemv_plan_destroy", "gemv_status_string"):
+            f.restype = ctypes.c_int
+    return L
 
 
 def _ptr(t) -> int | None:
@@ -233,6 +257,12 @@ def gemv_bf16_streamk_noalloc(W, x, y, N: int, K: int, ldw: int, rms_eps=None, s
     rc = lib().gemv_bf16_streamk_noalloc(_ptr(W), _ptr(x), _ptr(y), N, K, ldw, _options(rms_eps),
                                          _stream(stream))
     return _check(rc, "gemv_bf16_streamk_noalloc") if check else rc
+
+
+def gemv_debug_write_count(counts, y_base, n: int, check: bool = True) -> int:
+    """Test support (a GEMV_DEBUG_WRITECOUNT build only): count output stores."""
+    rc = lib().gemv_debug_write_count(_ptr(counts), _ptr(y_base), n)
+    return _check(rc, "gemv_debug_write_count") if check else rc
 
 
 def gemv_workspace_release() -> int:

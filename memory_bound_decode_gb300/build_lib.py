@@ -8,6 +8,7 @@ runtime that PyTorch loads.
 """
 from __future__ import annotations
 
+import hashlib
 import os
 import shutil
 import subprocess
@@ -61,11 +62,20 @@ def _newest(paths) -> float:
     return max(os.path.getmtime(p) for p in paths)
 
 
+LIB_DEBUG = os.path.join(OUT_DIR, "libgemv_debug.so")
+DEBUG_FLAGS = ("-DGEMV_DEBUG_WRITECOUNT",)
+
+
+def build_debug(force: bool = False, verbose: bool = False) -> str:
+    """The test build that counts output stores (gemv_debug_write_count)."""
+    return build(force=force, verbose=verbose, extra_flags=DEBUG_FLAGS, lib=LIB_DEBUG)
+
+
 def build(force: bool = False, verbose: bool = False, extra_flags=(), lib: str = LIB) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
     os.makedirs(OBJ_DIR, exist_ok=True)
     headers = [os.path.normpath(os.path.join(CSRC, h)) for h in HEADERS]
-    tag = "" if not extra_flags else "_" + str(abs(hash(tuple(extra_flags))) % 10**8)
+    tag = "" if not extra_flags else "_" + hashlib.sha256("\0".join(extra_flags).encode()).hexdigest()[:10]
     hdr_time = _newest(headers)
 
     def compile_one(src: str) -> str:

@@ -21,6 +21,10 @@ namespace {
 
 thread_local int g_last_cuda_error = 0;
 
+// Output-store counting for tests (gemv_debug_write_count); copied into every
+// launch prepared while set. Only a build with GEMV_DEBUG_WRITECOUNT sets it.
+gemv::WriteCount g_write_count = {nullptr, nullptr, 0};
+
 int cuda_fail(cudaError_t e) {
     g_last_cuda_error = static_cast<int>(e);
     return GEMV_ERR_CUDA;
@@ -185,6 +189,7 @@ int prepare_streamk(const gemv_segment* segs, int nsegs, int64_t total, const vo
     p.xstride = l.xstride;
     p.flags = (flags & GEMV_FLAG_RMSNORM) ? gemv::kFlagRmsNorm : 0;
     p.rms_eps = eps;
+    p.wc = g_write_count;
     out->sk = true;
     out->skp = p;
     out->skl = l;
@@ -240,6 +245,7 @@ int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B
     p.nbuf = l.nbuf;
     p.flags = (flags & GEMV_FLAG_RMSNORM) ? gemv::kFlagRmsNorm : 0;
     p.rms_eps = eps;
+    p.wc = g_write_count;
     out->p = p;
     out->l = l;
     out->B = B;
@@ -273,6 +279,7 @@ int prepare_w4(const void* Wq, const void* S, const void* x, float* y, int64_t N
     p.nbuf = l.nbuf;
     p.flags = (flags & GEMV_FLAG_RMSNORM) ? gemv::kFlagRmsNorm : 0;
     p.rms_eps = eps;
+    p.wc = g_write_count;
     out->p = p;
     out->l = l;
     out->B = B;
@@ -316,6 +323,7 @@ int prepare_fp8(const void* Wq, const float* S, const void* x, float* y, int64_t
     p.nbuf = l.nbuf;
     p.flags = (flags & GEMV_FLAG_RMSNORM) ? gemv::kFlagRmsNorm : 0;
     p.rms_eps = eps;
+    p.wc = g_write_count;
     out->p = p;
     out->l = l;
     out->B = B;
@@ -553,6 +561,19 @@ void gemv_plan_destroy(gemv_plan* plan) {
     if (plan->graph) cudaGraphDestroy(plan->graph);
     ws_free(plan->ws);
     delete plan;
+}
+
+int gemv_debug_write_count(int32_t* counts, const float* y_base, int64_t n) {
+#ifdef GEMV_DEBUG_WRITECOUNT
+    if (counts && (!y_base || n < 1)) return GEMV_ERR_INVALID;
+    g_write_count = counts ? gemv::WriteCount{counts, y_base, n} : gemv::WriteCount{nullptr, nullptr, 0};
+    return GEMV_OK;
+#else
+    (void)counts;
+    (void)y_base;
+    (void)n;
+    return GEMV_ERR_UNSUPPORTED;
+#endif
 }
 
 int gemv_workspace_release(void) {

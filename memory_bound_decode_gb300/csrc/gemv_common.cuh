@@ -174,6 +174,21 @@ __device__ __forceinline__ void xsq_accumulate(const uint16_t* xbuf, int xstride
     }
 }
 
+// Store one output element. A build with GEMV_DEBUG_WRITECOUNT also counts the
+// store in the caller's array (test support: every element must be written
+// exactly once); other builds only store.
+__device__ __forceinline__ void store_y(float* dst, float v, const WriteCount& wc) {
+    *dst = v;
+#ifdef GEMV_DEBUG_WRITECOUNT
+    if (wc.counts) {
+        const int64_t i = dst - wc.base;
+        atomicAdd(wc.counts + ((i >= 0 && i < wc.n) ? i : wc.n), 1);
+    }
+#else
+    (void)wc;
+#endif
+}
+
 // Where warp kq of a row group puts its partial sum of (row_local, b): rows
 // of B + 1 floats, so that the lanes of a warp writing neighbouring rows do
 // not fall on the same shared-memory bank.
@@ -188,7 +203,8 @@ __device__ __forceinline__ int red_index(int kq, int rows_per_cta, int row_local
 // output once.
 __device__ __forceinline__ void combine_and_store(const float* red, float* cpart, float* misc, int rows_per_cta,
                                                   int B, int kw, int S, int split, int64_t n_base, int64_t N,
-                                                  float* __restrict__ y, bool norm, int64_t K, float eps) {
+                                                  float* __restrict__ y, bool norm, int64_t K, float eps,
+                                                  const WriteCount& wc) {
     float* xsq = misc + kWarps * kMaxBatch;
     float* rsc = xsq + kMaxBatch;
     __syncthreads();
@@ -203,7 +219,7 @@ __device__ __forceinline__ void combine_and_store(const float* red, float* cpart
         for (int q = 1; q < kw; ++q) s += red[red_index(q, rows_per_cta, rl, B, b)];
         if (S == 1) {
             const int64_t n = n_base + rl;
-            if (n < N) y[static_cast<int64_t>(b) * N + n] = norm ? s * rsc[b] : s;
+            if (n < N) store_y(y + static_cast<int64_t>(b) * N + n, norm ? s * rsc[b] : s, wc);
         } else {
             cpart[i] = s;
         }
@@ -224,7 +240,7 @@ __device__ __forceinline__ void combine_and_store(const float* red, float* cpart
             for (int q = 1; q < S; ++q) s += ld_dsmem(&cpart[i], static_cast<uint32_t>(q));
             const int rl = i / B, b = i - (i / B) * B;
             const int64_t n = n_base + rl;
-            if (n < N) y[static_cast<int64_t>(b) * N + n] = norm ? s * rsc[b] : s;
+            if (n < N) store_y(y + static_cast<int64_t>(b) * N + n, norm ? s * rsc[b] : s, wc);
         }
         cluster_sync_all();   // no CTA leaves while another still reads its shared memory
     }

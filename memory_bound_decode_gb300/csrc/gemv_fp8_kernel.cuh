@@ -250,7 +250,7 @@ gemv_fp8_kernel(const __grid_constant__ Params p) {
         }
     }
     combine_and_store(red, cpart, misc, rows_per_cta, B, kw, S, split, sg.tile_local * rows_per_cta, sg.N, sg.y,
-                      norm, K, p.rms_eps);
+                      norm, K, p.rms_eps, p.wc);
 }
 
 template <int NB, int UJ>

@@ -26,6 +26,15 @@ struct Seg {
     const float* rs;       // FP8 weights: FP32 row scales [N]; unused otherwise
 };
 
+// Test support: where a build with GEMV_DEBUG_WRITECOUNT counts output
+// stores (counts[element - base], counts[n] for a store outside [base, base + n)).
+// Null counts: no counting. Other builds never read it.
+struct WriteCount {
+    int32_t* counts;
+    const float* base;
+    int64_t n;
+};
+
 // Everything one launch needs; passed by value as a __grid_constant__.
 struct Params {
     Seg seg[kMaxSegs];
@@ -41,6 +50,7 @@ struct Params {
     int32_t nbuf;     // x buffers (2 when the K-range takes more than one chunk)
     int32_t flags;    // kFlagRmsNorm
     float rms_eps;    // epsilon of the RMSNorm prologue
+    WriteCount wc;
 };
 
 // Scale each output row b by (mean_k x[b][k]^2 + rms_eps)^(-1/2) (RMSNorm
@@ -135,6 +145,7 @@ struct SkParams {
     int32_t xstride;      // staged x elements (whole vectors up to K)
     int32_t flags;        // kFlagRmsNorm
     float rms_eps;
+    WriteCount wc;
 };
 
 struct SkLaunch {

@@ -242,7 +242,7 @@ gemv_bf16_kernel(const __grid_constant__ Params p) {
             for (int b = 0; b < B; ++b) red[red_index(kq, rows_per_cta, g * RPW + r, B, b)] = acc[r][b];
     }
     combine_and_store(red, cpart, misc, rows_per_cta, B, kw, S, split, sg.tile_local * rows_per_cta, sg.N, sg.y,
-                      norm, K, p.rms_eps);
+                      norm, K, p.rms_eps, p.wc);
 }
 
 template <int B>

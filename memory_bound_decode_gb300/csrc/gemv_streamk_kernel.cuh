@@ -182,7 +182,7 @@ gemv_streamk_kernel(const __grid_constant__ SkParams p) {
         if (lane != 0) continue;
 
         if (cbd == 0 && ced == C) {   // the whole row is this warp's
-            *yout = norm ? s * rs : s;
+            store_y(yout, norm ? s * rs : s, p.wc);
             continue;
         }
         // A split-part row cut between warps wa .. wb (row index nl relative to
@@ -202,7 +202,7 @@ gemv_streamk_kernel(const __grid_constant__ SkParams p) {
             const int side_a = (sk_begin(wa, U, NW) < nl * C) ? 1 : 0;
             float v = __ldcg(&p.part[2 * wa + side_a]);
             for (int32_t q = wa + 1; q <= wb; ++q) v += __ldcg(&p.part[2 * q]);
-            *yout = norm ? v * rs : v;
+            store_y(yout, norm ? v * rs : v, p.wc);
             p.ticket[nl] = 0;
         }
     }

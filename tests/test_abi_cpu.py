@@ -238,3 +238,8 @@ def test_fp8_query(L, N, K, B):
     assert q["kslice"] % 64 == 0 and q["xstride"] >= q["kchunk"]
     with pytest.raises(binding.GemvError):
         binding.gemv_fp8_query_launch(N, 100, B, 152)
+
+
+def test_write_count_is_debug_only(L):
+    # the product build never counts stores
+    assert binding.gemv_debug_write_count(A16, A16, 8, check=False) == binding.GEMV_ERR_UNSUPPORTED
