@@ -78,6 +78,7 @@ enum WeightKind : int32_t {
 };
 constexpr int kW4Group = 128;
 constexpr int kW4Unroll = 4;      // 128-column groups in flight per lane (2 x 16 B each)
+constexpr int kW4DeepUnroll = 8;  // the deep instance (up to 8 rows of x, one x chunk): 2 CTAs per SM
 constexpr int kF8Slot = 64;       // FP8: columns of one slot (4 lanes x 16 codes); K is a multiple
 constexpr int kF8Unroll = 4;      // slots in flight per lane (2 x 16 B each)
 constexpr int kF8DeepUnroll = 8;  // the deep instance (up to 8 rows of x): 2 CTAs per SM

@@ -271,6 +271,11 @@ gemv_w4_kernel(const __grid_constant__ Params p) {
 
 template <int NB>
 cudaError_t launch_w4(const Params& p, const Launch& l, cudaStream_t s, bool pdl) {
+    if (l.unroll == kW4DeepUnroll) {   // the deep instance: up to 8 rows, one x chunk
+        if (NB != 1 || l.nbuf != 1) return cudaErrorInvalidValue;
+        return launch_kernel(gemv_w4_kernel<1, kW4DeepUnroll, false>, p, l, s, pdl);
+    }
+    if (l.unroll != kW4Unroll) return cudaErrorInvalidValue;
     if (l.nbuf > 1) return launch_kernel(gemv_w4_kernel<NB, kW4Unroll, true>, p, l, s, pdl);
     return launch_kernel(gemv_w4_kernel<NB, kW4Unroll, false>, p, l, s, pdl);
 }
@@ -280,6 +285,10 @@ cudaError_t prepare_w4() {
     cudaError_t e = cudaFuncSetAttribute(gemv_w4_kernel<NB, kW4Unroll, true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
     if (e != cudaSuccess) return e;
+    if (NB == 1 && (e = cudaFuncSetAttribute(gemv_w4_kernel<1, kW4DeepUnroll, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem)) !=
+                       cudaSuccess)
+        return e;
     return cudaFuncSetAttribute(gemv_w4_kernel<NB, kW4Unroll, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
 }

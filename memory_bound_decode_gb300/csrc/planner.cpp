@@ -37,20 +37,23 @@ int64_t round_up(int64_t a, int64_t m) { return cdiv(a, m) * m; }
 }  // namespace
 
 namespace {
-int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind, int f8_unroll);
+int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind, int q_unroll);
 }  // namespace
 
 int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind) {
-    // FP8 with up to 8 rows: the deep instance (kF8DeepUnroll slots in flight
-    // per lane; 2 CTAs per SM by registers) when its grid fits in one wave of
-    // it and spreads over the SMs at least as evenly as the kF8Unroll plan's:
-    // with CTAs of equal work the busiest SM sets the time, so the share of
-    // CTA places in use, grid / (SMs * ceil(grid / SMs)), is compared
+    // INT4 and FP8 with up to 8 rows: the deep instance (8 slots in flight per
+    // lane; 2 CTAs per SM by registers, one x chunk) when its grid fits in one
+    // wave of it and spreads over the SMs at least as evenly as the standard
+    // plan's: with CTAs of equal work the busiest SM sets the time, so the
+    // share of CTA places in use, grid / (SMs * ceil(grid / SMs)), is compared
     // (measured per decode shape).
-    int rc = plan_with(N, K, B, sm_count, out, weight_kind, kF8Unroll);
-    if (rc != GEMV_OK || weight_kind != kWeightFp8 || B > 8) return rc;
+    const bool w4 = weight_kind == kWeightInt4, f8 = weight_kind == kWeightFp8;
+    int rc = plan_with(N, K, B, sm_count, out, weight_kind, w4 ? kW4Unroll : kF8Unroll);
+    if (rc != GEMV_OK || !(w4 || f8) || B > 8) return rc;
     Launch deep;
-    if (plan_with(N, K, B, sm_count, &deep, weight_kind, kF8DeepUnroll) != GEMV_OK) return rc;
+    if (plan_with(N, K, B, sm_count, &deep, weight_kind, w4 ? kW4DeepUnroll : kF8DeepUnroll) != GEMV_OK ||
+        deep.nbuf != 1)
+        return rc;
     auto balance = [&](int64_t grid) {
         const int64_t per_sm = cdiv(grid, sm_count);
         return static_cast<double>(grid) / static_cast<double>(per_sm * sm_count);
@@ -61,7 +64,7 @@ int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weig
 
 namespace {
 
-int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind, int f8_unroll) {
+int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind, int q_unroll) {
     if (!out || N < 1 || K < 1 || B < 1 || B > kMaxBatch || sm_count < 1) return GEMV_ERR_INVALID;
     if (weight_kind != kWeightBf16 && weight_kind != kWeightInt4 && weight_kind != kWeightFp8)
         return GEMV_ERR_INVALID;
@@ -86,16 +89,16 @@ int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight
         xpad = kMmaXPad;
     } else if (path == kPathW4) {
         group_rows = kMmaRows;
-        unroll = kW4Unroll;
-        batch_cols = static_cast<int64_t>(kW4Group) * kW4Unroll;   // one group per slot
-        warp_inflight = 32LL * 16 * kW4Unroll * 2;
+        unroll = q_unroll;
+        batch_cols = static_cast<int64_t>(kW4Group) * q_unroll;   // one group per slot
+        warp_inflight = 32LL * 16 * q_unroll * 2;
         cluster_first = true;
         xpad = kW4XPad;
     } else {
         group_rows = kMmaRows;
-        unroll = f8_unroll;
-        batch_cols = static_cast<int64_t>(kF8Slot) * f8_unroll;
-        warp_inflight = 32LL * 16 * f8_unroll * 2;
+        unroll = q_unroll;
+        batch_cols = static_cast<int64_t>(kF8Slot) * q_unroll;
+        warp_inflight = 32LL * 16 * q_unroll * 2;
         cluster_first = true;
         xpad = kMmaXPad;
     }
