@@ -130,12 +130,17 @@ int gemv_bf16_ex(const void *W, const void *x, float *y,
 /*
  * gemv_bf16_ex for a caller whose activations live in host memory: copies x
  * from x_host (B*K BF16, pinned memory recommended) to the device buffer x_dev,
- * runs the GEMV into the device buffer y_dev, copies y back to y_host (B*N
- * floats) and waits for the stream, so y_host holds the result on return. The
- * device buffers are the caller's (x_dev B*K BF16, 16-byte aligned; y_dev B*N
- * floats); the library allocates nothing (but the stream-K workspace, see
- * GEMV_FLAG_STREAMK). This is the whole host-to-host path
- * of one decode-step projection, timed end to end by the benchmark.
+ * runs the GEMV, brings y to y_host (B*N floats) and waits for the stream, so
+ * y_host holds the result on return. When y is at most 256 KB and y_host is
+ * pinned memory mapped into the device's address space (cudaHostAlloc / pinned
+ * tensors under unified addressing, or cudaHostRegister with the mapped flag)
+ * the kernel stores y straight into it and y_dev is not used; otherwise the
+ * GEMV writes y_dev and a device-to-host copy follows. The wait polls the stream for up to a
+ * millisecond before it blocks. The device buffers are the caller's (x_dev B*K
+ * BF16, 16-byte aligned; y_dev B*N floats); the library allocates nothing (but
+ * the stream-K workspace, see GEMV_FLAG_STREAMK). This is the whole
+ * host-to-host path of one decode-step projection, timed end to end by the
+ * benchmark.
  */
 int gemv_bf16_host_io(const void *W, const void *x_host, float *y_host,
                       void *x_dev, float *y_dev,

@@ -1,6 +1,7 @@
 // C-ABI front end of libgemv.so: argument checks, per-device set-up, fused
 // launches and the CUDA-graph decode-step plan. Every operation on data runs
 // in the kernels; this file only validates, plans and launches.
+#include <chrono>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -87,6 +88,9 @@ bool pdl_enabled() {
     }();
     return on;
 }
+
+// Largest y that gemv_bf16_host_io stores straight into mapped host memory.
+constexpr size_t kMappedYMaxBytes = 256 * 1024;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -409,10 +413,31 @@ int gemv_bf16_host_io(const void* W, const void* x_host, float* y_host, void* x_
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t xbytes = static_cast<size_t>(B) * static_cast<size_t>(K) * 2;
     const size_t ybytes = static_cast<size_t>(B) * static_cast<size_t>(N) * 4;
+    // A device-mapped y_host (pinned memory) takes the kernel's stores directly
+    // when y is small; a large y goes back in one bulk copy (the kernel's
+    // scattered 32-byte stores cross the host link less efficiently).
+    float* y_mapped = nullptr;
+    void* dp = nullptr;
+    if (ybytes <= kMappedYMaxBytes && cudaHostGetDevicePointer(&dp, y_host, 0) == cudaSuccess && aligned(dp, 4)) {
+        y_mapped = static_cast<float*>(dp);
+    } else {
+        cudaGetLastError();   // not mapped: the copy path below
+    }
     cudaError_t e = cudaMemcpyAsync(x_dev, x_host, xbytes, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e);
-    if ((rc = gemv_bf16_ex(W, x_dev, y_dev, N, K, B, ldw, opt, stream)) != GEMV_OK) return rc;
-    if ((e = cudaMemcpyAsync(y_host, y_dev, ybytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess) return cuda_fail(e);
+    if ((rc = gemv_bf16_ex(W, x_dev, y_mapped ? y_mapped : y_dev, N, K, B, ldw, opt, stream)) != GEMV_OK) return rc;
+    if (!y_mapped &&
+        (e = cudaMemcpyAsync(y_host, y_dev, ybytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return cuda_fail(e);
+    // Poll for up to a millisecond (a decode step is tens of microseconds and a
+    // blocking wait adds a wake-up), then block.
+    const auto t0 = std::chrono::steady_clock::now();
+    for (;;) {
+        e = cudaStreamQuery(s);
+        if (e == cudaSuccess) return GEMV_OK;
+        if (e != cudaErrorNotReady) return cuda_fail(e);
+        if (std::chrono::steady_clock::now() - t0 > std::chrono::milliseconds(1)) break;
+    }
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e);
     return GEMV_OK;
 }

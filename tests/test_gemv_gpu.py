@@ -208,3 +208,23 @@ def test_host_io_round_trip():
     gu.assert_parity(y_host.numpy(), y_ref, sc)
     binding.gemv_bf16_host_io(W, x_host, y_host, x_dev, y_dev, N, K, B, ldw, rms_eps=1e-5, stream=s)
     assert np.isfinite(y_host.numpy()).all()
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_io_pinned_and_pageable(pinned):
+    """Pinned (device-mapped) y_host takes the kernel's stores directly; pageable
+    y_host goes through y_dev and a copy. Both hold the result on return."""
+    N, K, B = 4097, 4103, 3
+    W, x, ldw = make(N, K, B, seed=13)
+    x_host = x.cpu()
+    y_host = torch.full((B, N), float("nan"))
+    if pinned:
+        x_host, y_host = x_host.pin_memory(), y_host.pin_memory()
+    y_dev = torch.full((B, N), float("nan"), device=DEV)
+    binding.gemv_bf16_host_io(W, x_host, y_host, torch.empty_like(x), y_dev, N, K, B, ldw)
+    y_ref, sc = gu.reference(W, x, K)
+    gu.assert_parity(y_host.numpy(), y_ref, sc, f"pinned={pinned}")
+    for _ in range(3):   # repeated calls, no stale results
+        y_host.fill_(float("nan"))
+        binding.gemv_bf16_host_io(W, x_host, y_host, torch.empty_like(x), y_dev, N, K, B, ldw)
+        gu.assert_parity(y_host.numpy(), y_ref, sc, f"pinned={pinned} repeat")
