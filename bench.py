@@ -199,6 +199,16 @@ def split_w4(workload: str) -> tuple[str, bool]:
 
 SK_PREFIX = "sk:"
 F8_PREFIX = "f8:"
+CC_PREFIX = "cc:"
+
+
+def split_cc(workload: str) -> tuple[str, bool]:
+    """A workload name may start with "cc:": the same BF16 projections on the
+    CUDA-core kernel at every batch size (GEMV_FLAG_CUDA_CORES)."""
+    if workload.startswith(CC_PREFIX):
+        return workload[len(CC_PREFIX):], True
+    return workload, False
+
 
 
 def split_f8(workload: str) -> tuple[str, bool]:
@@ -223,6 +233,7 @@ def describe(workload: str):
     from memory_bound_decode_gb300 import workloads as wl
     workload, _ = split_norm(workload)
     workload, _ = split_sk(workload)
+    workload, _ = split_cc(workload)
     workload, _ = split_f8(workload)
     workload, _ = split_w4(workload)
     if workload in ("down_proj", "k_proj", "o_proj", "lm_head"):
@@ -246,7 +257,8 @@ def describe(workload: str):
 class GemvWorkload:
     """Rotating device-resident weight copies for one (possibly fused) GEMV."""
 
-    def __init__(self, kind, rows, K, B, device, l2_bytes, rms_eps=None, w4=False, streamk=False, fp8=False):
+    def __init__(self, kind, rows, K, B, device, l2_bytes, rms_eps=None, w4=False, streamk=False, fp8=False,
+                 cuda_cores=False):
         import torch
         from memory_bound_decode_gb300 import inputs, roofline
         self.kind, self.rows, self.K, self.B = kind, rows, K, B
@@ -254,6 +266,9 @@ class GemvWorkload:
         self.w4 = w4
         self.streamk = streamk
         self.fp8 = fp8
+        self.cuda_cores = cuda_cores
+        if cuda_cores and (w4 or fp8 or streamk):
+            raise SystemExit("cc: BF16 workloads only")
         if streamk and (w4 or fp8 or B != 1):
             raise SystemExit("stream-K: BF16 batch-1 workloads only")
         if fp8 and kind != "single":
@@ -301,25 +316,27 @@ class GemvWorkload:
             Wq, S = Ws[0]
             binding.gemv_w4_bf16(Wq, S, x, self.ys[0], self.N, self.K, self.B, self.ldq, self.lds,
                                  rms_eps=self.rms_eps, stream=stream)
-        elif self.kind == "single" and self.rms_eps is None and not self.streamk:
+        elif self.kind == "single" and self.rms_eps is None and not self.streamk and not self.cuda_cores:
             binding.gemv_bf16(Ws[0], x, self.ys[0], self.N, self.K, self.B, self.ldw, stream)
         elif self.kind == "single":
             binding.gemv_bf16_ex(Ws[0], x, self.ys[0], self.N, self.K, self.B, self.ldw,
-                                 rms_eps=self.rms_eps, stream=stream, streamk=self.streamk)
-        elif self.rms_eps is None and not self.streamk:
+                                 rms_eps=self.rms_eps, stream=stream, streamk=self.streamk,
+                                 cuda_cores=self.cuda_cores)
+        elif self.rms_eps is None and not self.streamk and not self.cuda_cores:
             binding.gemv_bf16_multi([(W, y, n, self.ldw) for W, y, n in zip(Ws, self.ys, self.rows)],
                                     x, self.K, self.B, stream)
         else:
             binding.gemv_bf16_multi_ex([(W, y, n, self.ldw) for W, y, n in zip(Ws, self.ys, self.rows)],
                                        x, self.K, self.B, rms_eps=self.rms_eps, stream=stream,
-                                       streamk=self.streamk)
+                                       streamk=self.streamk, cuda_cores=self.cuda_cores)
 
     def config(self) -> dict:
         shape = "+".join(str(n) for n in self.rows)
         norm = f", RMSNorm prologue eps={self.rms_eps}" if self.rms_eps is not None else ""
         wt = ("INT4-weight (128-col groups, BF16 scales)" if self.w4 else
               "FP8-weight (E4M3, FP32 row scales)" if self.fp8 else "BF16")
-        sk = ", stream-K one-wave grid" if self.streamk else ""
+        sk = (", stream-K one-wave grid" if self.streamk else
+              ", CUDA-core kernel" if self.cuda_cores else "")
         return {"workload": f"{self.kind} {wt} GEMV N={shape} K={self.K} B={self.B}{norm}{sk}",
                 "N": self.N, "K": self.K, "B": self.B,
                 "ldw": self.ldq if (self.w4 or self.fp8) else self.ldw,
@@ -403,10 +420,11 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
     kind, rows, K, B = describe(args.workload)
     _, rms_eps = split_norm(args.workload)
     base, streamk = split_sk(split_norm(args.workload)[0])
+    base, cuda_cores = split_cc(base)
     base, fp8 = split_f8(base)
     _, w4 = split_w4(base)
     wk = StepWorkload(device, torch.cuda.Stream(), rms_eps, streamk) if kind == "step" else \
-        GemvWorkload(kind, rows, K, B, device, l2, rms_eps, w4, streamk, fp8)
+        GemvWorkload(kind, rows, K, B, device, l2, rms_eps, w4, streamk, fp8, cuda_cores)
     torch.cuda.synchronize()
 
     def barrier():
@@ -453,7 +471,7 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
             if host_io:
                 binding.gemv_bf16_host_io(wk.Ws[i % wk.copies][0], x_host, y_host[0], x_dev, wk.ys[0],
                                           wk.N, wk.K, wk.B, wk.ldw, rms_eps=wk.rms_eps, stream=sh,
-                                          streamk=sk)
+                                          streamk=sk, cuda_cores=getattr(wk, "cuda_cores", False))
             else:
                 x_dev.copy_(x_host, non_blocking=True)
                 wk.step(i, stream, x_dev)
@@ -483,7 +501,8 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
     achieved = wk.bytes_per_step / (seconds / steps) / 1e9 if kind == "step" else \
         wk.bytes_per_step / per_launch_s / 1e9
     family = ("w4" if getattr(wk, "w4", False) else "f8" if getattr(wk, "fp8", False)
-              else "sk" if getattr(wk, "streamk", False) else "fma" if wk.B == 1 else "mma")
+              else "sk" if getattr(wk, "streamk", False)
+              else "fma" if (wk.B == 1 or getattr(wk, "cuda_cores", False)) else "mma")
     launch = None
     if kind == "single":
         sms = torch.cuda.get_device_properties(device).multi_processor_count
@@ -492,8 +511,10 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
         elif family == "f8":
             launch = binding.gemv_fp8_query_launch(wk.N, wk.K, wk.B, sms)
         else:
-            launch = binding.gemv_query_launch_ex(wk.N, wk.K, wk.B, sms,
-                                                  binding.GEMV_FLAG_STREAMK if family == "sk" else 0)
+            launch = binding.gemv_query_launch_ex(
+                wk.N, wk.K, wk.B, sms,
+                binding.GEMV_FLAG_STREAMK if family == "sk" else
+                binding.GEMV_FLAG_CUDA_CORES if getattr(wk, "cuda_cores", False) else 0)
     src_hash = kernel_source_hash(family, launch)
     traffic = profiled_traffic(args.workload, src_hash)
     result = {

@@ -117,6 +117,16 @@ int gemv_bf16(const void *W, const void *x, float *y,
  */
 #define GEMV_FLAG_STREAMK 2
 
+/*
+ * GEMV_FLAG_CUDA_CORES: BF16 weights only. Run the CUDA-core kernel (lanes
+ * along K, FP32 multiply-adds, B accumulators per row) at every batch size,
+ * instead of the BF16 tensor-core kernel the library uses for B >= 2. At
+ * B >= 4 on large matrices the CUDA-core kernel is bound by its arithmetic,
+ * not by HBM. Not combinable with GEMV_FLAG_STREAMK (GEMV_ERR_INVALID);
+ * INT4 and FP8 calls reject it (GEMV_ERR_UNSUPPORTED).
+ */
+#define GEMV_FLAG_CUDA_CORES 4
+
 typedef struct {
     int flags;
     float rms_eps;
@@ -261,7 +271,8 @@ int gemv_query_launch(int64_t N, int64_t K, int B, int sm_count,
                       gemv_launch_info *out);
 
 /* gemv_query_launch for a call with option flags (GEMV_FLAG_STREAMK selects
- * path 3; GEMV_ERR_UNSUPPORTED where that kernel does not apply). */
+ * path 3, GEMV_ERR_UNSUPPORTED where that kernel does not apply;
+ * GEMV_FLAG_CUDA_CORES selects path 0 at every batch size). */
 int gemv_query_launch_ex(int64_t N, int64_t K, int B, int sm_count, int flags,
                          gemv_launch_info *out);
 

@@ -30,6 +30,7 @@ GEMV_MAX_SEGMENTS = 8
 
 GEMV_FLAG_RMSNORM = 1
 GEMV_FLAG_STREAMK = 2
+GEMV_FLAG_CUDA_CORES = 4
 
 EXPORTED = [
     "gemv_bf16", "gemv_bf16_ex", "gemv_bf16_host_io", "gemv_bf16_multi", "gemv_bf16_multi_ex",
@@ -196,36 +197,38 @@ def gemv_bf16(W, x, y, N: int, K: int, B: int, ldw: int, stream=None, check: boo
     return _check(rc, "gemv_bf16") if check else rc
 
 
-def _options(rms_eps, streamk: bool = False):
-    if rms_eps is None and not streamk:
+def _options(rms_eps, streamk: bool = False, cuda_cores: bool = False):
+    if rms_eps is None and not streamk and not cuda_cores:
         return None
-    flags = (GEMV_FLAG_RMSNORM if rms_eps is not None else 0) | (GEMV_FLAG_STREAMK if streamk else 0)
+    flags = ((GEMV_FLAG_RMSNORM if rms_eps is not None else 0) | (GEMV_FLAG_STREAMK if streamk else 0)
+             | (GEMV_FLAG_CUDA_CORES if cuda_cores else 0))
     return ctypes.byref(gemv_options(flags, float(rms_eps) if rms_eps is not None else 0.0))
 
 
 def gemv_bf16_ex(W, x, y, N: int, K: int, B: int, ldw: int, rms_eps=None, stream=None,
-                 check: bool = True, options=None, streamk: bool = False) -> int:
+                 check: bool = True, options=None, streamk: bool = False, cuda_cores: bool = False) -> int:
     """gemv_bf16 with options; ``rms_eps`` (not None) turns on the RMSNorm prologue,
-    ``streamk`` the stream-K kernel. ``options`` (a gemv_options) overrides both."""
-    opt = ctypes.byref(options) if options is not None else _options(rms_eps, streamk)
+    ``streamk`` the stream-K kernel, ``cuda_cores`` the CUDA-core kernel at every
+    batch size. ``options`` (a gemv_options) overrides them."""
+    opt = ctypes.byref(options) if options is not None else _options(rms_eps, streamk, cuda_cores)
     rc = lib().gemv_bf16_ex(_ptr(W), _ptr(x), _ptr(y), N, K, B, ldw, opt, _stream(stream))
     return _check(rc, "gemv_bf16_ex") if check else rc
 
 
 def gemv_bf16_host_io(W, x_host, y_host, x_dev, y_dev, N: int, K: int, B: int, ldw: int, rms_eps=None,
-                      stream=None, check: bool = True, streamk: bool = False) -> int:
+                      stream=None, check: bool = True, streamk: bool = False, cuda_cores: bool = False) -> int:
     """Host x in, host y out, synchronous (see gemv.h)."""
     rc = lib().gemv_bf16_host_io(_ptr(W), _ptr(x_host), _ptr(y_host), _ptr(x_dev), _ptr(y_dev), N, K, B, ldw,
-                                 _options(rms_eps, streamk), _stream(stream))
+                                 _options(rms_eps, streamk, cuda_cores), _stream(stream))
     return _check(rc, "gemv_bf16_host_io") if check else rc
 
 
 def gemv_bf16_multi_ex(segments, x, K: int, B: int, rms_eps=None, stream=None, check: bool = True,
-                       options=None, streamk: bool = False) -> int:
+                       options=None, streamk: bool = False, cuda_cores: bool = False) -> int:
     arr = (gemv_segment * max(1, len(segments)))()
     for i, (W, y, N, ldw) in enumerate(segments):
         arr[i] = gemv_segment(_ptr(W), _ptr(y), N, ldw)
-    opt = ctypes.byref(options) if options is not None else _options(rms_eps, streamk)
+    opt = ctypes.byref(options) if options is not None else _options(rms_eps, streamk, cuda_cores)
     rc = lib().gemv_bf16_multi_ex(arr, len(segments), _ptr(x), K, B, opt, _stream(stream))
     return _check(rc, "gemv_bf16_multi_ex") if check else rc
 

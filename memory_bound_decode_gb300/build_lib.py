@@ -24,6 +24,8 @@ LIB = os.path.join(OUT_DIR, "libgemv.so")
 
 SOURCES = [
     "gemv_fma_instances.cu",
+    "gemv_fma_instances_b3_8.cu",
+    "gemv_fma_instances_b9_16.cu",
     "gemv_mma_instances_nb1.cu",
     "gemv_mma_instances_nb2.cu",
     "gemv_w4_instances.cu",

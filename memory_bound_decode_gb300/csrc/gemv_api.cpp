@@ -112,7 +112,8 @@ int check_options(const gemv_options* opt, int* flags, float* eps) {
     *flags = 0;
     *eps = 0.f;
     if (!opt) return GEMV_OK;
-    if (opt->flags & ~(GEMV_FLAG_RMSNORM | GEMV_FLAG_STREAMK)) return GEMV_ERR_INVALID;
+    if (opt->flags & ~(GEMV_FLAG_RMSNORM | GEMV_FLAG_STREAMK | GEMV_FLAG_CUDA_CORES)) return GEMV_ERR_INVALID;
+    if ((opt->flags & GEMV_FLAG_STREAMK) && (opt->flags & GEMV_FLAG_CUDA_CORES)) return GEMV_ERR_INVALID;
     if (opt->flags & GEMV_FLAG_RMSNORM) {
         if (!std::isfinite(opt->rms_eps) || opt->rms_eps < 0.f) return GEMV_ERR_INVALID;
         *eps = opt->rms_eps;
@@ -221,7 +222,8 @@ int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B
         prepare_streamk(segs, nsegs, total, x, K, flags, eps, sm_count, out) == GEMV_OK)
         return GEMV_OK;
     Launch l;
-    if ((rc = gemv::plan_launch(total, K, B, sm_count, &l)) != GEMV_OK) return rc;
+    const int kind = (flags & GEMV_FLAG_CUDA_CORES) ? gemv::kWeightBf16CudaCores : gemv::kWeightBf16;
+    if ((rc = gemv::plan_launch(total, K, B, sm_count, &l, kind)) != GEMV_OK) return rc;
 
     Params p;
     std::memset(&p, 0, sizeof p);
@@ -372,6 +374,27 @@ int run(const Prepared& pr, cudaStream_t s, Workspace* ws = nullptr) {
     }
     if (e != cudaSuccess) return cuda_fail(e);
     return GEMV_OK;
+}
+
+}  // namespace
+
+namespace {
+
+void fill_info(const Launch& l, gemv_launch_info* out) {
+    out->rows_per_cta = l.rows_per_cta;
+    out->row_tiles = l.row_tiles;
+    out->grid = l.grid;
+    out->kslice = l.kslice;
+    out->kchunk = l.kchunk;
+    out->warps_per_cta = gemv::kWarps;
+    out->warps_per_row = l.kw;
+    out->splits = l.splits;
+    out->rows_per_warp = l.rows_per_warp;
+    out->unroll = l.unroll;
+    out->smem_bytes = l.smem_bytes;
+    out->path = l.path;
+    out->xstride = l.xstride;
+    out->nbuf = l.nbuf;
 }
 
 }  // namespace
@@ -660,7 +683,16 @@ int gemv_bf16_streamk_noalloc(const void* W, const void* x, float* y, int64_t N,
 
 int gemv_query_launch_ex(int64_t N, int64_t K, int B, int sm_count, int flags, gemv_launch_info* out) {
     if (!out) return GEMV_ERR_INVALID;
-    if (flags & ~(GEMV_FLAG_RMSNORM | GEMV_FLAG_STREAMK)) return GEMV_ERR_INVALID;
+    if (flags & ~(GEMV_FLAG_RMSNORM | GEMV_FLAG_STREAMK | GEMV_FLAG_CUDA_CORES)) return GEMV_ERR_INVALID;
+    if ((flags & GEMV_FLAG_STREAMK) && (flags & GEMV_FLAG_CUDA_CORES)) return GEMV_ERR_INVALID;
+    if (flags & GEMV_FLAG_CUDA_CORES) {
+        std::memset(out, 0, sizeof *out);
+        Launch l;
+        int rc = gemv::plan_launch(N, K, B, sm_count, &l, gemv::kWeightBf16CudaCores);
+        if (rc != GEMV_OK) return rc;
+        fill_info(l, out);
+        return GEMV_OK;
+    }
     const bool sk = (flags & GEMV_FLAG_STREAMK) ||
                     (B == 1 && gemv::prefer_streamk(N, K, B, sm_count));
     if (!sk) return gemv_query_launch(N, K, B, sm_count, out);
@@ -697,20 +729,7 @@ int gemv_query_launch(int64_t N, int64_t K, int B, int sm_count, gemv_launch_inf
     Launch l;
     int rc = gemv::plan_launch(N, K, B, sm_count, &l);
     if (rc != GEMV_OK) return rc;
-    out->rows_per_cta = l.rows_per_cta;
-    out->row_tiles = l.row_tiles;
-    out->grid = l.grid;
-    out->kslice = l.kslice;
-    out->kchunk = l.kchunk;
-    out->warps_per_cta = gemv::kWarps;
-    out->warps_per_row = l.kw;
-    out->splits = l.splits;
-    out->rows_per_warp = l.rows_per_warp;
-    out->unroll = l.unroll;
-    out->smem_bytes = l.smem_bytes;
-    out->path = l.path;
-    out->xstride = l.xstride;
-    out->nbuf = l.nbuf;
+    fill_info(l, out);
     return GEMV_OK;
 }
 
@@ -721,7 +740,7 @@ int gemv_w4_bf16(const void* Wq, const void* S, const void* x, float* y, int64_t
     int flags = 0;
     float eps = 0.f;
     if ((rc = check_options(opt, &flags, &eps)) != GEMV_OK) return rc;
-    if (flags & GEMV_FLAG_STREAMK) return GEMV_ERR_UNSUPPORTED;
+    if (flags & (GEMV_FLAG_STREAMK | GEMV_FLAG_CUDA_CORES)) return GEMV_ERR_UNSUPPORTED;
     int sm_count = 0;
     if ((rc = device_state(&sm_count)) != GEMV_OK) return rc;
     Prepared pr;
@@ -736,7 +755,7 @@ int gemv_fp8_bf16(const void* Wq, const float* S, const void* x, float* y, int64
     int flags = 0;
     float eps = 0.f;
     if ((rc = check_options(opt, &flags, &eps)) != GEMV_OK) return rc;
-    if (flags & GEMV_FLAG_STREAMK) return GEMV_ERR_UNSUPPORTED;
+    if (flags & (GEMV_FLAG_STREAMK | GEMV_FLAG_CUDA_CORES)) return GEMV_ERR_UNSUPPORTED;
     int sm_count = 0;
     if ((rc = device_state(&sm_count)) != GEMV_OK) return rc;
     Prepared pr;

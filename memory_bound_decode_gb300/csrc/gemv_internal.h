@@ -75,6 +75,7 @@ enum WeightKind : int32_t {
     kWeightBf16 = 0,
     kWeightInt4 = 1,   // 128-column groups, BF16 scales
     kWeightFp8 = 2,    // E4M3 codes, FP32 row scales
+    kWeightBf16CudaCores = 3,   // BF16 on the CUDA-core kernel at every batch size
 };
 constexpr int kW4Group = 128;
 constexpr int kW4Unroll = 4;      // 128-column groups in flight per lane (2 x 16 B each)

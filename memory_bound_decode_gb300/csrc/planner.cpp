@@ -66,9 +66,13 @@ namespace {
 
 int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind, int q_unroll) {
     if (!out || N < 1 || K < 1 || B < 1 || B > kMaxBatch || sm_count < 1) return GEMV_ERR_INVALID;
-    if (weight_kind != kWeightBf16 && weight_kind != kWeightInt4 && weight_kind != kWeightFp8)
+    if (weight_kind != kWeightBf16 && weight_kind != kWeightInt4 && weight_kind != kWeightFp8 &&
+        weight_kind != kWeightBf16CudaCores)
         return GEMV_ERR_INVALID;
-    const Path path = weight_kind == kWeightInt4 ? kPathW4 : weight_kind == kWeightFp8 ? kPathFp8 : path_for(B);
+    const Path path = weight_kind == kWeightInt4           ? kPathW4
+                      : weight_kind == kWeightFp8          ? kPathFp8
+                      : weight_kind == kWeightBf16CudaCores ? kPathFma
+                                                           : path_for(B);
     int group_rows, unroll, xpad;
     int64_t batch_cols, warp_inflight;
     bool cluster_first;

@@ -161,8 +161,9 @@ def test_planner_rejects(L):
 
 def test_options_rejected_before_launch(L):
     ok = dict(stream=0, check=False)
-    bad_flags = binding.gemv_options(4, 0.0)
-    assert binding.gemv_bf16_ex(A16, A16, A16, 8, 8, 1, 8, options=bad_flags, **ok) == binding.GEMV_ERR_INVALID
+    for flags in (8, 16, binding.GEMV_FLAG_STREAMK | binding.GEMV_FLAG_CUDA_CORES):   # unknown, conflicting
+        bad_flags = binding.gemv_options(flags, 0.0)
+        assert binding.gemv_bf16_ex(A16, A16, A16, 8, 8, 1, 8, options=bad_flags, **ok) == binding.GEMV_ERR_INVALID
     for eps in (-1.0, float("nan"), float("inf")):
         assert binding.gemv_bf16_ex(A16, A16, A16, 8, 8, 1, 8, rms_eps=eps, **ok) == binding.GEMV_ERR_INVALID
         assert binding.gemv_bf16_multi_ex([(A16, A16, 8, 8)], A16, 8, 1, rms_eps=eps, **ok) == binding.GEMV_ERR_INVALID
@@ -243,3 +244,14 @@ def test_fp8_query(L, N, K, B):
 def test_write_count_is_debug_only(L):
     # the product build never counts stores
     assert binding.gemv_debug_write_count(A16, A16, 8, check=False) == binding.GEMV_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("B", [1, 2, 3, 8, 9, 16])
+def test_cuda_core_plans(L, B):
+    for N, K in [(4096, 14336), (7, 129), (33, 65537), (128256, 4096)]:
+        q = binding.gemv_query_launch_ex(N, K, B, GB300_SMS, binding.GEMV_FLAG_CUDA_CORES)
+        assert q["path"] == 0 and q["rows_per_warp"] == 1
+        assert q["grid"] == q["row_tiles"] * q["splits"]
+        assert q["smem_bytes"] <= 112 * 1024
+    with pytest.raises(binding.GemvError):
+        binding.gemv_query_launch_ex(8, 8, 1, GB300_SMS, binding.GEMV_FLAG_CUDA_CORES | binding.GEMV_FLAG_STREAMK)

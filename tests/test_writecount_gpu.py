@@ -1,8 +1,8 @@
 """Every output element is written exactly once and nothing else is written:
 the test build of the library (GEMV_DEBUG_WRITECOUNT) adds 1 per store to a
 counter per element of y (one more counter for stores outside y), on every
-kernel family and launch shape: the CUDA-core kernel with warps and cluster
-CTAs along K and chunked x, the tensor-core kernel, fused segments, the
+kernel family and launch shape: the CUDA-core kernel (every batch size) with
+warps and cluster CTAs along K and chunked x, the tensor-core kernel, fused segments, the
 RMSNorm prologue, INT4 and FP8 weights, the stream-K kernel with rows cut
 between warps, its fixed-scratch entry point, and a captured plan."""
 import numpy as np
@@ -45,10 +45,11 @@ def test_bf16_written_once(debug_lib, N, K, B):
     W = inputs.weight(N, K, ldw, seed=1, device=DEV)
     x = inputs.activations(B, K, seed=2, device=DEV)
     for eps in (None, 1e-5):
-        y, counts = counted(B * N)
-        binding.gemv_bf16_ex(W, x, y, N, K, B, ldw, rms_eps=eps)
-        assert_once(counts, f"N={N} K={K} B={B} eps={eps}")
-        assert torch.isfinite(y).all()
+        for cc in ((False, True) if B > 1 else (False,)):
+            y, counts = counted(B * N)
+            binding.gemv_bf16_ex(W, x, y, N, K, B, ldw, rms_eps=eps, cuda_cores=cc)
+            assert_once(counts, f"N={N} K={K} B={B} eps={eps} cuda_cores={cc}")
+            assert torch.isfinite(y).all()
     binding.gemv_debug_write_count(None, None, 0)
 
 
