@@ -581,9 +581,23 @@ def cpu_baseline(workload: str, seconds: float) -> dict:
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return {"value": round(nbytes * passes / el / 1e9, 4), "unit": UNIT, "cores": threads,
-            "kind": "oracle",
-            "sample": f"{passes} full passes of the FP64 oracle over {n}x{K} (B={B}) in {el:.1f} s"}
+    result = {"value": round(nbytes * passes / el / 1e9, 4), "unit": UNIT, "cores": threads,
+              "kind": "oracle",
+              "sample": f"{passes} full passes of the FP64 oracle over {n}x{K} (B={B}) in {el:.1f} s"}
+    # the same oracle on one core, on a row sample of about a tenth of the time
+    rows = max(1, min(N, int(n * (seconds / 10.0) / max(el / passes * threads, 1e-9))))
+    W1, x1, K1, B1, n1, _, nbytes1 = oracle_sample(workload, rows_cap=rows)
+    passes1 = 0
+    t0 = time.perf_counter()
+    while True:
+        lib.gemv(W1, x1, K1, threads=1)
+        passes1 += 1
+        el1 = time.perf_counter() - t0
+        if el1 >= seconds / 10.0:
+            break
+    result["single_thread"] = {"value": round(nbytes1 * passes1 / el1 / 1e9, 4), "unit": UNIT, "cores": 1,
+                               "sample": f"{passes1} passes over {n1} of {N} rows x K={K1} (B={B1}) in {el1:.1f} s"}
+    return result
 
 
 def run_reference(args, rank: int) -> dict | None:
