@@ -348,15 +348,18 @@ class GemvWorkload:
 class StepWorkload:
     """The full decode-step projection set replayed as one CUDA graph."""
 
-    def __init__(self, device, stream, rms_eps=None, streamk=False):
+    def __init__(self, device, stream, rms_eps=None, streamk=False, weights="bf16"):
         from memory_bound_decode_gb300 import workloads as wl
         self.spec = wl.decode_step_spec()
-        self.data = wl.DecodeStep(self.spec, seed=0, device=device)
+        self.weights = weights
+        self.data = wl.DecodeStep(self.spec, seed=0, device=device, weights=weights)
         self.rms_eps = rms_eps
         self.streamk = streamk
+        self.w4, self.fp8 = weights == "int4", weights == "fp8"
         self.plan = self.data.plan(rms_eps=rms_eps, streamk=streamk)
         self.plan.capture(stream)
-        self.bytes_per_step = wl.step_bytes_formula(self.spec)
+        self.bytes_per_step = (wl.step_bytes_formula(self.spec) if weights == "bf16"
+                               else self.data.algorithmic_bytes())
         self.launches_per_step = self.plan.num_launches()
         self.x = None
         self.B = 1
@@ -367,8 +370,10 @@ class StepWorkload:
     def config(self) -> dict:
         norm = (f"; RMSNorm prologue (eps={self.rms_eps}) on QKV, gate_up and lm_head"
                 if self.rms_eps is not None else "")
+        wt = {"bf16": "BF16", "fp8": "FP8 (E4M3, FP32 row scales)",
+              "int4": "INT4 (128-col groups, BF16 scales)"}[self.weights]
         return {"workload": "decode step: 32 x {QKV 6144x4096, o 4096x4096, gate_up 28672x4096, "
-                            "down 4096x14336} + lm_head 128256x4096, BF16, batch 1, one CUDA graph" + norm,
+                            f"down 4096x14336}} + lm_head 128256x4096, {wt} weights, batch 1, one CUDA graph" + norm,
                 "launches_per_step": self.launches_per_step,
                 "l2": f"inputs larger than L2: {self.data.weight_bytes() / 1e9:.2f} GB of weights per step"}
 
@@ -423,7 +428,8 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
     base, cuda_cores = split_cc(base)
     base, fp8 = split_f8(base)
     _, w4 = split_w4(base)
-    wk = StepWorkload(device, torch.cuda.Stream(), rms_eps, streamk) if kind == "step" else \
+    wk = StepWorkload(device, torch.cuda.Stream(), rms_eps, streamk,
+                      "int4" if w4 else "fp8" if fp8 else "bf16") if kind == "step" else \
         GemvWorkload(kind, rows, K, B, device, l2, rms_eps, w4, streamk, fp8, cuda_cores)
     torch.cuda.synchronize()
 

@@ -187,10 +187,22 @@ int gemv_bf16_multi_ex(const gemv_segment *segs, int nsegs, const void *x,
 
 /*
  * One projection of a decode step. Projections with the same fuse_group > 0,
- * the same x, K, B, flags and rms_eps, that are adjacent in the list, become
- * one fused launch (at most GEMV_MAX_SEGMENTS per launch); fuse_group 0 means
- * "alone". flags and rms_eps are those of gemv_options.
+ * the same x, K, B, flags, rms_eps and weight kind, that are adjacent in the
+ * list, become one fused launch (at most GEMV_MAX_SEGMENTS per launch);
+ * fuse_group 0 means "alone". flags and rms_eps are those of gemv_options.
+ * weight_kind selects the weight format, with the layouts and preconditions
+ * of the single-matrix calls:
+ *   GEMV_WEIGHT_BF16 (0): W BF16 [N, ldw] (gemv_bf16_ex); S and lds unused.
+ *   GEMV_WEIGHT_INT4 (1): W the codes [N, ldw bytes], S the BF16 group scales
+ *                         [N, lds] (gemv_w4_bf16, ldw = ldq).
+ *   GEMV_WEIGHT_FP8  (2): W the E4M3 codes [N, ldw bytes], S the FP32 row
+ *                         scales [N] (gemv_fp8_bf16, ldw = ldq); lds unused.
+ * Quantised kinds take no GEMV_FLAG_STREAMK or GEMV_FLAG_CUDA_CORES.
  */
+#define GEMV_WEIGHT_BF16 0
+#define GEMV_WEIGHT_INT4 1
+#define GEMV_WEIGHT_FP8 2
+
 typedef struct {
     const void *W;
     const void *x;
@@ -202,6 +214,9 @@ typedef struct {
     int fuse_group;
     int flags;
     float rms_eps;
+    int weight_kind;
+    const void *S;
+    int64_t lds;
 } gemv_proj;
 
 typedef struct gemv_plan gemv_plan;   /* opaque; owned by the library */

@@ -32,6 +32,10 @@ GEMV_FLAG_RMSNORM = 1
 GEMV_FLAG_STREAMK = 2
 GEMV_FLAG_CUDA_CORES = 4
 
+GEMV_WEIGHT_BF16 = 0
+GEMV_WEIGHT_INT4 = 1
+GEMV_WEIGHT_FP8 = 2
+
 EXPORTED = [
     "gemv_bf16", "gemv_bf16_ex", "gemv_bf16_host_io", "gemv_bf16_multi", "gemv_bf16_multi_ex",
     "gemv_plan_create", "gemv_plan_capture",
@@ -54,7 +58,7 @@ class gemv_segment(ctypes.Structure):
 class gemv_proj(ctypes.Structure):
     _fields_ = [("W", vp), ("x", vp), ("y", vp), ("N", i64), ("K", i64), ("ldw", i64),
                 ("B", ctypes.c_int), ("fuse_group", ctypes.c_int), ("flags", ctypes.c_int),
-                ("rms_eps", ctypes.c_float)]
+                ("rms_eps", ctypes.c_float), ("weight_kind", ctypes.c_int), ("S", vp), ("lds", i64)]
 
 
 class gemv_options(ctypes.Structure):
@@ -313,8 +317,10 @@ class Plan:
 
     ``projections``: sequence of (W, x, y, N, K, ldw, B, fuse_group),
     (W, x, y, N, K, ldw, B, fuse_group, rms_eps) with rms_eps None for no
-    RMSNorm prologue, or (..., rms_eps, streamk) with streamk a bool. The
-    tensors behind the pointers must outlive the plan; keep them referenced.
+    RMSNorm prologue, (..., rms_eps, streamk) with streamk a bool, or
+    (..., rms_eps, streamk, weight_kind, S, lds) for INT4 / FP8 weights (W the
+    codes, ldw their row stride in bytes, S the scales). The tensors behind the
+    pointers must outlive the plan; keep them referenced.
     """
 
     def __init__(self, projections, keepalive=None):
@@ -324,9 +330,12 @@ class Plan:
             W, x, y, N, K, ldw, B, grp = pr[:8]
             eps = pr[8] if len(pr) > 8 else None
             sk = bool(pr[9]) if len(pr) > 9 else False
+            kind = int(pr[10]) if len(pr) > 10 else GEMV_WEIGHT_BF16
+            S = pr[11] if len(pr) > 11 else None
+            lds = int(pr[12]) if len(pr) > 12 else 0
             flags = (GEMV_FLAG_RMSNORM if eps is not None else 0) | (GEMV_FLAG_STREAMK if sk else 0)
             arr[i] = gemv_proj(_ptr(W), _ptr(x), _ptr(y), N, K, ldw, B, grp, flags,
-                               float(eps) if eps is not None else 0.0)
+                               float(eps) if eps is not None else 0.0, kind, _ptr(S), lds)
         handle = vp()
         _check(lib().gemv_plan_create(arr, n, ctypes.byref(handle)), "gemv_plan_create")
         self._h = handle

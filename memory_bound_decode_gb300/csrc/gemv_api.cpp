@@ -258,26 +258,54 @@ int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B
     return GEMV_OK;
 }
 
-// Validate and plan one INT4-weight GEMV.
-int prepare_w4(const void* Wq, const void* S, const void* x, float* y, int64_t N, int64_t K, int B,
-               int64_t ldq, int64_t lds, int flags, float eps, int sm_count, Prepared* out) {
+// One quantised weight matrix of a launch.
+struct QSeg {
+    const void* Wq;    // codes
+    const void* S;     // INT4: BF16 group scales [N, lds]; FP8: FP32 row scales [N]
+    float* y;
+    int64_t N;
+    int64_t ldq;       // row stride of the codes in bytes
+    int64_t lds;       // INT4 only
+};
+
+// Plan one launch over INT4 (kind gemv::kWeightInt4) or FP8 (gemv::kWeightFp8)
+// segments sharing x, K and B.
+int prepare_quant(int kind, const QSeg* segs, int nsegs, const void* x, int64_t K, int B, int flags, float eps,
+                  int sm_count, Prepared* out) {
+    if (nsegs < 1 || nsegs > GEMV_MAX_SEGMENTS) return GEMV_ERR_INVALID;
+    int64_t total = 0;
+    for (int i = 0; i < nsegs; ++i) {
+        total += segs[i].N;
+        if (total > 0x7fffffffLL) return GEMV_ERR_INVALID;
+    }
     Launch l;
-    int rc = gemv::plan_launch(N, K, B, sm_count, &l, gemv::kWeightInt4);
+    int rc = gemv::plan_launch(total, K, B, sm_count, &l, kind);
     if (rc != GEMV_OK) return rc;
     Params p;
     std::memset(&p, 0, sizeof p);
-    p.seg[0].W = static_cast<const uint16_t*>(Wq);
-    p.seg[0].y = y;
-    p.seg[0].N = N;
-    p.seg[0].ldw = ldq;
-    p.seg[0].tile_begin = 0;
-    p.seg[0].S = static_cast<const uint16_t*>(S);
-    p.seg[0].lds = lds;
+    int64_t tiles = 0;
+    for (int i = 0; i < nsegs; ++i) {
+        p.seg[i].W = static_cast<const uint16_t*>(segs[i].Wq);
+        p.seg[i].y = segs[i].y;
+        p.seg[i].N = segs[i].N;
+        p.seg[i].ldw = segs[i].ldq;
+        p.seg[i].tile_begin = tiles;
+        if (kind == gemv::kWeightInt4) {
+            p.seg[i].S = static_cast<const uint16_t*>(segs[i].S);
+            p.seg[i].lds = segs[i].lds;
+        } else {
+            p.seg[i].rs = static_cast<const float*>(segs[i].S);
+        }
+        tiles += (segs[i].N + l.rows_per_cta - 1) / l.rows_per_cta;
+    }
+    l.row_tiles = tiles;
+    l.grid = tiles * l.splits;
+    if (l.grid > 0x7fffffffLL) return GEMV_ERR_UNSUPPORTED;
     p.x = static_cast<const uint16_t*>(x);
     p.K = K;
     p.kslice = l.kslice;
     p.kchunk = l.kchunk;
-    p.nseg = 1;
+    p.nseg = nsegs;
     p.splits = l.splits;
     p.kw = l.kw;
     p.xstride = l.xstride;
@@ -300,39 +328,6 @@ int check_fp8(const void* Wq, const float* S, const void* x, const float* y, int
     if (B < 1 || B > GEMV_MAX_BATCH || ldq < K) return GEMV_ERR_INVALID;
     if (ldq % 16 != 0 || !aligned(Wq, 16) || !aligned(S, 4) || !aligned(x, 2) || !aligned(y, 4))
         return GEMV_ERR_ALIGN;
-    return GEMV_OK;
-}
-
-// Validate and plan one FP8-weight GEMV.
-int prepare_fp8(const void* Wq, const float* S, const void* x, float* y, int64_t N, int64_t K, int B,
-                int64_t ldq, int flags, float eps, int sm_count, Prepared* out) {
-    Launch l;
-    int rc = gemv::plan_launch(N, K, B, sm_count, &l, gemv::kWeightFp8);
-    if (rc != GEMV_OK) return rc;
-    Params p;
-    std::memset(&p, 0, sizeof p);
-    p.seg[0].W = static_cast<const uint16_t*>(Wq);
-    p.seg[0].y = y;
-    p.seg[0].N = N;
-    p.seg[0].ldw = ldq;
-    p.seg[0].tile_begin = 0;
-    p.seg[0].rs = S;
-    p.x = static_cast<const uint16_t*>(x);
-    p.K = K;
-    p.kslice = l.kslice;
-    p.kchunk = l.kchunk;
-    p.nseg = 1;
-    p.splits = l.splits;
-    p.kw = l.kw;
-    p.xstride = l.xstride;
-    p.batch = B;
-    p.nbuf = l.nbuf;
-    p.flags = (flags & GEMV_FLAG_RMSNORM) ? gemv::kFlagRmsNorm : 0;
-    p.rms_eps = eps;
-    p.wc = g_write_count;
-    out->p = p;
-    out->l = l;
-    out->B = B;
     return GEMV_OK;
 }
 
@@ -498,15 +493,26 @@ int gemv_plan_create(const gemv_proj* projs, int nproj, gemv_plan** out) {
     if (!projs || nproj < 1) return GEMV_ERR_INVALID;
     // Check every projection before touching the device.
     for (int i = 0; i < nproj; ++i) {
-        int rc = check_common(projs[i].x, projs[i].K, projs[i].B);
+        const gemv_proj& q = projs[i];
+        int rc = check_common(q.x, q.K, q.B);
         if (rc != GEMV_OK) return rc;
-        if ((rc = check_matrix(projs[i].W, projs[i].y, projs[i].N, projs[i].K, projs[i].ldw)) != GEMV_OK)
-            return rc;
-        if (projs[i].fuse_group < 0) return GEMV_ERR_INVALID;
-        gemv_options o{projs[i].flags, projs[i].rms_eps};
+        if (q.weight_kind == GEMV_WEIGHT_BF16) {
+            rc = check_matrix(q.W, q.y, q.N, q.K, q.ldw);
+        } else if (q.weight_kind == GEMV_WEIGHT_INT4) {
+            rc = check_w4(q.W, q.S, q.x, q.y, q.N, q.K, q.B, q.ldw, q.lds);
+        } else if (q.weight_kind == GEMV_WEIGHT_FP8) {
+            rc = check_fp8(q.W, static_cast<const float*>(q.S), q.x, q.y, q.N, q.K, q.B, q.ldw);
+        } else {
+            rc = GEMV_ERR_INVALID;
+        }
+        if (rc != GEMV_OK) return rc;
+        if (q.fuse_group < 0) return GEMV_ERR_INVALID;
+        gemv_options o{q.flags, q.rms_eps};
         int f = 0;
         float e = 0.f;
         if ((rc = check_options(&o, &f, &e)) != GEMV_OK) return rc;
+        if (q.weight_kind != GEMV_WEIGHT_BF16 && (f & (GEMV_FLAG_STREAMK | GEMV_FLAG_CUDA_CORES)))
+            return GEMV_ERR_UNSUPPORTED;
     }
     int sm_count = 0;
     int rc = device_state(&sm_count);
@@ -522,14 +528,25 @@ int gemv_plan_create(const gemv_proj* projs, int nproj, gemv_plan** out) {
             if (a.fuse_group > 0) {
                 while (j < nproj && j - i < GEMV_MAX_SEGMENTS && projs[j].fuse_group == a.fuse_group &&
                        projs[j].x == a.x && projs[j].K == a.K && projs[j].B == a.B &&
-                       projs[j].flags == a.flags && projs[j].rms_eps == a.rms_eps)
+                       projs[j].flags == a.flags && projs[j].rms_eps == a.rms_eps &&
+                       projs[j].weight_kind == a.weight_kind)
                     ++j;
             }
-            gemv_segment segs[GEMV_MAX_SEGMENTS];
-            for (int q = i; q < j; ++q) segs[q - i] = gemv_segment{projs[q].W, projs[q].y, projs[q].N, projs[q].ldw};
             Prepared pr;
             const float eps = (a.flags & GEMV_FLAG_RMSNORM) ? a.rms_eps : 0.f;
-            if ((rc = prepare(segs, j - i, a.x, a.K, a.B, a.flags, eps, sm_count, &pr)) != GEMV_OK) {
+            if (a.weight_kind == GEMV_WEIGHT_BF16) {
+                gemv_segment segs[GEMV_MAX_SEGMENTS];
+                for (int q = i; q < j; ++q)
+                    segs[q - i] = gemv_segment{projs[q].W, projs[q].y, projs[q].N, projs[q].ldw};
+                rc = prepare(segs, j - i, a.x, a.K, a.B, a.flags, eps, sm_count, &pr);
+            } else {
+                QSeg segs[GEMV_MAX_SEGMENTS];
+                for (int q = i; q < j; ++q)
+                    segs[q - i] = QSeg{projs[q].W, projs[q].S, projs[q].y, projs[q].N, projs[q].ldw, projs[q].lds};
+                rc = prepare_quant(a.weight_kind == GEMV_WEIGHT_INT4 ? gemv::kWeightInt4 : gemv::kWeightFp8, segs,
+                                   j - i, a.x, a.K, a.B, a.flags, eps, sm_count, &pr);
+            }
+            if (rc != GEMV_OK) {
                 delete plan;
                 return rc;
             }
@@ -744,7 +761,8 @@ int gemv_w4_bf16(const void* Wq, const void* S, const void* x, float* y, int64_t
     int sm_count = 0;
     if ((rc = device_state(&sm_count)) != GEMV_OK) return rc;
     Prepared pr;
-    if ((rc = prepare_w4(Wq, S, x, y, N, K, B, ldq, lds, flags, eps, sm_count, &pr)) != GEMV_OK) return rc;
+    const QSeg seg{Wq, S, y, N, ldq, lds};
+    if ((rc = prepare_quant(gemv::kWeightInt4, &seg, 1, x, K, B, flags, eps, sm_count, &pr)) != GEMV_OK) return rc;
     return run(pr, static_cast<cudaStream_t>(stream));
 }
 
@@ -759,7 +777,8 @@ int gemv_fp8_bf16(const void* Wq, const float* S, const void* x, float* y, int64
     int sm_count = 0;
     if ((rc = device_state(&sm_count)) != GEMV_OK) return rc;
     Prepared pr;
-    if ((rc = prepare_fp8(Wq, S, x, y, N, K, B, ldq, flags, eps, sm_count, &pr)) != GEMV_OK) return rc;
+    const QSeg seg{Wq, S, y, N, ldq, 0};
+    if ((rc = prepare_quant(gemv::kWeightFp8, &seg, 1, x, K, B, flags, eps, sm_count, &pr)) != GEMV_OK) return rc;
     return run(pr, static_cast<cudaStream_t>(stream));
 }
 

@@ -45,21 +45,32 @@ def decode_step_spec(**overrides) -> dict:
 @dataclass
 class Proj:
     name: str
-    W: torch.Tensor
+    W: torch.Tensor          # BF16 weights, or the INT4 / FP8 codes
     x: torch.Tensor
     y: torch.Tensor
     N: int
     K: int
-    ldw: int
+    ldw: int                 # row stride (elements for BF16, bytes for codes)
     group: int
+    S: torch.Tensor | None = None   # INT4 group scales / FP8 row scales
+    lds: int = 0
+
+
+WEIGHT_KINDS = {"bf16": binding.GEMV_WEIGHT_BF16, "int4": binding.GEMV_WEIGHT_INT4,
+                "fp8": binding.GEMV_WEIGHT_FP8}
 
 
 class DecodeStep:
-    """Device-resident weights, activations and outputs of one decode step."""
+    """Device-resident weights, activations and outputs of one decode step, with
+    BF16, INT4 (128-column groups, BF16 scales) or FP8 (E4M3, FP32 row scales)
+    weights."""
 
-    def __init__(self, spec: dict, seed: int = 0, device="cuda"):
+    def __init__(self, spec: dict, seed: int = 0, device="cuda", weights: str = "bf16"):
+        if weights not in WEIGHT_KINDS:
+            raise ValueError(f"weights must be one of {sorted(WEIGHT_KINDS)}")
         self.spec = spec
         self.device = device
+        self.weights = weights
         self.projs: list[Proj] = []
         self.xs: list[tuple[torch.Tensor, int]] = []
         H, I, V = spec["hidden"], spec["intermediate"], spec["vocab"]
@@ -84,10 +95,17 @@ class DecodeStep:
         self._add("lm_head", V, H, xl, 0, seed, base)
 
     def _add(self, name, N, K, x, group, seed, index):
-        ldw = inputs.padded_ldw(K)
-        W = inputs.weight(N, K, ldw, seed=seed, index=index, device=self.device)
         y = torch.empty((1, N), dtype=torch.float32, device=self.device)
-        self.projs.append(Proj(name, W, x, y, N, K, ldw, group))
+        if self.weights == "bf16":
+            ldw = inputs.padded_ldw(K)
+            W = inputs.weight(N, K, ldw, seed=seed, index=index, device=self.device)
+            self.projs.append(Proj(name, W, x, y, N, K, ldw, group))
+        elif self.weights == "fp8":
+            W, S = inputs.fp8_weight(N, K, seed=seed, index=index, device=self.device)
+            self.projs.append(Proj(name, W, x, y, N, K, W.shape[1], group, S, 0))
+        else:
+            W, S = inputs.w4_weight_device(N, K, seed=seed, index=index, device=self.device)
+            self.projs.append(Proj(name, W, x, y, N, K, W.shape[1], group, S, S.shape[1]))
 
     def plan(self, rms_eps: float | None = None, streamk: bool = False) -> binding.Plan:
         """The step as one plan. With rms_eps, the projections that read a
@@ -99,7 +117,8 @@ class DecodeStep:
                 return None
             return rms_eps if (p.name.endswith(("q_proj", "k_proj", "v_proj", "gate_proj", "up_proj"))
                                or p.name == "lm_head") else None
-        return binding.Plan([(p.W, p.x, p.y, p.N, p.K, p.ldw, 1, p.group, eps_of(p), streamk)
+        kind = WEIGHT_KINDS[self.weights]
+        return binding.Plan([(p.W, p.x, p.y, p.N, p.K, p.ldw, 1, p.group, eps_of(p), streamk, kind, p.S, p.lds)
                              for p in self.projs], keepalive=self)
 
     def outputs(self):
@@ -114,20 +133,29 @@ class DecodeStep:
         for p in self.projs:
             yield p.name, p.W, p.x, p.y, p.K
 
+    def _wbytes(self, p) -> int:
+        """Weight bytes of one projection: BF16 2*N*K; INT4 N*K/2 codes plus
+        2*N*K/128 scale bytes; FP8 N*K codes plus 4*N scale bytes."""
+        if self.weights == "bf16":
+            return 2 * p.N * p.K
+        if self.weights == "fp8":
+            return p.N * p.K + 4 * p.N
+        return p.N * p.K // 2 + 2 * p.N * (p.K // inputs.W4_GROUP)
+
     def algorithmic_bytes(self) -> int:
-        """Sum of N*K*2 + K*2 + N*4 over the projections; a fused launch moves
-        its x once, so each launch group counts x once."""
+        """Sum of weight bytes + K*2 + N*4 over the projections; a fused launch
+        moves its x once, so each launch group counts x once."""
         total = 0
         seen_groups = set()
         for p in self.projs:
-            total += 2 * p.N * p.K + 4 * p.N
+            total += self._wbytes(p) + 4 * p.N
             if p.group == 0 or p.group not in seen_groups:
                 total += 2 * p.K
                 seen_groups.add(p.group)
         return total
 
     def weight_bytes(self) -> int:
-        return sum(2 * p.N * p.K for p in self.projs)
+        return sum(self._wbytes(p) for p in self.projs)
 
 
 def step_bytes_formula(spec: dict) -> int:
