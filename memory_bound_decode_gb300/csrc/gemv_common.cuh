@@ -49,6 +49,16 @@ __device__ __forceinline__ void pdl_wait_prerequisites() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Split cluster barrier: every CTA of a cluster along K arrives at kernel
+// entry and waits just before its first store into another CTA's shared
+// memory, so that no CTA writes there before the owner has started.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -60,14 +70,21 @@ __device__ __forceinline__ uint32_t cluster_rank() {
     return r;
 }
 
-// Load a float from the same shared-memory offset in CTA `rank` of this cluster.
-__device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank) {
-    uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
-    uint32_t r;
-    float v;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
-    return v;
+// Generic address of the same shared-memory location in CTA `rank` of this
+// cluster. Stores through it are ordinary stores; the cluster barrier that
+// follows them (release / acquire) makes them visible to that CTA.
+__device__ __forceinline__ float* dsmem_at(float* local, uint32_t rank) {
+    uint64_t r;
+    asm("mapa.u64 %0, %1, %2;" : "=l"(r) : "l"(local), "r"(rank));
+    return reinterpret_cast<float*>(r);
+}
+
+// i / B for 0 <= i < 2^16 and 2 <= B <= 16 with magic = 0xFFFFFFFF / B + 1
+// (ceil(2^32 / B), or 2^32 / B exactly when B is a power of two): the
+// rounding up adds less than i * B / 2^32 < 1/B to i / B, too little to
+// reach the next integer.
+__device__ __forceinline__ int div_by_batch(int i, int B, uint32_t magic) {
+    return B == 1 ? i : static_cast<int>(__umulhi(static_cast<uint32_t>(i), magic));
 }
 
 // 16-byte asynchronous global->shared copy of `nbytes` (2..16) bytes; the rest
@@ -119,6 +136,45 @@ __device__ __forceinline__ void stage_x(uint16_t* xs, int xstride, const uint16_
                 w[q] = lo | (hi << 16);
             }
             *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    cp_async_commit();
+}
+
+// stage_x for B >= 2 rows without a division per piece: pieces (b, i),
+// numbered b * nv + i, are taken with stride kThreads as in stage_x, but the
+// position advances by (db, di) per step with one carry, so every thread of
+// the CTA stays busy whatever nv is. Same copies, same zero fill, one copy
+// group.
+__device__ __forceinline__ void stage_x_rows(uint16_t* xs, int xstride, const uint16_t* __restrict__ x,
+                                             int B, int64_t K, int64_t c0, int nv) {
+    if (nv > 0) {
+        int b = static_cast<int>(threadIdx.x) / nv;
+        int i = static_cast<int>(threadIdx.x) - b * nv;
+        const int db = kThreads / nv;
+        const int di = kThreads - db * nv;
+#pragma unroll 1
+        for (; b < B; i += di, b += db) {
+            if (i >= nv) {
+                i -= nv;
+                ++b;
+                if (b >= B) break;
+            }
+            const int64_t col = c0 + 8 * static_cast<int64_t>(i);
+            const uint16_t* s = x + static_cast<int64_t>(b) * K + col;
+            uint16_t* d = xs + static_cast<int64_t>(b) * xstride + 8 * i;
+            if ((reinterpret_cast<uintptr_t>(s) & 15u) == 0) {
+                cp_async16(d, s, (col + 8 <= K) ? 16 : static_cast<int>(K - col) * 2);
+            } else {
+                uint32_t w[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t lo = (col + 2 * q < K) ? __ldg(s + 2 * q) : 0u;
+                    uint32_t hi = (col + 2 * q + 1 < K) ? __ldg(s + 2 * q + 1) : 0u;
+                    w[q] = lo | (hi << 16);
+                }
+                *reinterpret_cast<uint4*>(d) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
         }
     }
     cp_async_commit();
@@ -201,48 +257,81 @@ __device__ __forceinline__ int red_index(int kq, int rows_per_cta, int row_local
 // rank order, scale by the RMSNorm factor of the batch row when asked (its sum
 // of squares combined over the cluster in rank order as well), and store each
 // output once.
+//
+// Cluster combine (S > 1), a reduce-scatter through distributed shared memory:
+// rank r owns outputs [r * chunk, (r + 1) * chunk). Every rank pushes its
+// partial of each output into slot [rank][output - owner * chunk] of the
+// owner's cpart (and its sums of squares into every rank's slot [rank][b] of
+// the RMSNorm exchange area), one cluster barrier publishes the stores, and
+// each owner adds its S slots in rank order. No CTA reads another CTA's shared
+// memory, so none has to wait for its peers before it exits. cpart holds
+// S * chunk <= rows_per_cta * B + kMaxSplits floats. Kernels with S > 1 call
+// cluster_arrive_relaxed() at entry.
 __device__ __forceinline__ void combine_and_store(const float* red, float* cpart, float* misc, int rows_per_cta,
                                                   int B, int kw, int S, int split, int64_t n_base, int64_t N,
                                                   float* __restrict__ y, bool norm, int64_t K, float eps,
                                                   const WriteCount& wc) {
     float* xsq = misc + kWarps * kMaxBatch;
     float* rsc = xsq + kMaxBatch;
-    __syncthreads();
-    if (norm && S == 1) {
-        if (threadIdx.x < B) rsc[threadIdx.x] = 1.0f / sqrtf(xsq[threadIdx.x] / static_cast<float>(K) + eps);
-        __syncthreads();
-    }
+    float* xrecv = rsc + kMaxBatch;   // [kMaxSplits][kMaxBatch]
+    const uint32_t magic = B > 1 ? 0xFFFFFFFFu / static_cast<uint32_t>(B) + 1u : 0u;
     const int nout = rows_per_cta * B;   // index i = row_local * B + b
-    for (int i = threadIdx.x; i < nout; i += kThreads) {
-        const int rl = i / B, b = i - (i / B) * B;
-        float s = red[red_index(0, rows_per_cta, rl, B, b)];
-        for (int q = 1; q < kw; ++q) s += red[red_index(q, rows_per_cta, rl, B, b)];
-        if (S == 1) {
-            const int64_t n = n_base + rl;
-            if (n < N) store_y(y + static_cast<int64_t>(b) * N + n, norm ? s * rsc[b] : s, wc);
-        } else {
-            cpart[i] = s;
-        }
-    }
-    if (S > 1) {
-        cluster_sync_all();   // every CTA of the cluster has its partials in shared memory
+    __syncthreads();
+    if (S == 1) {
         if (norm) {
-            if (threadIdx.x < B) {
-                float t = ld_dsmem(&xsq[threadIdx.x], 0);
-                for (int q = 1; q < S; ++q) t += ld_dsmem(&xsq[threadIdx.x], static_cast<uint32_t>(q));
-                rsc[threadIdx.x] = 1.0f / sqrtf(t / static_cast<float>(K) + eps);
-            }
+            if (threadIdx.x < B) rsc[threadIdx.x] = 1.0f / sqrtf(xsq[threadIdx.x] / static_cast<float>(K) + eps);
             __syncthreads();
         }
         for (int i = threadIdx.x; i < nout; i += kThreads) {
-            if (i % S != split) continue;   // outputs are shared out over the ranks
-            float s = ld_dsmem(&cpart[i], 0);
-            for (int q = 1; q < S; ++q) s += ld_dsmem(&cpart[i], static_cast<uint32_t>(q));
-            const int rl = i / B, b = i - (i / B) * B;
+            const int rl = div_by_batch(i, B, magic), b = i - rl * B;
+            float s = red[red_index(0, rows_per_cta, rl, B, b)];
+#pragma unroll 1
+            for (int q = 1; q < kw; ++q) s += red[red_index(q, rows_per_cta, rl, B, b)];
             const int64_t n = n_base + rl;
             if (n < N) store_y(y + static_cast<int64_t>(b) * N + n, norm ? s * rsc[b] : s, wc);
         }
-        cluster_sync_all();   // no CTA leaves while another still reads its shared memory
+        return;
+    }
+
+    const int chunk = (nout + S - 1) / S;
+    cluster_wait();   // pairs with the arrival at kernel entry: every owner has started
+#pragma unroll 1
+    for (int owner = 0; owner < S; ++owner) {
+        float* dst = dsmem_at(cpart + split * chunk, static_cast<uint32_t>(owner));
+        const int i0 = owner * chunk;
+        const int i1 = (i0 + chunk < nout) ? i0 + chunk : nout;
+        for (int i = i0 + static_cast<int>(threadIdx.x); i < i1; i += kThreads) {
+            const int rl = div_by_batch(i, B, magic), b = i - rl * B;
+            float s = red[red_index(0, rows_per_cta, rl, B, b)];
+#pragma unroll 1
+            for (int q = 1; q < kw; ++q) s += red[red_index(q, rows_per_cta, rl, B, b)];
+            dst[i - i0] = s;
+        }
+    }
+    if (norm && threadIdx.x < B) {
+#pragma unroll 1
+        for (int q = 0; q < S; ++q)
+            dsmem_at(xrecv + split * kMaxBatch + threadIdx.x, static_cast<uint32_t>(q))[0] = xsq[threadIdx.x];
+    }
+    cluster_sync_all();   // every rank's partials are in their owners' shared memory
+    if (norm) {
+        if (threadIdx.x < B) {
+            float t = xrecv[threadIdx.x];
+            for (int q = 1; q < S; ++q) t += xrecv[q * kMaxBatch + threadIdx.x];
+            rsc[threadIdx.x] = 1.0f / sqrtf(t / static_cast<float>(K) + eps);
+        }
+        __syncthreads();
+    }
+    const int i0 = split * chunk;
+    const int i1 = (i0 + chunk < nout) ? i0 + chunk : nout;
+    for (int i = i0 + static_cast<int>(threadIdx.x); i < i1; i += kThreads) {
+        const int j = i - i0;
+        float s = cpart[j];
+#pragma unroll 1
+        for (int q = 1; q < S; ++q) s += cpart[q * chunk + j];
+        const int rl = div_by_batch(i, B, magic), b = i - rl * B;
+        const int64_t n = n_base + rl;
+        if (n < N) store_y(y + static_cast<int64_t>(b) * N + n, norm ? s * rsc[b] : s, wc);
     }
 }
 

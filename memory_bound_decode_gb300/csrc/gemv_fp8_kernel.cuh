@@ -77,6 +77,7 @@ gemv_fp8_kernel(const __grid_constant__ Params p) {
     pdl_launch_dependents();
 
     const int S = p.splits;
+    if (S > 1) cluster_arrive_relaxed();   // see combine_and_store
     const int64_t tile = blockIdx.x / S;
     const int split = (S > 1) ? static_cast<int>(cluster_rank()) : 0;
     const SegView sg = segment_of(p, tile);
@@ -108,7 +109,7 @@ gemv_fp8_kernel(const __grid_constant__ Params p) {
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem_raw);
     float* red = reinterpret_cast<float*>(smem_raw + static_cast<size_t>(p.nbuf) * xbuf * 2);
     float* cpart = red + rows_per_cta * (B + 1) * kw;
-    float* misc = cpart + rows_per_cta * B;
+    float* misc = cpart + rows_per_cta * B + kMaxSplits;   // cpart: cluster slots, see combine_and_store
     const bool norm = (p.flags & kFlagRmsNorm) != 0;
 
     // Byte offset, within one staged x buffer, of the 8 columns that words

@@ -58,8 +58,9 @@ struct Params {
 constexpr int32_t kFlagRmsNorm = 1;
 
 // Shared floats after the partial sums: per-warp sums of squares of x
-// [kWarps][kMaxBatch], the CTA's sums [kMaxBatch] and the row scales [kMaxBatch].
-constexpr int kMiscFloats = kWarps * kMaxBatch + 2 * kMaxBatch;
+// [kWarps][kMaxBatch], the CTA's sums [kMaxBatch], the row scales [kMaxBatch]
+// and, for a cluster along K, every rank's sums [kMaxSplits][kMaxBatch].
+constexpr int kMiscFloats = kWarps * kMaxBatch + 2 * kMaxBatch + kMaxSplits * kMaxBatch;
 
 // Kernel families.
 enum Path : int32_t {

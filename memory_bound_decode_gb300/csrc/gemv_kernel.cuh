@@ -109,8 +109,10 @@ __device__ __forceinline__ FmaRange fma_range(const Chunk& c, int kw, int kq) {
 // CHUNKED: the CTA's K-range is staged in several double-buffered chunks;
 // otherwise it is one chunk and the chunk loop runs once (a separate, leaner
 // instance, since the common large projections need no chunking).
+// Launch bounds: the batch-16 chunked instance is held to 2 CTAs per SM (128
+// registers); the others are left to the compiler.
 template <int B, int RPW, int UJ, bool CHUNKED>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, (B == 16 && CHUNKED) ? 2 : 0)
 gemv_bf16_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
 
@@ -119,6 +121,7 @@ gemv_bf16_kernel(const __grid_constant__ Params p) {
     pdl_launch_dependents();
 
     const int S = p.splits;
+    if (S > 1) cluster_arrive_relaxed();   // see combine_and_store
     const int64_t tile = blockIdx.x / S;
     const int split = (S > 1) ? static_cast<int>(cluster_rank()) : 0;
     const SegView sg = segment_of(p, tile);
@@ -144,7 +147,7 @@ gemv_bf16_kernel(const __grid_constant__ Params p) {
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem_raw);
     float* red = reinterpret_cast<float*>(smem_raw + static_cast<size_t>(p.nbuf) * xbuf * 2);
     float* cpart = red + rows_per_cta * (B + 1) * kw;
-    float* misc = cpart + rows_per_cta * B;
+    float* misc = cpart + rows_per_cta * B + kMaxSplits;   // cpart: cluster slots, see combine_and_store
     const bool norm = (p.flags & kFlagRmsNorm) != 0;
 
     const int64_t K = p.K;

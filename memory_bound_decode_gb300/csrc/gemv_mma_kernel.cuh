@@ -144,6 +144,7 @@ gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
     pdl_launch_dependents();
 
     const int S = p.splits;
+    if (S > 1) cluster_arrive_relaxed();   // see combine_and_store
     const int64_t tile = blockIdx.x / S;
     const int split = (S > 1) ? static_cast<int>(cluster_rank()) : 0;
     const SegView sg = segment_of(p, tile);
@@ -169,7 +170,7 @@ gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem_raw);
     float* red = reinterpret_cast<float*>(smem_raw + static_cast<size_t>(p.nbuf) * xbuf * 2);
     float* cpart = red + rows_per_cta * (B + 1) * kw;
-    float* misc = cpart + rows_per_cta * B;
+    float* misc = cpart + rows_per_cta * B + kMaxSplits;   // cpart: cluster slots, see combine_and_store
     const bool norm = (p.flags & kFlagRmsNorm) != 0;
 
     const int64_t K = p.K;
@@ -192,7 +193,7 @@ gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
     const uint16_t* p1 = w1row + ch.c0 + 8 * static_cast<int64_t>(v);
     mma_issue<UJ, true>(w0, w1, ok, p0, p1, v, rg.my_blocks, ch);
     pdl_wait_prerequisites();
-    stage_x(xs, xstride, p.x, B, K, ch.c0, ch.nv);
+    stage_x_rows(xs, xstride, p.x, B, K, ch.c0, ch.nv);
 
 #pragma unroll 1
     for (int c = 0;; ++c) {
@@ -202,7 +203,7 @@ gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
         Chunk nch{};
         if (more) {
             nch = chunk_at(next_c0, k1, p.kchunk, K);
-            stage_x(xs + ((c + 1) & 1) * xbuf, xstride, p.x, B, K, nch.c0, nch.nv);
+            stage_x_rows(xs + ((c + 1) & 1) * xbuf, xstride, p.x, B, K, nch.c0, nch.nv);
             cp_async_wait<1>();
         } else {
             cp_async_wait<0>();

@@ -73,14 +73,17 @@ __device__ __forceinline__ W4Range w4_range(int ngroups, int kw, int kq) {
     return r;
 }
 
+// Launch bounds: 3 CTAs per SM for the standard one-block instance, 2 for
+// the others (the occupancy the planner assumes for each).
 template <int NB, int UJ, bool CHUNKED>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, NB == 2 ? 2 : 0)
 gemv_w4_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
 
     pdl_launch_dependents();
 
     const int S = p.splits;
+    if (S > 1) cluster_arrive_relaxed();   // see combine_and_store
     const int64_t tile = blockIdx.x / S;
     const int split = (S > 1) ? static_cast<int>(cluster_rank()) : 0;
     const SegView sg = segment_of(p, tile);
@@ -113,7 +116,7 @@ gemv_w4_kernel(const __grid_constant__ Params p) {
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem_raw);
     float* red = reinterpret_cast<float*>(smem_raw + static_cast<size_t>(p.nbuf) * xbuf * 2);
     float* cpart = red + rows_per_cta * (B + 1) * kw;
-    float* misc = cpart + rows_per_cta * B;
+    float* misc = cpart + rows_per_cta * B + kMaxSplits;   // cpart: cluster slots, see combine_and_store
     const bool norm = (p.flags & kFlagRmsNorm) != 0;
 
     // Byte offset, within one staged x buffer, of the 8 columns that word m of

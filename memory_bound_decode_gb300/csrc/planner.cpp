@@ -185,7 +185,7 @@ int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight
     const int64_t grid = row_tiles * splits;
     if (grid > 0x7fffffffLL) return GEMV_ERR_UNSUPPORTED;
     const int64_t smem = nbuf * static_cast<int64_t>(B) * xstride * 2 +
-                         rows_per_cta * (B + 1) * kw * 4 + rows_per_cta * B * 4 + kMiscFloats * 4;
+                         rows_per_cta * (B + 1) * kw * 4 + (rows_per_cta * B + kMaxSplits) * 4 + kMiscFloats * 4;
     if (smem > kMaxDynSmem) return GEMV_ERR_UNSUPPORTED;
 
     out->rows_per_cta = rows_per_cta;
