@@ -132,9 +132,10 @@ int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight
         while (kw < kWarps && warps_for(kw, splits) < target_warps / 2 && room(kw, splits)) kw *= 2;
         if (B >= 8 && splits == 1 && room(kw, splits)) splits = 2;
     } else if (path == kPathW4 && B == 1) {
-        // INT4, one activation row: two warps along K first, then CTAs along K
-        // (measured best on the decode shapes).
-        while (kw < 2 && warps_for(kw, splits) < target_warps && room(kw, splits)) kw *= 2;
+        // INT4, one activation row: up to four warps along K first (combined in
+        // shared memory), then CTAs along K (measured best on the decode shapes:
+        // o_proj and the QKV shape take no cluster at all, down_proj two CTAs).
+        while (kw < 4 && warps_for(kw, splits) < target_warps && room(kw, splits)) kw *= 2;
         while (splits < 4 && warps_for(kw, splits) < target_warps && room(kw, splits)) splits *= 2;
         while (kw < kWarps && warps_for(kw, splits) < target_warps && room(kw, splits)) kw *= 2;
         while (splits < kMaxSplits && warps_for(kw, splits) < target_warps && room(kw, splits)) splits *= 2;
