@@ -258,7 +258,8 @@ void gemv_plan_destroy(gemv_plan *plan);
 typedef struct {
     int64_t rows_per_cta;    /* output rows one CTA produces                      */
     int64_t row_tiles;       /* ceil(N / rows_per_cta), per fused launch summed   */
-    int64_t grid;            /* CTAs launched = row_tiles * splits                */
+    int64_t grid;            /* CTAs launched = row_tiles * splits (rounded up to
+                                whole clusters of mcast CTAs when mcast > 1)      */
     int64_t kslice;          /* columns per K-split (all but the last)            */
     int64_t kchunk;          /* columns of x staged in shared memory at a time    */
     int32_t warps_per_cta;
@@ -280,6 +281,13 @@ typedef struct {
     int32_t ctas_per_sm;     /* resident CTAs per SM the one-wave grid assumes    */
     int32_t dp_rounds;       /* rounds of whole rows, one per warp of the grid,
                                 taken before the split part                       */
+    int32_t mcast;           /* path 0, batch 1, no K split, x in one chunk: CTAs
+                                of a cluster along the rows that share one
+                                multicast copy of x (CTA rank 0 copies x once
+                                into all of their shared memory with the
+                                Tensor Memory Accelerator); 1: each CTA copies
+                                its own. A call whose x is not 16-byte aligned
+                                falls back to 1                                   */
 } gemv_launch_info;
 
 int gemv_query_launch(int64_t N, int64_t K, int B, int sm_count,
@@ -294,6 +302,18 @@ int gemv_query_launch_ex(int64_t N, int64_t K, int B, int sm_count, int flags,
 /* Free the stream-K workspace the library holds for the current device. No
  * stream-K call on that device may be in flight. Returns GEMV_OK. */
 int gemv_workspace_release(void);
+
+/*
+ * Status bits the kernels recorded on the current device since the last reset:
+ * GEMV_STATUS_WAIT_TIMEOUT means a kernel gave up waiting for a copy of x into
+ * shared memory (an mbarrier wait has an iteration limit instead of spinning
+ * forever); the outputs of that launch are then undefined. Writes the bits to
+ * *bits and clears them when reset != 0. Synchronous with respect to the
+ * device's work (like cudaMemcpyFromSymbol). Returns GEMV_OK, GEMV_ERR_INVALID
+ * for a NULL pointer, or GEMV_ERR_CUDA.
+ */
+#define GEMV_STATUS_WAIT_TIMEOUT 1u
+int gemv_device_status(unsigned int *bits, int reset);
 
 /*
  * Test support, not part of the method. In a library built with

@@ -40,7 +40,8 @@ EXPORTED = [
     "gemv_bf16", "gemv_bf16_ex", "gemv_bf16_host_io", "gemv_bf16_multi", "gemv_bf16_multi_ex",
     "gemv_plan_create", "gemv_plan_capture",
     "gemv_plan_launch", "gemv_plan_num_launches", "gemv_plan_destroy",
-    "gemv_query_launch", "gemv_query_launch_ex", "gemv_workspace_release", "gemv_bf16_streamk_noalloc",
+    "gemv_query_launch", "gemv_query_launch_ex", "gemv_workspace_release", "gemv_device_status",
+    "gemv_bf16_streamk_noalloc",
     "gemv_debug_write_count",
     "gemv_w4_bf16", "gemv_w4_query_launch", "gemv_fp8_bf16", "gemv_fp8_query_launch",
     "gemv_probe_stream_read", "gemv_probe_sink_words",
@@ -72,7 +73,7 @@ class gemv_launch_info(ctypes.Structure):
                 ("unroll", ctypes.c_int32), ("smem_bytes", ctypes.c_int32), ("path", ctypes.c_int32),
                 ("xstride", ctypes.c_int32), ("nbuf", ctypes.c_int32),
                 ("units", i64), ("warps", i64), ("chunks", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
-                ("dp_rounds", ctypes.c_int32)]
+                ("dp_rounds", ctypes.c_int32), ("mcast", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -143,6 +144,7 @@ def _load(path: str) -> ctypes.CDLL:
     L.gemv_query_launch_ex.argtypes = [i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.POINTER(gemv_launch_info)]
     L.gemv_workspace_release.argtypes = []
+    L.gemv_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]
     L.gemv_debug_write_count.argtypes = [vp, vp, i64]
     L.gemv_bf16_streamk_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.POINTER(gemv_options), vp]
     L.gemv_w4_bf16.argtypes = [vp, vp, vp, vp, i64, i64, ctypes.c_int, i64, i64,
@@ -274,6 +276,17 @@ def gemv_debug_write_count(counts, y_base, n: int, check: bool = True) -> int:
 
 def gemv_workspace_release() -> int:
     return _check(lib().gemv_workspace_release(), "gemv_workspace_release")
+
+
+GEMV_STATUS_WAIT_TIMEOUT = 1
+
+
+def gemv_device_status(reset: bool = True) -> int:
+    """Status bits the kernels recorded on the current device (GEMV_STATUS_*),
+    cleared when ``reset``."""
+    bits = ctypes.c_uint(0)
+    _check(lib().gemv_device_status(ctypes.byref(bits), 1 if reset else 0), "gemv_device_status")
+    return bits.value
 
 
 def gemv_w4_bf16(Wq, S, x, y, N: int, K: int, B: int, ldq: int, lds: int, rms_eps=None,

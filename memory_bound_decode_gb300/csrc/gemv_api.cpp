@@ -237,7 +237,12 @@ int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B
         tiles += (segs[i].N + l.rows_per_cta - 1) / l.rows_per_cta;
     }
     l.row_tiles = tiles;
-    l.grid = tiles * l.splits;
+    {   // EXPERIMENT: multicast cluster size override
+        const char* v = std::getenv("GEMV_MCAST");
+        if (v && l.mcast > 1) l.mcast = std::atoi(v);
+    }
+    if (l.mcast > 1 && !aligned(x, 16)) l.mcast = 1;   // the bulk copy reads x from a 16-byte boundary
+    l.grid = l.mcast > 1 ? (tiles + l.mcast - 1) / l.mcast * l.mcast : tiles * l.splits;
     if (l.grid > 0x7fffffffLL) return GEMV_ERR_UNSUPPORTED;
     p.x = static_cast<const uint16_t*>(x);
     p.K = K;
@@ -251,6 +256,7 @@ int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B
     p.nbuf = l.nbuf;
     p.flags = (flags & GEMV_FLAG_RMSNORM) ? gemv::kFlagRmsNorm : 0;
     p.rms_eps = eps;
+    p.mcast = l.mcast > 1 ? l.mcast : 1;
     p.wc = g_write_count;
     out->p = p;
     out->l = l;
@@ -313,6 +319,7 @@ int prepare_quant(int kind, const QSeg* segs, int nsegs, const void* x, int64_t 
     p.nbuf = l.nbuf;
     p.flags = (flags & GEMV_FLAG_RMSNORM) ? gemv::kFlagRmsNorm : 0;
     p.rms_eps = eps;
+    p.mcast = 1;
     p.wc = g_write_count;
     out->p = p;
     out->l = l;
@@ -390,6 +397,7 @@ void fill_info(const Launch& l, gemv_launch_info* out) {
     out->path = l.path;
     out->xstride = l.xstride;
     out->nbuf = l.nbuf;
+    out->mcast = l.mcast;
 }
 
 }  // namespace
@@ -858,5 +866,13 @@ const char* gemv_status_string(int status) {
 }
 
 int gemv_last_cuda_error(void) { return g_last_cuda_error; }
+
+int gemv_device_status(unsigned int* bits, int reset) {
+    if (!bits) return GEMV_ERR_INVALID;
+    *bits = 0;
+    cudaError_t e = gemv::read_fma_status(bits, reset != 0);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return GEMV_OK;
+}
 
 }  // extern "C"

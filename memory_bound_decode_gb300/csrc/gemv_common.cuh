@@ -87,6 +87,72 @@ __device__ __forceinline__ int div_by_batch(int i, int B, uint32_t magic) {
     return B == 1 ? i : static_cast<int>(__umulhi(static_cast<uint32_t>(i), magic));
 }
 
+// ---- x multicast (batch 1, one K chunk): one bulk copy per cluster ------------
+//
+// Every CTA of a launch without a K split stages the same x. With a cluster of
+// C CTAs along the rows, the CTA of rank 0 copies x once from global memory
+// into the shared memory of all C CTAs (cp.async.bulk with .multicast::cluster,
+// the Tensor Memory Accelerator's 1-D copy); each CTA's mbarrier counts the
+// bytes that arrive in its own shared memory. The L2 then serves x once per
+// cluster instead of once per CTA, which matters at kernel start, when every
+// CTA asks for x at the same moment.
+
+// Device status word of this translation unit: bit 0 is set when an mbarrier
+// wait ran out of iterations (the copy it waited for never completed). Read and
+// cleared by the host through gemv_device_status.
+static __device__ unsigned int g_device_status;
+constexpr unsigned int kStatusWaitTimeout = 1u;
+constexpr int kMbarWaitLimit = 1 << 20;      // try_wait rounds before giving up
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// Make this CTA's mbarrier initialisation visible to the cluster (the copy
+// engine of another CTA's bulk copy completes transactions on it).
+__device__ __forceinline__ void fence_mbar_init_cluster() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Arrive on the barrier and add `bytes` to the transactions it waits for.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+// Wait for phase `parity` of the barrier to complete, for at most
+// kMbarWaitLimit rounds of try_wait (each returns when the phase completes or
+// after a time limit of the hardware's choosing). Returns false, and sets the
+// status bit, if the limit ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    const uint32_t a = smem_addr(bar);
+#pragma unroll 1
+    for (int it = 0; it < kMbarWaitLimit; ++it) {
+        uint32_t done;
+        asm volatile("{\n\t.reg .pred P1;\n\t"
+                     "mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2;\n\t"
+                     "selp.b32 %0, 1, 0, P1;\n\t}"
+                     : "=r"(done) : "r"(a), "r"(parity) : "memory");
+        if (done) return true;
+    }
+    atomicOr(&g_device_status, kStatusWaitTimeout);
+    return false;
+}
+
+// Copy `bytes` (a multiple of 16, 16-byte aligned source) from global memory
+// to the same shared-memory offset `dst` in every CTA of `mask`, completing
+// `bytes` transactions on the mbarrier at the same offset `bar` in each.
+__device__ __forceinline__ void bulk_copy_multicast(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                                    uint16_t mask) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+                 " [%0], [%1], %2, [%3], %4;"
+                 :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)), "h"(mask) : "memory");
+}
+
 // 16-byte asynchronous global->shared copy of `nbytes` (2..16) bytes; the rest
 // of the 16 bytes is zero-filled. Both addresses 16-byte aligned.
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src, int nbytes) {
@@ -364,8 +430,8 @@ __device__ __forceinline__ SegView segment_of(const Params& p, int64_t tile) {
     return s;
 }
 
-// Launch a kernel with the plan's grid, cluster (when K is split over CTAs)
-// and programmatic dependent launch.
+// Launch a kernel with the plan's grid, cluster (when K is split over CTAs,
+// or CTAs share a multicast copy of x) and programmatic dependent launch.
 template <typename KernelT>
 cudaError_t launch_kernel(KernelT kernel, const Params& p, const Launch& l, cudaStream_t s, bool pdl) {
     cudaLaunchConfig_t cfg = {};
@@ -375,9 +441,10 @@ cudaError_t launch_kernel(KernelT kernel, const Params& p, const Launch& l, cuda
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     int na = 0;
-    if (l.splits > 1) {
+    const int cluster = l.splits > 1 ? l.splits : (l.mcast > 1 ? l.mcast : 1);
+    if (cluster > 1) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = static_cast<unsigned>(l.splits);
+        attr[na].val.clusterDim.x = static_cast<unsigned>(cluster);
         attr[na].val.clusterDim.y = 1;
         attr[na].val.clusterDim.z = 1;
         ++na;

@@ -25,4 +25,11 @@ cudaError_t prepare_fma_all() {
     return prepare_fma_b9_16();
 }
 
+cudaError_t read_fma_status(unsigned int* bits, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(bits, g_device_status, sizeof(unsigned int));
+    if (e != cudaSuccess || !reset || *bits == 0) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_device_status, &zero, sizeof(unsigned int));
+}
+
 }  // namespace gemv

@@ -50,8 +50,21 @@ struct Params {
     int32_t nbuf;     // x buffers (2 when the K-range takes more than one chunk)
     int32_t flags;    // kFlagRmsNorm
     float rms_eps;    // epsilon of the RMSNorm prologue
+    int32_t mcast;    // CUDA-core kernel, batch 1, one K chunk, no K split: CTAs of a cluster along
+                      // the rows that share one multicast copy of x (1: every CTA stages its own)
     WriteCount wc;
 };
+
+// Bytes at the start of the multicast instance's dynamic shared memory before
+// x: its mbarrier (16 to keep x 16-byte aligned). Planned for every CUDA-core
+// launch; the other instances leave them unused.
+constexpr int kFmaSmemHead = 16;
+// Multicast x for batch 1 when the launch has no K split and x is at least
+// this many 16-byte vectors, i.e. K >= 8,192 (measured: down_proj, x = 28 KB,
+// 18.25 -> 17.94 us with clusters of 2; with x = 8 KB the launches with and
+// without it were within noise, so they keep the plain grid).
+constexpr int kMcastCtas = 2;
+constexpr int kMcastMinVectors = 1024;
 
 // Scale each output row b by (mean_k x[b][k]^2 + rms_eps)^(-1/2) (RMSNorm
 // prologue; the norm's elementwise weight is folded into W).
@@ -117,6 +130,7 @@ struct Launch {
     int32_t path;
     int32_t xstride;
     int32_t nbuf;
+    int32_t mcast;     // CTAs sharing one multicast copy of x (cluster along the rows); 1: none
 };
 
 // Returns 0 and fills `out`, or a negative GEMV_ERR_* code.
@@ -186,6 +200,9 @@ cudaError_t launch_gemv(int B, const Params& p, const Launch& l, cudaStream_t s,
 cudaError_t launch_streamk(const SkParams& p, const SkLaunch& l, cudaStream_t s, bool pdl);
 cudaError_t prepare_streamk();
 cudaError_t prepare_kernels(int device);   // per-device function attributes
+// Status bits the CUDA-core kernels' translation unit recorded on the current
+// device (kStatusWaitTimeout...), cleared when `reset`.
+cudaError_t read_fma_status(unsigned int* bits, bool reset);
 cudaError_t launch_probe_read(const void* src, int64_t bytes, float* sink, int grid,
                               cudaStream_t s);
 

@@ -111,7 +111,11 @@ __device__ __forceinline__ FmaRange fma_range(const Chunk& c, int kw, int kq) {
 // instance, since the common large projections need no chunking).
 // Launch bounds: the batch-16 chunked instance is held to 2 CTAs per SM (128
 // registers); the others are left to the compiler.
-template <int B, int RPW, int UJ, bool CHUNKED>
+// MCAST: the batch-1 single-chunk instance that receives x by cluster
+// multicast (launched with a cluster along the rows, p.mcast CTAs). It is a
+// separate instance: the others carry none of its bulk-copy and mbarrier code
+// and launch without a cluster.
+template <int B, int RPW, int UJ, bool CHUNKED, bool MCAST = false>
 __global__ void __launch_bounds__(kThreads, (B == 16 && CHUNKED) ? 2 : 0)
 gemv_bf16_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -119,6 +123,18 @@ gemv_bf16_kernel(const __grid_constant__ Params p) {
     // Let the next grid on the stream start as SMs free up; it only reads W
     // before it waits on this grid.
     pdl_launch_dependents();
+
+    // x multicast (batch 1, one chunk, no K split): initialise this CTA's
+    // mbarrier and announce it to the cluster before anything else.
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(smem_raw);
+    constexpr bool mcast = MCAST && B == 1 && !CHUNKED;
+    if constexpr (mcast) {
+        if (threadIdx.x == 0) {
+            mbar_init(mbar, 1);
+            fence_mbar_init_cluster();
+        }
+        cluster_arrive_relaxed();
+    }
 
     const int S = p.splits;
     if (S > 1) cluster_arrive_relaxed();   // see combine_and_store
@@ -144,8 +160,8 @@ gemv_bf16_kernel(const __grid_constant__ Params p) {
 
     const int xstride = p.xstride;
     const int xbuf = B * xstride;      // elements per x buffer
-    uint16_t* xs = reinterpret_cast<uint16_t*>(smem_raw);
-    float* red = reinterpret_cast<float*>(smem_raw + static_cast<size_t>(p.nbuf) * xbuf * 2);
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem_raw + (mcast ? kFmaSmemHead : 0));
+    float* red = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(xs) + static_cast<size_t>(p.nbuf) * xbuf * 2);
     float* cpart = red + rows_per_cta * (B + 1) * kw;
     float* misc = cpart + rows_per_cta * B + kMaxSplits;   // cpart: cluster slots, see combine_and_store
     const bool norm = (p.flags & kFlagRmsNorm) != 0;
@@ -173,7 +189,36 @@ gemv_bf16_kernel(const __grid_constant__ Params p) {
     for (int r = 0; r < RPW; ++r) wp[r] = wrow[r] + ch.c0 + 8 * static_cast<int64_t>(v0);
     issue_batch<RPW, UJ, true>(wv, ok, wp, v0, rg.my_steps, ch.nv, ch.nfull, ch.tail_m);
     pdl_wait_prerequisites();
-    stage_x(xs, xstride, p.x, B, K, ch.c0, ch.nv);
+    if constexpr (mcast) {
+        // Every CTA of the cluster has initialised its mbarrier; rank 0 copies
+        // the whole vectors of x into all of them (pieces of at most 32 KB);
+        // each CTA writes the partial vector at column K itself (zero-filled).
+        cluster_wait();
+        const uint32_t bytes = 16u * static_cast<uint32_t>(ch.nfull);
+        if (threadIdx.x == 0) mbar_arrive_expect_tx(mbar, bytes);
+        if (threadIdx.x == 0 && cluster_rank() == 0) {
+            const uint16_t mask = static_cast<uint16_t>((1u << p.mcast) - 1u);
+            for (uint32_t off = 0; off < bytes; off += 32768u) {
+                const uint32_t n = bytes - off < 32768u ? bytes - off : 32768u;
+                bulk_copy_multicast(reinterpret_cast<unsigned char*>(xs) + off,
+                                    reinterpret_cast<const unsigned char*>(p.x) + off, n, mbar, mask);
+            }
+        }
+        if (ch.tail_m != 0 && threadIdx.x == 32) {
+            const int64_t col = 8 * static_cast<int64_t>(ch.nfull);
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t lo = (col + 2 * q < K) ? __ldg(p.x + col + 2 * q) : 0u;
+                const uint32_t hi = (col + 2 * q + 1 < K) ? __ldg(p.x + col + 2 * q + 1) : 0u;
+                w[q] = lo | (hi << 16);
+            }
+            *reinterpret_cast<uint4*>(xs + col) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        mbar_wait_bounded(mbar, 0);
+    } else {
+        stage_x(xs, xstride, p.x, B, K, ch.c0, ch.nv);
+    }
 
 #pragma unroll 1
     for (int c = 0;; ++c) {
@@ -252,6 +297,10 @@ template <int B>
 cudaError_t launch_fma(const Params& p, const Launch& l, cudaStream_t s, bool pdl) {
     constexpr Variant v = fma_variant(B);
     if (l.nbuf > 1) return launch_kernel(gemv_bf16_kernel<B, v.rows_per_warp, v.unroll, true>, p, l, s, pdl);
+    if constexpr (B == 1) {
+        if (p.mcast > 1)
+            return launch_kernel(gemv_bf16_kernel<B, v.rows_per_warp, v.unroll, false, true>, p, l, s, pdl);
+    }
     return launch_kernel(gemv_bf16_kernel<B, v.rows_per_warp, v.unroll, false>, p, l, s, pdl);
 }
 
@@ -261,6 +310,11 @@ cudaError_t prepare_fma() {
     cudaError_t e = cudaFuncSetAttribute(gemv_bf16_kernel<B, v.rows_per_warp, v.unroll, true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
     if (e != cudaSuccess) return e;
+    if constexpr (B == 1) {
+        e = cudaFuncSetAttribute(gemv_bf16_kernel<B, v.rows_per_warp, v.unroll, false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+        if (e != cudaSuccess) return e;
+    }
     return cudaFuncSetAttribute(gemv_bf16_kernel<B, v.rows_per_warp, v.unroll, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
 }

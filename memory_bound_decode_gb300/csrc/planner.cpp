@@ -183,9 +183,15 @@ int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight
 
     const int64_t rows_per_cta = static_cast<int64_t>(kWarps / kw) * group_rows;
     const int64_t row_tiles = cdiv(N, rows_per_cta);
-    const int64_t grid = row_tiles * splits;
+    // Batch 1 on the CUDA cores without a K split and with x in one chunk: CTAs
+    // in clusters of kMcastCtas along the rows share one multicast copy of x
+    // (the grid is rounded up to whole clusters; the extra CTAs' rows are past
+    // N and their results dropped).
+    const int mcast = (path == kPathFma && B == 1 && splits == 1 && nbuf == 1 && K / 8 >= kMcastMinVectors &&
+                       row_tiles >= kMcastCtas) ? kMcastCtas : 1;
+    const int64_t grid = mcast > 1 ? round_up(row_tiles, mcast) : row_tiles * splits;
     if (grid > 0x7fffffffLL) return GEMV_ERR_UNSUPPORTED;
-    const int64_t smem = nbuf * static_cast<int64_t>(B) * xstride * 2 +
+    const int64_t smem = (path == kPathFma ? kFmaSmemHead : 0) + nbuf * static_cast<int64_t>(B) * xstride * 2 +
                          rows_per_cta * (B + 1) * kw * 4 + (rows_per_cta * B + kMaxSplits) * 4 + kMiscFloats * 4;
     if (smem > kMaxDynSmem) return GEMV_ERR_UNSUPPORTED;
 
@@ -202,6 +208,7 @@ int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight
     out->path = path;
     out->xstride = static_cast<int32_t>(xstride);
     out->nbuf = nbuf;
+    out->mcast = mcast;
     return GEMV_OK;
 }
 

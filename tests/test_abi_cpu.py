@@ -119,7 +119,15 @@ def test_plan_covers_the_problem(L, N, K, B):
     assert q["rows_per_warp"] == (1 if B == 1 else 16)
     assert q["rows_per_cta"] == (8 // q["warps_per_row"]) * q["rows_per_warp"]
     assert q["row_tiles"] * q["rows_per_cta"] >= N > (q["row_tiles"] - 1) * q["rows_per_cta"]
-    assert q["grid"] == q["row_tiles"] * q["splits"]
+    # x multicast: batch 1, no K split, one x chunk, x of at least 1,024 vectors; the
+    # grid is then whole clusters of mcast CTAs along the rows
+    if q["mcast"] > 1:
+        assert B == 1 and q["splits"] == 1 and q["nbuf"] == 1 and K // 8 >= 1024 and q["mcast"] == 2
+        assert q["grid"] == -(-q["row_tiles"] // q["mcast"]) * q["mcast"]
+    else:
+        assert q["mcast"] == 1
+        assert not (B == 1 and q["splits"] == 1 and q["nbuf"] == 1 and K // 8 >= 1024 and q["row_tiles"] >= 2)
+        assert q["grid"] == q["row_tiles"] * q["splits"]
     # K-slices are whole 256-column steps, cover K, and none is empty
     assert q["kslice"] % 256 == 0 and q["kchunk"] % 256 == 0
     assert q["splits"] * q["kslice"] >= K > (q["splits"] - 1) * q["kslice"]

@@ -1,0 +1,103 @@
+"""Batch 1 with x multicast: CTAs in clusters of 2 along the rows share one
+bulk copy of x (rank 0 copies it into both CTAs' shared memory, an
+mbarrier counts the bytes in each). The result must be the same bits as the
+per-CTA staging, which a call takes when x is not 16-byte aligned (same
+values, 2 bytes further on in memory), and agree with the CPU oracle; the
+device status must stay clear (no mbarrier wait ran out)."""
+import numpy as np
+import pytest
+import torch
+
+from memory_bound_decode_gb300 import binding, inputs
+from oracle import oracle
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def shifted(x):
+    """The same values at a 2-byte offset from a 16-byte boundary."""
+    B, K = x.shape
+    buf = torch.empty(B * K + 8, dtype=x.dtype, device=x.device)
+    out = buf[1:1 + B * K].view(B, K)
+    out.copy_(x)
+    assert out.data_ptr() % 16 == 2
+    return out
+
+
+def run(W, x, K, rms_eps=None, cuda_cores=False):
+    N, ldw = W.shape
+    buf, y = gu.guarded_y(1, N)
+    binding.gemv_bf16_ex(W, x, y, N, K, 1, ldw, rms_eps=rms_eps, cuda_cores=cuda_cores)
+    torch.cuda.synchronize()
+    gu.check_guards(buf)
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("N,K,mcast", [(4096, 14336, 2), (4097, 8199, 2), (1024, 14336, 2), (17, 16384, 2),
+                                       (4096, 4096, 1), (9, 40960, 1)])
+def test_multicast_matches_per_cta_staging_and_oracle(N, K, mcast):
+    q = binding.gemv_query_launch(N, K, 1, sms())
+    assert q["mcast"] == mcast, q
+    ldw = inputs.padded_ldw(K)
+    W = inputs.weight(N, K, ldw, seed=N + K, device=DEV)
+    x = inputs.activations(1, K, seed=K, device=DEV)
+    assert x.data_ptr() % 16 == 0
+    binding.gemv_device_status(reset=True)
+    y = run(W, x, K)
+    y_fallback = run(W, shifted(x), K)
+    assert np.array_equal(y.view(np.uint32), y_fallback.view(np.uint32))
+    y_ref, s = gu.reference(W, x, K)
+    gu.assert_parity(y, y_ref, s, f"multicast={q['mcast']} N={N} K={K}")
+    assert binding.gemv_device_status(reset=True) == 0
+
+
+def test_multicast_is_planned_for_long_x_only():
+    q = binding.gemv_query_launch(4096, 14336, 1, sms())          # down_proj: x of 28 KB
+    assert q["mcast"] == 2 and q["grid"] % 2 == 0, q
+    for N, K in [(4096, 4096), (1024, 4096), (6144, 4096), (28672, 4096), (128256, 4096)]:
+        assert binding.gemv_query_launch(N, K, 1, sms())["mcast"] == 1, (N, K)
+
+
+def test_multicast_with_rmsnorm_and_segments():
+    K, rows, eps = 14336, [4096, 1024, 1024, 7], 1e-5
+    Ws = [inputs.weight(n, K, seed=30 + i, device=DEV) for i, n in enumerate(rows)]
+    x = inputs.activations(1, K, seed=31, device=DEV)
+    for xx in (x, shifted(x)):
+        ys = [torch.full((1, n), float("nan"), device=DEV) for n in rows]
+        binding.gemv_bf16_multi_ex([(W, y, n, K) for W, y, n in zip(Ws, ys, rows)], xx, K, 1, rms_eps=eps)
+        torch.cuda.synchronize()
+        if xx is x:
+            first = [y.cpu().numpy() for y in ys]
+        else:
+            for a, y in zip(first, ys):
+                assert np.array_equal(a.view(np.uint32), y.cpu().numpy().view(np.uint32))
+    for W, a in zip(Ws, first):
+        y_ref, s, _ = oracle.gemv_rmsnorm(inputs.bits(W), inputs.bits(x), eps, K, threads=oracle.default_threads())
+        gu.assert_parity(a, y_ref, s, "segment with RMSNorm")
+    assert binding.gemv_device_status(reset=True) == 0
+
+
+def test_multicast_back_to_back_in_a_captured_graph():
+    # the decode-step use: the same calls replayed from a graph, x updated in place
+    N, K = 4096, 14336
+    ldw = inputs.padded_ldw(K)
+    W = inputs.weight(N, K, ldw, seed=5, device=DEV)
+    x = inputs.activations(1, K, seed=6, device=DEV)
+    y = torch.full((1, N), float("nan"), device=DEV)
+    plan = binding.Plan([(W, x, y, N, K, ldw, 1, 0)] * 3, keepalive=(W, x, y))
+    s = torch.cuda.Stream()
+    plan.capture(s)
+    for seed in (7, 8):
+        x.copy_(inputs.activations(1, K, seed=seed, device=DEV))
+        torch.cuda.synchronize()
+        plan.launch(s)
+        s.synchronize()
+        y_ref, sc = gu.reference(W, x, K)
+        gu.assert_parity(y.cpu().numpy(), y_ref, sc, f"graph replay, x seed {seed}")
+    assert binding.gemv_device_status(reset=True) == 0

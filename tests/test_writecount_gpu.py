@@ -38,7 +38,7 @@ def assert_once(counts: torch.Tensor, what: str):
     assert bad.size == 0, f"{what}: {bad.size} elements not written exactly once, e.g. {bad[:5]} -> {c[bad[:5]]}"
 
 
-@pytest.mark.parametrize("N,K,B", [(4096, 14336, 1), (33, 65537, 1), (1024, 4096, 1), (7, 129, 3),
+@pytest.mark.parametrize("N,K,B", [(4096, 14336, 1), (33, 65537, 1), (1024, 4096, 1), (4097, 4103, 1), (7, 129, 3),
                                    (4097, 4103, 8), (4096, 14336, 16), (1, 8191, 16), (300, 2056, 5)])
 def test_bf16_written_once(debug_lib, N, K, B):
     ldw = inputs.padded_ldw(K)
