@@ -237,10 +237,6 @@ int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B
         tiles += (segs[i].N + l.rows_per_cta - 1) / l.rows_per_cta;
     }
     l.row_tiles = tiles;
-    {   // EXPERIMENT: multicast cluster size override
-        const char* v = std::getenv("GEMV_MCAST");
-        if (v && l.mcast > 1) l.mcast = std::atoi(v);
-    }
     if (l.mcast > 1 && !aligned(x, 16)) l.mcast = 1;   // the bulk copy reads x from a 16-byte boundary
     l.grid = l.mcast > 1 ? (tiles + l.mcast - 1) / l.mcast * l.mcast : tiles * l.splits;
     if (l.grid > 0x7fffffffLL) return GEMV_ERR_UNSUPPORTED;

@@ -11,7 +11,7 @@ rows over threads (ctypes releases the GIL during the call, so the threads run
 in parallel; each thread owns a disjoint range of output rows, so threading does
 not change any result).
 
-The acceptance rule is the one the decode-GEMV problem is judged by: an FP32
+The acceptance rule for the decode GEMV: an FP32
 result may differ from the exact value only by summation rounding, so each
 element is accepted when |y_gpu - y_ref| <= rtol * sum_k |W[n,k] * x[b,k]|
 and y_gpu is finite ("Decode GEMV at half of HBM bandwidth", "A strong answer":
