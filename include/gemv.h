@@ -46,7 +46,9 @@
  * must not be written by a kernel that immediately precedes a call on the same
  * stream and triggers its dependents early; x and y are touched only after the
  * wait. Calls are thread-safe; the library keeps only per-device launch
- * settings, created on first use.
+ * settings, created on first use. Setting the environment variable GEMV_PDL=0
+ * before the first call turns programmatic dependent launch off (each kernel
+ * then starts only after the preceding one has finished), for comparison.
  */
 #ifndef GEMV_H
 #define GEMV_H
