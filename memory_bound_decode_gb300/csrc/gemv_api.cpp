@@ -94,6 +94,20 @@ constexpr size_t kMappedYMaxBytes = 256 * 1024;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// Whether p points into device memory of the current device: the x multicast
+// copies from there only (a pointer into mapped host or managed memory takes
+// the per-CTA staging instead).
+bool on_current_device(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    return a.type == cudaMemoryTypeDevice && a.device == dev;
+}
+
 int check_common(const void* x, int64_t K, int B) {
     if (!x) return GEMV_ERR_INVALID;
     if (K < 1 || K > 0x7fffffffLL || B < 1 || B > GEMV_MAX_BATCH) return GEMV_ERR_INVALID;
@@ -237,7 +251,8 @@ int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B
         tiles += (segs[i].N + l.rows_per_cta - 1) / l.rows_per_cta;
     }
     l.row_tiles = tiles;
-    if (l.mcast > 1 && !aligned(x, 16)) l.mcast = 1;   // the bulk copy reads x from a 16-byte boundary
+    // The bulk copy reads x from a 16-byte boundary, and only from this GPU's memory.
+    if (l.mcast > 1 && (!aligned(x, 16) || !on_current_device(x))) l.mcast = 1;
     l.grid = l.mcast > 1 ? (tiles + l.mcast - 1) / l.mcast * l.mcast : tiles * l.splits;
     if (l.grid > 0x7fffffffLL) return GEMV_ERR_UNSUPPORTED;
     p.x = static_cast<const uint16_t*>(x);

@@ -101,3 +101,26 @@ def test_multicast_back_to_back_in_a_captured_graph():
         y_ref, sc = gu.reference(W, x, K)
         gu.assert_parity(y.cpu().numpy(), y_ref, sc, f"graph replay, x seed {seed}")
     assert binding.gemv_device_status(reset=True) == 0
+
+
+def test_multicast_only_from_device_memory_and_under_capture():
+    # x in pinned host memory (mapped, reachable by the GPU): the per-CTA
+    # staging serves it, with the same bits as device-resident x
+    N, K = 4096, 14336
+    ldw = inputs.padded_ldw(K)
+    W = inputs.weight(N, K, ldw, seed=9, device=DEV)
+    x = inputs.activations(1, K, seed=10, device=DEV)
+    y_dev = run(W, x, K)
+    x_host = x.cpu().pin_memory()
+    y_host = run(W, x_host, K)
+    assert np.array_equal(y_dev.view(np.uint32), y_host.view(np.uint32))
+    # a direct call captured into a CUDA graph (the pointer query runs during capture)
+    y = torch.full((1, N), float("nan"), device=DEV)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        binding.gemv_bf16(W, x, y, N, K, 1, ldw, s.cuda_stream)
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), y_dev.view(np.uint32))
+    assert binding.gemv_device_status(reset=True) == 0
