@@ -263,3 +263,27 @@ def test_cuda_core_plans(L, B):
         assert q["smem_bytes"] <= 112 * 1024
     with pytest.raises(binding.GemvError):
         binding.gemv_query_launch_ex(8, 8, 1, GB300_SMS, binding.GEMV_FLAG_CUDA_CORES | binding.GEMV_FLAG_STREAMK)
+
+
+@pytest.mark.parametrize("N,K", [(4096, 14336), (4097, 8199), (17, 16384), (1024, 14336), (9, 40960),
+                                 (3000, 40960), (5, 8192), (2, 8200)])
+def test_multicast_copy_geometry(L, N, K):
+    # the multicast instance copies the whole vectors of x in one or more bulk
+    # copies of at most 32 KB (sizes multiples of 16 bytes) into the staged x
+    # area, and writes the partial vector at column K itself
+    q = binding.gemv_query_launch(N, K, 1, GB300_SMS)
+    if q["mcast"] == 1:
+        assert q["splits"] > 1 or q["nbuf"] > 1 or K // 8 < 1024 or q["row_tiles"] < 2
+        return
+    nfull = K // 8
+    nbytes = 16 * nfull
+    pieces = [min(32768, nbytes - off) for off in range(0, nbytes, 32768)]
+    assert sum(pieces) == nbytes and all(p % 16 == 0 and 0 < p <= 32768 for p in pieces)
+    tail = 1 if K % 8 else 0
+    assert 8 * (nfull + tail) <= q["xstride"]                  # x area holds every vector
+    assert q["smem_bytes"] >= 16 + 2 * q["xstride"]            # mbarrier head + x
+    assert q["grid"] % q["mcast"] == 0 and q["grid"] - q["row_tiles"] < q["mcast"]
+
+
+def test_device_status_rejects_null(L):
+    assert L.gemv_device_status(None, 0) == binding.GEMV_ERR_INVALID
