@@ -9,11 +9,22 @@ weights rotate over enough copies that together exceed the L2 cache, so every
 step streams W from HBM ("Decode GEMV at half of HBM bandwidth", "Common
 mistakes": a matrix that sits in L2 reports more than the HBM can deliver).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py [--gpus 1] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the CPU oracle, timed as the baseline arm
 
-Under torchrun each rank runs its own replica (weak scaling); the time is the
-maximum over ranks.
+Timing: the K timed steps are captured into CUDA graphs (up to --graph-steps
+calls each, cycling over the weight copies) and replayed between two CUDA
+events on one stream, after a short device-side delay kernel that lets the
+host enqueue the replays before the first event fires: the window holds the
+K steps' device time and nothing of the host's launch cost. A lone launch
+(GPU idle before it) is reported beside it as us_isolated.
+
+The default run also times the other two decode targets, the fused gate/up
+projection and the graph-captured decode step, under "targets".
+
+One GPU only: the path has no multi-GPU form, and a multi-rank launch
+(WORLD_SIZE > 1) exits with an error before any CUDA call. The reference arm
+(the CPU oracle) runs on rank 0 alone; other ranks exit without work.
 """
 from __future__ import annotations
 
@@ -55,6 +66,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-probe", action="store_true",
                     help="skip the read-only ceiling probe (keeps device memory small)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--graph-steps", type=int, default=256,
+                    help="most calls captured into one CUDA graph of the timed loop")
+    ap.add_argument("--no-targets", action="store_true",
+                    help="skip timing the gate/up and decode-step targets of the default run")
     return ap.parse_args(argv)
 
 
@@ -380,14 +395,8 @@ class StepWorkload:
 
 # ----------------------------------------------------------------------------- our arm
 
-def max_over_ranks(value: float, dist, device) -> float:
-    """The largest value any rank holds (all ranks get it)."""
-    if dist is None:
-        return value
-    import torch
-    t = torch.tensor([value], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+TARGETS = {"down_proj": 0.85, "gate_up": 0.85, "decode_step": 0.80}   # fraction of HBM peak
+DELAY_CYCLES = 1_000_000   # device-side delay before the first event (about 0.5 ms at 2 GHz)
 
 
 def read_ceiling_gbs(torch, binding, stream) -> float:
@@ -409,109 +418,247 @@ def read_ceiling_gbs(torch, binding, stream) -> float:
     return nbytes / best / 1e9
 
 
-def run_ours(args, rank: int, world: int, dist) -> dict | None:
-    import torch
-    from memory_bound_decode_gb300 import binding, build_lib
+def device_delay(torch) -> None:
+    """A short device-side delay on the current stream: what is enqueued after
+    it is in the stream before the GPU reaches it."""
+    sleep = getattr(torch.cuda, "_sleep", None)
+    if sleep is not None:
+        sleep(DELAY_CYCLES)
 
-    build_lib.build()
-    binding.lib()
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    stream = torch.cuda.current_stream()
-    props = torch.cuda.get_device_properties(device)
-    l2 = getattr(props, "L2_cache_size", 126 << 20)
 
-    kind, rows, K, B = describe(args.workload)
-    _, rms_eps = split_norm(args.workload)
-    base, streamk = split_sk(split_norm(args.workload)[0])
-    base, cuda_cores = split_cc(base)
-    base, fp8 = split_f8(base)
-    _, w4 = split_w4(base)
-    wk = StepWorkload(device, torch.cuda.Stream(), rms_eps, streamk,
-                      "int4" if w4 else "fp8" if fp8 else "bf16") if kind == "step" else \
-        GemvWorkload(kind, rows, K, B, device, l2, rms_eps, w4, streamk, fp8, cuda_cores)
-    torch.cuda.synchronize()
+def graph_partition(steps: int, copies: int, graph_max: int) -> tuple[int, int, int]:
+    """(a, q, r): graph A holds a calls (a multiple of the weight copies, at
+    most max(graph_max, copies)) and is replayed q times, graph B holds the
+    remaining r < a calls (or all of them when steps < copies); q * a + r ==
+    steps. Call i of either graph reads copy i % copies, so the copy sequence
+    over A ... A B never repeats a copy back to back when copies > 1."""
+    a = (min(steps, max(graph_max, copies)) // copies) * copies
+    q = steps // a if a else 0
+    return a, q, steps - q * a
 
-    def barrier():
-        if dist is not None:
-            dist.barrier()
+
+class TimedLoop:
+    """The K steps of the timed region, replayable: for matrix workloads CUDA
+    graphs of consecutive calls (graph A with a multiple of the weight copies,
+    replayed q times, then graph B with the remaining r calls, so that no two
+    neighbouring calls read the same copy), for the decode step K launches of
+    its captured plan."""
+
+    def __init__(self, torch, wk, steps: int, stream, graph_max: int):
+        self.torch, self.wk, self.steps, self.stream = torch, wk, steps, stream
+        self.graphs = []
+        if isinstance(wk, StepWorkload):
+            self.q, self.r = 0, 0
+            return
+        a, self.q, self.r = graph_partition(steps, wk.copies, graph_max)
+        self.gA = self._capture(a) if self.q else None
+        self.gB = self._capture(self.r) if self.r else None
+
+    def _capture(self, n: int):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream, capture_error_mode="thread_local"):
+            cs = torch.cuda.current_stream()
+            for i in range(n):
+                self.wk.step(i, cs)
+        return g
+
+    def run(self) -> None:
+        if isinstance(self.wk, StepWorkload):
+            for i in range(self.steps):
+                self.wk.step(i, self.stream)
+            return
+        for _ in range(self.q):
+            self.gA.replay()
+        if self.gB is not None:
+            self.gB.replay()
+
+
+def time_workload(torch, wk, args, stream, gpu_index: int, isolated: int = 20) -> dict:
+    """Warm up, time exactly args.steps steps on the device (clocks sampled
+    around the region while the same loop keeps the GPU busy), then time
+    single launches with the GPU idle before each."""
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            wk.step(i, stream)
+        loop = TimedLoop(torch, wk, args.steps, stream, args.graph_steps)
+        loop.run()
         torch.cuda.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
 
-    for i in range(max(3, args.warmup)):
-        wk.step(i, stream)
-    torch.cuda.synchronize()
+        def region() -> float:
+            torch.cuda.synchronize()
+            device_delay(torch)
+            ev0.record(stream)
+            loop.run()
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            return ev0.elapsed_time(ev1) / 1e3
 
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.05)
-    barrier()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for i in range(args.steps):
-        wk.step(i, stream)
-    ev1.record(stream)
-    barrier()
-    clock_info = clocks.stop()
-    seconds = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, dist, device)
+        est = region()
+        clocks = ClockSampler(gpu_index)
+        clocks.start()
+        soak = max(1, math.ceil(0.25 / max(est, 1e-6)))   # about 250 ms under the same load
+        for _ in range(soak):
+            loop.run()
+        seconds = region()
+        for _ in range(max(1, soak // 4)):
+            loop.run()
+        torch.cuda.synchronize()
+        clock_info = clocks.stop()
+        clock_info["soak_loops"] = soak
 
-    steps = args.steps
-    total_bytes = wk.bytes_per_step * steps * world
-    value = total_bytes / seconds / 1e9
-    per_launch_s = seconds / (steps * wk.launches_per_step)
+        iso = []
+        for i in range(isolated):
+            torch.cuda.synchronize()
+            device_delay(torch)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            wk.step(i, stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            iso.append(a.elapsed_time(b) / 1e3)
+    return {"seconds": seconds, "clocks": clock_info, "isolated_s": statistics.median(iso),
+            "graphs": {"calls_per_graph": (args.steps - loop.r) // loop.q if loop.q else loop.r,
+                       "replays": loop.q + (1 if loop.r else 0)}
+            if not isinstance(wk, StepWorkload) else {"plan_launches": args.steps}}
 
-    # end to end through the public call: pinned host x in, GEMV, host y out,
-    # synchronized, every step (gemv_bf16_host_io for single BF16 matrices)
-    e2e = None
-    if not args.no_e2e and kind != "step":
+
+def time_e2e(torch, binding, wk, steps: int, stream) -> dict | None:
+    """The same workload end to end through the public C entry points with
+    host buffers: every step copies its inputs in from pinned host memory,
+    runs, copies its outputs back and waits (host wall clock)."""
+    sh = stream.cuda_stream
+    if isinstance(wk, StepWorkload):
+        d = wk.data
+        x_host = d.x_arena.cpu().pin_memory()
+        y_host = torch.empty(d.y_arena.shape, dtype=d.y_arena.dtype).pin_memory()
+        xb = x_host.numel() * x_host.element_size()
+        yb = y_host.numel() * y_host.element_size()
+
+        def e2e_step(i):
+            wk.plan.launch_host_io(x_host, d.x_arena, xb, d.y_arena, y_host, yb, sh)
+        h2d, d2h = xb, yb
+        n = max(5, min(steps, 200))
+    else:
         x_host = wk.x.cpu().pin_memory()
         y_host = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in wk.ys]
         x_dev = torch.empty_like(wk.x)
-        e2e_steps = max(10, min(steps, 2000))
-        host_io = kind == "single" and not getattr(wk, "w4", False) and not getattr(wk, "fp8", False)
-        sk = getattr(wk, "streamk", False)
-        sh = stream.cuda_stream
+        bf16 = not wk.w4 and not wk.fp8
 
         def e2e_step(i):
-            if host_io:
-                binding.gemv_bf16_host_io(wk.Ws[i % wk.copies][0], x_host, y_host[0], x_dev, wk.ys[0],
-                                          wk.N, wk.K, wk.B, wk.ldw, rms_eps=wk.rms_eps, stream=sh,
-                                          streamk=sk, cuda_cores=getattr(wk, "cuda_cores", False))
-            else:
+            Ws = wk.Ws[i % wk.copies]
+            if bf16 and wk.kind == "single":
+                binding.gemv_bf16_host_io(Ws[0], x_host, y_host[0], x_dev, wk.ys[0], wk.N, wk.K, wk.B, wk.ldw,
+                                          rms_eps=wk.rms_eps, stream=sh, streamk=wk.streamk,
+                                          cuda_cores=wk.cuda_cores)
+            elif bf16:
+                binding.gemv_bf16_multi_host_io([(W, y, n_, wk.ldw) for W, y, n_ in zip(Ws, wk.ys, wk.rows)],
+                                                x_host, x_dev, y_host, wk.K, wk.B, rms_eps=wk.rms_eps,
+                                                stream=sh, streamk=wk.streamk, cuda_cores=wk.cuda_cores)
+            else:   # quantised weights: the binding's copy, launch, copy, wait
                 x_dev.copy_(x_host, non_blocking=True)
                 wk.step(i, stream, x_dev)
                 for yh, yd in zip(y_host, wk.ys):
                     yh.copy_(yd, non_blocking=True)
                 stream.synchronize()
-
+        h2d = int(x_host.numel() * x_host.element_size())
+        d2h = int(sum(y.numel() * y.element_size() for y in y_host))
+        n = max(10, min(steps, 2000))
+    with torch.cuda.stream(stream):
         for i in range(5):
             e2e_step(i)
-        barrier()
+        torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for i in range(e2e_steps):
+        for i in range(n):
             e2e_step(i)
-        e2e_s = max_over_ranks(time.perf_counter() - t0, dist, device)
-        e2e = {"value": round(wk.bytes_per_step * e2e_steps * world / e2e_s / 1e9, 2), "unit": UNIT,
-               "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
-               "d2h_bytes_per_step": int(sum(y.numel() * y.element_size() for y in y_host)),
-               "us_per_step": round(e2e_s / e2e_steps * 1e6, 3), "steps": e2e_steps}
+        el = time.perf_counter() - t0
+    return {"value": round(wk.bytes_per_step * n / el / 1e9, 2), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "us_per_step": round(el / n * 1e6, 3), "steps": n}
 
-    read_ceiling = None
-    if rank == 0 and not args.no_probe:
-        read_ceiling = read_ceiling_gbs(torch, binding, stream)
 
-    if rank != 0:
-        return None
+def make_workload(torch, name: str, device, l2: int):
+    kind, rows, K, B = describe(name)
+    _, rms_eps = split_norm(name)
+    base, streamk = split_sk(split_norm(name)[0])
+    base, cuda_cores = split_cc(base)
+    base, fp8 = split_f8(base)
+    _, w4 = split_w4(base)
+    if kind == "step":
+        return StepWorkload(device, torch.cuda.Stream(), rms_eps, streamk,
+                            "int4" if w4 else "fp8" if fp8 else "bf16")
+    return GemvWorkload(kind, rows, K, B, device, l2, rms_eps, w4, streamk, fp8, cuda_cores)
+
+
+def family_of(wk) -> str:
+    if isinstance(wk, StepWorkload):
+        return "w4" if wk.w4 else "f8" if wk.fp8 else "fma"
+    return ("w4" if wk.w4 else "f8" if wk.fp8 else "sk" if wk.streamk
+            else "fma" if (wk.B == 1 or wk.cuda_cores) else "mma")
+
+
+def target_entry(torch, binding, name: str, args, stream, device, l2, peak, read_ceiling, gpu_index) -> dict:
+    """One of the decode targets, timed like the headline."""
+    wk = make_workload(torch, name, device, l2)
+    t = time_workload(torch, wk, args, stream, gpu_index)
+    per_step = t["seconds"] / args.steps
+    gbs = wk.bytes_per_step / per_step / 1e9
+    out = {"workload": wk.config()["workload"], "bytes_per_step": wk.bytes_per_step,
+           "steps": args.steps, "us_per_step": round(per_step * 1e6, 3),
+           "us_isolated": round(t["isolated_s"] * 1e6, 3),
+           "gbs": round(gbs, 2), "frac": round(gbs / peak, 4),
+           "frac_of_read_probe": round(gbs / read_ceiling, 4) if read_ceiling else None,
+           "target_frac": TARGETS[name],
+           "met": gbs / peak >= TARGETS[name],
+           "met_vs_max_of_copy_and_read_probe": gbs / max(peak, read_ceiling or 0) >= TARGETS[name],
+           "gpu_launches": args.steps * wk.launches_per_step,
+           "clocks": t["clocks"]}
+    if isinstance(wk, StepWorkload):
+        out["launches_per_step"] = wk.launches_per_step
+    if not args.no_e2e:
+        out["e2e"] = time_e2e(torch, binding, wk, args.steps, stream)
+    del wk
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args) -> dict:
+    import torch
+    from memory_bound_decode_gb300 import binding, build_lib
+
+    build_lib.build()
+    binding.lib()
+    gpu_index = 0
+    torch.cuda.set_device(gpu_index)
+    device = torch.device("cuda", gpu_index)
+    stream = torch.cuda.Stream()
+    props = torch.cuda.get_device_properties(device)
+    l2 = getattr(props, "L2_cache_size", 126 << 20)
+
+    wk = make_workload(torch, args.workload, device, l2)
+    kind = "step" if isinstance(wk, StepWorkload) else wk.kind
+    torch.cuda.synchronize()
+    t = time_workload(torch, wk, args, stream, gpu_index)
+    seconds = t["seconds"]
+    steps = args.steps
+    value = wk.bytes_per_step * steps / seconds / 1e9
+    per_launch_s = seconds / (steps * wk.launches_per_step)
+
+    e2e = None if args.no_e2e else time_e2e(torch, binding, wk, steps, stream)
+
+    read_ceiling = None if args.no_probe else read_ceiling_gbs(torch, binding, stream)
+
     peak, peak_kind = load_peaks()
     achieved = wk.bytes_per_step / (seconds / steps) / 1e9 if kind == "step" else \
         wk.bytes_per_step / per_launch_s / 1e9
-    family = ("w4" if getattr(wk, "w4", False) else "f8" if getattr(wk, "fp8", False)
-              else "sk" if getattr(wk, "streamk", False)
-              else "fma" if (wk.B == 1 or getattr(wk, "cuda_cores", False)) else "mma")
+    family = family_of(wk)
     launch = None
     if kind == "single":
-        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        sms = props.multi_processor_count
         if family == "w4":
             launch = binding.gemv_w4_query_launch(wk.N, wk.K, wk.B, sms)
         elif family == "f8":
@@ -520,20 +667,25 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
             launch = binding.gemv_query_launch_ex(
                 wk.N, wk.K, wk.B, sms,
                 binding.GEMV_FLAG_STREAMK if family == "sk" else
-                binding.GEMV_FLAG_CUDA_CORES if getattr(wk, "cuda_cores", False) else 0)
+                binding.GEMV_FLAG_CUDA_CORES if wk.cuda_cores else 0)
     src_hash = kernel_source_hash(family, launch)
     traffic = profiled_traffic(args.workload, src_hash)
+    knobs = {k: v for k, v in os.environ.items() if k in ("GEMV_FORCE_SPLIT", "GEMV_FORCE_VARIANT", "GEMV_PDL")}
     result = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": 1,
         "steps": steps, "warmup": max(3, args.warmup),
         "ms_per_step": round(seconds / steps * 1e3, 6),
         "us_per_call": round(per_launch_s * 1e6, 3),
+        "us_isolated": round(t["isolated_s"] * 1e6, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {"w4": "u4 weights (bf16 group scales), bf16 x, fp32 accumulate",
                   "f8": "e4m3 weights (fp32 row scales), bf16 x, fp32 accumulate"}.get(family, "bf16 in, fp32 accumulate"),
         "data": "synthetic (seeded N(0,0.02^2) weights, N(0,1) x)",
-        "config": dict(wk.config(), parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
-                       pdl=os.environ.get("GEMV_PDL", "1") != "0"),
+        "config": dict(wk.config(), parallelism="1 GPU",
+                       pdl=os.environ.get("GEMV_PDL", "1") != "0",
+                       timing=("K steps as CUDA graph replays between two events, after a device-side "
+                               "delay kernel; " + json.dumps(t["graphs"])),
+                       **({"knobs": knobs} if knobs else {})),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": UNIT,
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_kind": f"{peak_kind} copy (MEASURED_PEAKS hbm_gbs, burst)"
@@ -541,7 +693,7 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
                      "kernel": ("gemv_w4_kernel (INT4 codes, BF16 tensor cores)" if family == "w4"
                                 else "gemv_fp8_kernel (E4M3 codes, BF16 tensor cores)" if family == "f8"
                                 else "gemv_streamk_kernel (CUDA cores, one-wave grid)" if family == "sk"
-                                else "gemv_bf16_kernel (CUDA cores)" if wk.B == 1
+                                else "gemv_bf16_kernel (CUDA cores)" if wk.B == 1 or family == "fma"
                                 else "gemv_bf16_mma_kernel (BF16 tensor cores)"),
                      "kernel_source_hash": src_hash},
         "ceilings": {"copy_gbs": peak,
@@ -550,10 +702,25 @@ def run_ours(args, rank: int, world: int, dist) -> dict | None:
                      "frac_of_read_probe": round(achieved / read_ceiling, 4) if read_ceiling else None,
                      "frac_of_vendor": round(achieved / VENDOR_HBM_GBS, 4)},
         "gpu_launches": steps * wk.launches_per_step,
-        "clocks": clock_info,
+        "clocks": t["clocks"],
     }
     if e2e is not None:
         result["e2e"] = e2e
+    del wk
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    if args.workload == "down_proj" and not args.no_targets:
+        targets = {"down_proj": {"us_per_step": result["us_per_call"], "gbs": result["value"],
+                                 "frac": result["roofline"]["frac"],
+                                 "frac_of_read_probe": result["ceilings"]["frac_of_read_probe"],
+                                 "target_frac": TARGETS["down_proj"],
+                                 "met": result["roofline"]["frac"] >= TARGETS["down_proj"],
+                                 "met_vs_max_of_copy_and_read_probe":
+                                     achieved / max(peak, read_ceiling or 0) >= TARGETS["down_proj"]}}
+        for name in ("gate_up", "decode_step"):
+            targets[name] = target_entry(torch, binding, name, args, stream, device, l2, peak, read_ceiling,
+                                         gpu_index)
+        result["targets"] = targets
     return result
 
 
@@ -656,21 +823,15 @@ def main(argv=None) -> int:
             print(json.dumps(out), flush=True)
         return 0
 
-    dist = None
-    if world > 1:
-        import torch
-        import torch.distributed as dist_mod
-        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
-        dist_mod.init_process_group("nccl")
-        dist = dist_mod
-    out = run_ours(args, rank, world, dist)
-    if out is not None:
-        if not args.no_cpu_baseline and world == 1:
-            out["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
-        print(json.dumps(out), flush=True)
-    if dist is not None:
-        dist.barrier()
-        dist.destroy_process_group()
+    if world > 1 or args.gpus != 1:
+        # Checked before anything touches CUDA: the path runs on one GPU.
+        print(f"bench.py: one GPU only (got --gpus {args.gpus}, WORLD_SIZE {world}); "
+              "the decode GEMV has no multi-GPU form here", file=sys.stderr, flush=True)
+        return 2
+    out = run_ours(args)
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+    print(json.dumps(out), flush=True)
     return 0
 
 

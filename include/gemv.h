@@ -38,7 +38,9 @@
  * within the accuracy bound |y - exact| <= 1e-5 * sum_k |W[n][k] * x[b][k]|.
  *
  * Streams: every call is asynchronous on the given stream (a cudaStream_t passed
- * as void*; NULL means the legacy default stream) and never synchronizes.
+ * as void*; NULL means the legacy default stream) and never synchronizes, except
+ * the three *_host_io calls, which copy host buffers in and out and wait for
+ * their stream.
  * Launch failures return GEMV_ERR_CUDA; gemv_last_cuda_error() then returns the
  * cudaError_t. Faults inside a kernel surface at the caller's next
  * synchronization, as for any CUDA kernel. The kernels read W before they wait
@@ -152,7 +154,8 @@ int gemv_bf16_ex(const void *W, const void *x, float *y,
  * BF16, 16-byte aligned; y_dev B*N floats); the library allocates nothing (but
  * the stream-K workspace, see GEMV_FLAG_STREAMK). This is the whole
  * host-to-host path of one decode-step projection, timed end to end by the
- * benchmark.
+ * benchmark. Returns GEMV_ERR_CAPTURE on a capturing stream (the call waits for
+ * its stream).
  */
 int gemv_bf16_host_io(const void *W, const void *x_host, float *y_host,
                       void *x_dev, float *y_dev,
@@ -186,6 +189,22 @@ int gemv_bf16_multi(const gemv_segment *segs, int nsegs, const void *x,
 /* gemv_bf16_multi with options; the options apply to every segment (one x). */
 int gemv_bf16_multi_ex(const gemv_segment *segs, int nsegs, const void *x,
                        int64_t K, int B, const gemv_options *opt, void *stream);
+
+/*
+ * gemv_bf16_multi_ex for a caller whose activations live in host memory (the
+ * end-to-end path of a fused projection, "How to optimize an ML kernel that
+ * underutilizes the GPU", Step 5: compare the end-to-end time with the
+ * kernel's): copies x from x_host (B*K BF16, pinned memory recommended) to the
+ * device buffer x_dev (B*K BF16), runs the fused launch over segs (their y are
+ * device buffers, as for gemv_bf16_multi_ex), copies each segment's y to the
+ * host buffer y_host[i] (B*N_i floats) and waits for the stream, so the host
+ * buffers hold the results on return. The wait polls the stream for up to a
+ * millisecond before it blocks. Allocates nothing. Returns GEMV_ERR_CAPTURE on
+ * a capturing stream (the call waits for its stream).
+ */
+int gemv_bf16_multi_host_io(const gemv_segment *segs, int nsegs, const void *x_host, void *x_dev,
+                            float *const *y_host, int64_t K, int B, const gemv_options *opt,
+                            void *stream);
 
 /*
  * One projection of a decode step. Projections with the same fuse_group > 0,
@@ -246,6 +265,22 @@ int gemv_plan_capture(gemv_plan *plan, void *stream);
  * launches. Returns GEMV_ERR_UNSUPPORTED if the plan was never captured.
  */
 int gemv_plan_launch(gemv_plan *plan, void *stream);
+
+/*
+ * A decode step from host to host ("GPU performance chains", "Launch gaps in
+ * a decode step": the step's time is what the caller waits for, gaps and
+ * copies included): copies x_bytes from x_host to x_dev, launches the captured
+ * plan, copies y_bytes from y_dev to y_host and waits for the stream, so
+ * y_host holds the step's outputs on return. The caller lays the plan's
+ * activation vectors out in one device buffer (x_dev) and its outputs in
+ * another (y_dev), so that each direction is one copy; x_bytes or y_bytes may
+ * be 0 (no copy, pointers then unused). Pinned host buffers are recommended.
+ * The wait polls the stream for up to a millisecond before it blocks.
+ * Returns GEMV_ERR_UNSUPPORTED if the plan was never captured,
+ * GEMV_ERR_CAPTURE on a capturing stream. Allocates nothing.
+ */
+int gemv_plan_launch_host_io(gemv_plan *plan, const void *x_host, void *x_dev, int64_t x_bytes,
+                             const void *y_dev, void *y_host, int64_t y_bytes, void *stream);
 
 /* Number of kernel launches one gemv_plan_launch performs (after fusion). */
 int gemv_plan_num_launches(const gemv_plan *plan);
@@ -309,7 +344,10 @@ int gemv_workspace_release(void);
  * Status bits the kernels recorded on the current device since the last reset:
  * GEMV_STATUS_WAIT_TIMEOUT means a kernel gave up waiting for a copy of x into
  * shared memory (an mbarrier wait has an iteration limit instead of spinning
- * forever); the outputs of that launch are then undefined. Writes the bits to
+ * forever); the CTAs that gave up store NaN in place of their outputs, so a
+ * timed-out launch never returns plausible numbers. The calls themselves still
+ * return GEMV_OK (the wait happens on the device, after the call): a caller
+ * that must know reads the bits after synchronizing. Writes the bits to
  * *bits and clears them when reset != 0. Synchronous with respect to the
  * device's work (like cudaMemcpyFromSymbol). Returns GEMV_OK, GEMV_ERR_INVALID
  * for a NULL pointer, or GEMV_ERR_CUDA.

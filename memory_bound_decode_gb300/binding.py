@@ -38,8 +38,9 @@ GEMV_WEIGHT_FP8 = 2
 
 EXPORTED = [
     "gemv_bf16", "gemv_bf16_ex", "gemv_bf16_host_io", "gemv_bf16_multi", "gemv_bf16_multi_ex",
+    "gemv_bf16_multi_host_io",
     "gemv_plan_create", "gemv_plan_capture",
-    "gemv_plan_launch", "gemv_plan_num_launches", "gemv_plan_destroy",
+    "gemv_plan_launch", "gemv_plan_launch_host_io", "gemv_plan_num_launches", "gemv_plan_destroy",
     "gemv_query_launch", "gemv_query_launch_ex", "gemv_workspace_release", "gemv_device_status",
     "gemv_bf16_streamk_noalloc",
     "gemv_debug_write_count",
@@ -136,6 +137,10 @@ def _load(path: str) -> ctypes.CDLL:
                                    ctypes.POINTER(vp)]
     L.gemv_plan_capture.argtypes = [vp, vp]
     L.gemv_plan_launch.argtypes = [vp, vp]
+    L.gemv_plan_launch_host_io.argtypes = [vp, vp, vp, i64, vp, vp, i64, vp]
+    L.gemv_bf16_multi_host_io.argtypes = [ctypes.POINTER(gemv_segment), ctypes.c_int, vp, vp,
+                                          ctypes.POINTER(vp), i64, ctypes.c_int,
+                                          ctypes.POINTER(gemv_options), vp]
     L.gemv_plan_num_launches.argtypes = [vp]
     L.gemv_plan_destroy.argtypes = [vp]
     L.gemv_plan_destroy.restype = None
@@ -237,6 +242,20 @@ def gemv_bf16_multi_ex(segments, x, K: int, B: int, rms_eps=None, stream=None, c
     opt = ctypes.byref(options) if options is not None else _options(rms_eps, streamk, cuda_cores)
     rc = lib().gemv_bf16_multi_ex(arr, len(segments), _ptr(x), K, B, opt, _stream(stream))
     return _check(rc, "gemv_bf16_multi_ex") if check else rc
+
+
+def gemv_bf16_multi_host_io(segments, x_host, x_dev, y_host, K: int, B: int, rms_eps=None, stream=None,
+                            check: bool = True, streamk: bool = False, cuda_cores: bool = False) -> int:
+    """Host x in, fused launch over ``segments`` (W, y_dev, N, ldw), each
+    segment's y copied to ``y_host[i]``, synchronous (see gemv.h)."""
+    n = len(segments)
+    arr = (gemv_segment * max(1, n))()
+    for i, (W, y, N, ldw) in enumerate(segments):
+        arr[i] = gemv_segment(_ptr(W), _ptr(y), N, ldw)
+    yh = (vp * max(1, n))(*[_ptr(t) for t in y_host])
+    rc = lib().gemv_bf16_multi_host_io(arr, n, _ptr(x_host), _ptr(x_dev), yh, K, B,
+                                       _options(rms_eps, streamk, cuda_cores), _stream(stream))
+    return _check(rc, "gemv_bf16_multi_host_io") if check else rc
 
 
 def gemv_bf16_multi(segments, x, K: int, B: int, stream=None, check: bool = True) -> int:
@@ -364,6 +383,13 @@ class Plan:
     def launch(self, stream=None, check: bool = True) -> int:
         rc = lib().gemv_plan_launch(self._h, _stream(stream))
         return _check(rc, "gemv_plan_launch") if check else rc
+
+    def launch_host_io(self, x_host, x_dev, x_bytes: int, y_dev, y_host, y_bytes: int, stream=None,
+                       check: bool = True) -> int:
+        """gemv_plan_launch_host_io: host x in, the captured step, host y out, synchronous."""
+        rc = lib().gemv_plan_launch_host_io(self._h, _ptr(x_host), _ptr(x_dev), int(x_bytes), _ptr(y_dev),
+                                            _ptr(y_host), int(y_bytes), _stream(stream))
+        return _check(rc, "gemv_plan_launch_host_io") if check else rc
 
     def num_launches(self) -> int:
         return lib().gemv_plan_num_launches(self._h)

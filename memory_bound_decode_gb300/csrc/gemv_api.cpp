@@ -413,6 +413,35 @@ void fill_info(const Launch& l, gemv_launch_info* out) {
 
 }  // namespace
 
+namespace {
+
+// Wait for the end of a host-to-host call: poll for up to a millisecond (a
+// decode projection takes tens of microseconds and a blocking wait adds a
+// wake-up), then block.
+int wait_host_io(cudaStream_t s) {
+    const auto t0 = std::chrono::steady_clock::now();
+    cudaError_t e;
+    for (;;) {
+        e = cudaStreamQuery(s);
+        if (e == cudaSuccess) return GEMV_OK;
+        if (e != cudaErrorNotReady) return cuda_fail(e);
+        if (std::chrono::steady_clock::now() - t0 > std::chrono::milliseconds(1)) break;
+    }
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e);
+    return GEMV_OK;
+}
+
+// The host-to-host calls wait for their stream, which a capturing stream
+// cannot do.
+int not_capturing(cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return cs == cudaStreamCaptureStatusNone ? GEMV_OK : GEMV_ERR_CAPTURE;
+}
+
+}  // namespace
+
 struct gemv_plan {
     std::vector<Prepared> launches;
     cudaGraph_t graph = nullptr;
@@ -448,6 +477,7 @@ int gemv_bf16_host_io(const void* W, const void* x_host, float* y_host, void* x_
     float eps = 0.f;
     if ((rc = check_options(opt, &flags, &eps)) != GEMV_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((rc = not_capturing(s)) != GEMV_OK) return rc;
     const size_t xbytes = static_cast<size_t>(B) * static_cast<size_t>(K) * 2;
     const size_t ybytes = static_cast<size_t>(B) * static_cast<size_t>(N) * 4;
     // A device-mapped y_host (pinned memory) takes the kernel's stores directly
@@ -466,17 +496,33 @@ int gemv_bf16_host_io(const void* W, const void* x_host, float* y_host, void* x_
     if (!y_mapped &&
         (e = cudaMemcpyAsync(y_host, y_dev, ybytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
         return cuda_fail(e);
-    // Poll for up to a millisecond (a decode step is tens of microseconds and a
-    // blocking wait adds a wake-up), then block.
-    const auto t0 = std::chrono::steady_clock::now();
-    for (;;) {
-        e = cudaStreamQuery(s);
-        if (e == cudaSuccess) return GEMV_OK;
-        if (e != cudaErrorNotReady) return cuda_fail(e);
-        if (std::chrono::steady_clock::now() - t0 > std::chrono::milliseconds(1)) break;
+    return wait_host_io(s);
+}
+
+int gemv_bf16_multi_host_io(const gemv_segment* segs, int nsegs, const void* x_host, void* x_dev,
+                            float* const* y_host, int64_t K, int B, const gemv_options* opt, void* stream) {
+    if (!segs || nsegs < 1 || nsegs > GEMV_MAX_SEGMENTS || !x_host || !y_host) return GEMV_ERR_INVALID;
+    for (int i = 0; i < nsegs; ++i)
+        if (!y_host[i]) return GEMV_ERR_INVALID;
+    int rc = check_common(x_dev, K, B);
+    if (rc != GEMV_OK) return rc;
+    for (int i = 0; i < nsegs; ++i)
+        if ((rc = check_matrix(segs[i].W, segs[i].y, segs[i].N, K, segs[i].ldw)) != GEMV_OK) return rc;
+    int flags = 0;
+    float eps = 0.f;
+    if ((rc = check_options(opt, &flags, &eps)) != GEMV_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((rc = not_capturing(s)) != GEMV_OK) return rc;
+    const size_t xbytes = static_cast<size_t>(B) * static_cast<size_t>(K) * 2;
+    cudaError_t e = cudaMemcpyAsync(x_dev, x_host, xbytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if ((rc = gemv_bf16_multi_ex(segs, nsegs, x_dev, K, B, opt, stream)) != GEMV_OK) return rc;
+    for (int i = 0; i < nsegs; ++i) {
+        const size_t ybytes = static_cast<size_t>(B) * static_cast<size_t>(segs[i].N) * 4;
+        if ((e = cudaMemcpyAsync(y_host[i], segs[i].y, ybytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+            return cuda_fail(e);
     }
-    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e);
-    return GEMV_OK;
+    return wait_host_io(s);
 }
 
 int gemv_bf16(const void* W, const void* x, float* y, int64_t N, int64_t K, int B, int64_t ldw,
@@ -633,6 +679,26 @@ int gemv_plan_launch(gemv_plan* plan, void* stream) {
     cudaError_t e = cudaGraphLaunch(plan->exec, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return GEMV_OK;
+}
+
+int gemv_plan_launch_host_io(gemv_plan* plan, const void* x_host, void* x_dev, int64_t x_bytes,
+                             const void* y_dev, void* y_host, int64_t y_bytes, void* stream) {
+    if (!plan || x_bytes < 0 || y_bytes < 0) return GEMV_ERR_INVALID;
+    if (x_bytes > 0 && (!x_host || !x_dev)) return GEMV_ERR_INVALID;
+    if (y_bytes > 0 && (!y_host || !y_dev)) return GEMV_ERR_INVALID;
+    if (!plan->exec) return GEMV_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int rc = not_capturing(s);
+    if (rc != GEMV_OK) return rc;
+    cudaError_t e;
+    if (x_bytes > 0 &&
+        (e = cudaMemcpyAsync(x_dev, x_host, static_cast<size_t>(x_bytes), cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail(e);
+    if ((e = cudaGraphLaunch(plan->exec, s)) != cudaSuccess) return cuda_fail(e);
+    if (y_bytes > 0 &&
+        (e = cudaMemcpyAsync(y_host, y_dev, static_cast<size_t>(y_bytes), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return cuda_fail(e);
+    return wait_host_io(s);
 }
 
 int gemv_plan_num_launches(const gemv_plan* plan) {

@@ -179,6 +179,7 @@ gemv_bf16_kernel(const __grid_constant__ Params p) {
     uint4 wv[UJ][RPW];
     bool ok[UJ];
     const uint16_t* wp[RPW];
+    bool x_ok = true;   // false when the wait for the multicast copy of x ran out
 
     // Chunk 0: weight loads go out first; then wait for the preceding grid (x
     // may be its output) and start copying x.
@@ -215,7 +216,10 @@ gemv_bf16_kernel(const __grid_constant__ Params p) {
             }
             *reinterpret_cast<uint4*>(xs + col) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        mbar_wait_bounded(mbar, 0);
+        x_ok = mbar_wait_bounded(mbar, 0);
+        // Second phase of the cluster barrier: arrive now, wait just before
+        // exit, so that no CTA of the cluster leaves while its peers still run.
+        cluster_arrive_relaxed();
     } else {
         stage_x(xs, xstride, p.x, B, K, ch.c0, ch.nv);
     }
@@ -272,12 +276,14 @@ gemv_bf16_kernel(const __grid_constant__ Params p) {
     }
 
     // Lane reduction: the same xor butterfly for every row, so the result does
-    // not depend on where a row sits in the grid.
+    // not depend on where a row sits in the grid. A launch whose copy of x did
+    // not arrive in time stores NaN (and has set the status bit) rather than
+    // sums over an incomplete x.
 #pragma unroll
     for (int r = 0; r < RPW; ++r)
 #pragma unroll
         for (int b = 0; b < B; ++b) {
-            float v = acc[r][b];
+            float v = x_ok ? acc[r][b] : __uint_as_float(0x7fc00000u);
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
             acc[r][b] = v;
@@ -291,6 +297,12 @@ gemv_bf16_kernel(const __grid_constant__ Params p) {
     }
     combine_and_store(red, cpart, misc, rows_per_cta, B, kw, S, split, sg.tile_local * rows_per_cta, sg.N, sg.y,
                       norm, K, p.rms_eps, p.wc);
+    if constexpr (mcast) {
+        // After a timed-out wait the copy may still be in flight into this
+        // CTA's shared memory: wait for it once more (bounded) before leaving.
+        if (!x_ok) mbar_wait_bounded(mbar, 0);
+        cluster_wait();
+    }
 }
 
 template <int B>

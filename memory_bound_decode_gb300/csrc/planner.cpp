@@ -16,7 +16,22 @@
 //     over a cluster of up to 4 CTAs first: that keeps many rows per CTA, so the
 //     x slice each CTA stages (B rows of it) stays small next to the weight bytes
 //     it streams; then among the warps of a CTA; then over up to 8 CTAs.
+//
+// Sweep knobs (environment, read on every plan; unset in normal use), so that
+// the measured alternatives to these rules can be reproduced:
+//   GEMV_FORCE_SPLIT=<kw>x<S>   warps along K (1, 2, 4, 8) and CTAs along K
+//                               (1, 2, 4, 8) instead of the rules' choice;
+//   GEMV_FORCE_VARIANT=<list>   comma-separated: mcast=<1|2|4|8> (CTAs sharing
+//                               one multicast copy of x, where the multicast
+//                               instance applies), unroll=<4|8> (INT4 / FP8:
+//                               the standard or the deep instance, where the
+//                               deep one applies), streamk=<0|1> (batch-1 BF16
+//                               calls: the stream-K kernel or not).
+// A value the planner cannot use makes every plan fail with GEMV_ERR_INVALID,
+// so that a mistyped sweep stops instead of timing the default.
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 
 #include "../../include/gemv.h"
 #include "gemv_internal.h"
@@ -24,6 +39,64 @@
 namespace gemv {
 
 namespace {
+
+struct Overrides {
+    int kw = 0, splits = 0;    // 0: the rules decide
+    int mcast = 0;             // 0: the rules decide
+    int unroll = 0;            // 0: the rules decide
+    int streamk = -1;          // -1: the rules decide
+    bool bad = false;
+};
+
+bool pow2_upto8(long v) { return v == 1 || v == 2 || v == 4 || v == 8; }
+
+Overrides read_overrides() {
+    Overrides o;
+    if (const char* s = std::getenv("GEMV_FORCE_SPLIT")) {
+        char* end = nullptr;
+        const long kw = std::strtol(s, &end, 10);
+        if (end && *end == 'x') {
+            const char* t = end + 1;
+            const long sp = std::strtol(t, &end, 10);
+            if (end != t && *end == '\0' && pow2_upto8(kw) && pow2_upto8(sp)) {
+                o.kw = static_cast<int>(kw);
+                o.splits = static_cast<int>(sp);
+            } else {
+                o.bad = true;
+            }
+        } else if (*s != '\0') {
+            o.bad = true;
+        }
+    }
+    if (const char* s = std::getenv("GEMV_FORCE_VARIANT")) {
+        const char* p = s;
+        while (*p) {
+            const char* comma = std::strchr(p, ',');
+            const size_t len = comma ? static_cast<size_t>(comma - p) : std::strlen(p);
+            const char* eq = static_cast<const char*>(std::memchr(p, '=', len));
+            if (!eq) {
+                o.bad = true;
+                break;
+            }
+            const size_t klen = static_cast<size_t>(eq - p);
+            char* end = nullptr;
+            const long v = std::strtol(eq + 1, &end, 10);
+            const bool num = end == p + len && end != eq + 1;
+            if (num && klen == 5 && std::strncmp(p, "mcast", 5) == 0 && pow2_upto8(v)) {
+                o.mcast = static_cast<int>(v);
+            } else if (num && klen == 6 && std::strncmp(p, "unroll", 6) == 0 && (v == 4 || v == 8)) {
+                o.unroll = static_cast<int>(v);
+            } else if (num && klen == 7 && std::strncmp(p, "streamk", 7) == 0 && (v == 0 || v == 1)) {
+                o.streamk = static_cast<int>(v);
+            } else {
+                o.bad = true;
+                break;
+            }
+            p = comma ? comma + 1 : p + len;
+        }
+    }
+    return o;
+}
 
 constexpr int64_t kTargetInflightPerSm = 64 * 1024;
 constexpr int64_t kXBudgetBytes = 80 * 1024;   // staged x per CTA, all buffers
@@ -37,10 +110,13 @@ int64_t round_up(int64_t a, int64_t m) { return cdiv(a, m) * m; }
 }  // namespace
 
 namespace {
-int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind, int q_unroll);
+int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind, int q_unroll,
+              const Overrides& ov);
 }  // namespace
 
 int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind) {
+    const Overrides ov = read_overrides();
+    if (ov.bad) return GEMV_ERR_INVALID;
     // INT4 and FP8 with up to 8 rows: the deep instance (8 slots in flight per
     // lane; 2 CTAs per SM by registers, one x chunk) when its grid fits in one
     // wave of it and spreads over the SMs at least as evenly as the standard
@@ -48,12 +124,16 @@ int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weig
     // share of CTA places in use, grid / (SMs * ceil(grid / SMs)), is compared
     // (measured per decode shape).
     const bool w4 = weight_kind == kWeightInt4, f8 = weight_kind == kWeightFp8;
-    int rc = plan_with(N, K, B, sm_count, out, weight_kind, w4 ? kW4Unroll : kF8Unroll);
-    if (rc != GEMV_OK || !(w4 || f8) || B > 8) return rc;
+    int rc = plan_with(N, K, B, sm_count, out, weight_kind, w4 ? kW4Unroll : kF8Unroll, ov);
+    if (rc != GEMV_OK || !(w4 || f8) || B > 8 || ov.unroll == 4) return rc;
     Launch deep;
-    if (plan_with(N, K, B, sm_count, &deep, weight_kind, w4 ? kW4DeepUnroll : kF8DeepUnroll) != GEMV_OK ||
+    if (plan_with(N, K, B, sm_count, &deep, weight_kind, w4 ? kW4DeepUnroll : kF8DeepUnroll, ov) != GEMV_OK ||
         deep.nbuf != 1)
         return rc;
+    if (ov.unroll == 8) {
+        *out = deep;
+        return GEMV_OK;
+    }
     auto balance = [&](int64_t grid) {
         const int64_t per_sm = cdiv(grid, sm_count);
         return static_cast<double>(grid) / static_cast<double>(per_sm * sm_count);
@@ -64,7 +144,8 @@ int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weig
 
 namespace {
 
-int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind, int q_unroll) {
+int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind, int q_unroll,
+              const Overrides& ov) {
     if (!out || N < 1 || K < 1 || B < 1 || B > kMaxBatch || sm_count < 1) return GEMV_ERR_INVALID;
     if (weight_kind != kWeightBf16 && weight_kind != kWeightInt4 && weight_kind != kWeightFp8 &&
         weight_kind != kWeightBf16CudaCores)
@@ -158,7 +239,10 @@ int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight
     // along K while the CTA's x slice does not fit in one staged chunk (same
     // warps, fewer x bytes per CTA, no chunk barriers). The FP8 kernel measured
     // faster with the chunks.
-    if (cluster_first && path != kPathFp8) {
+    if (ov.kw > 0) {
+        kw = ov.kw;
+        splits = ov.splits;
+    } else if (cluster_first && path != kPathFp8) {
         while (splits < kMaxSplits && kw > 1 &&
                static_cast<int64_t>(B) * (cdiv(K, splits) + xpad) * 2 > kXBudgetBytes) {
             splits *= 2;
@@ -187,8 +271,9 @@ int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight
     // in clusters of kMcastCtas along the rows share one multicast copy of x
     // (the grid is rounded up to whole clusters; the extra CTAs' rows are past
     // N and their results dropped).
-    const int mcast = (path == kPathFma && B == 1 && splits == 1 && nbuf == 1 && K / 8 >= kMcastMinVectors &&
-                       row_tiles >= kMcastCtas) ? kMcastCtas : 1;
+    const bool mcast_ok = path == kPathFma && B == 1 && splits == 1 && nbuf == 1;
+    int mcast = (mcast_ok && K / 8 >= kMcastMinVectors && row_tiles >= kMcastCtas) ? kMcastCtas : 1;
+    if (ov.mcast > 0) mcast = (mcast_ok && K >= 8 && row_tiles >= ov.mcast) ? ov.mcast : 1;
     const int64_t grid = mcast > 1 ? round_up(row_tiles, mcast) : row_tiles * splits;
     if (grid > 0x7fffffffLL) return GEMV_ERR_UNSUPPORTED;
     const int64_t smem = (path == kPathFma ? kFmaSmemHead : 0) + nbuf * static_cast<int64_t>(B) * xstride * 2 +
@@ -256,9 +341,14 @@ int plan_streamk(int64_t rows, int64_t K, int B, int sm_count, SkLaunch* out) {
     return GEMV_OK;
 }
 
+// The default grid measured faster than the stream-K grid on every decode
+// shape (batch 1, 2,000 calls each), so the rules never pick it; the sweep
+// knob streamk=1 does, for batch-1 shapes the stream-K kernel takes.
 bool prefer_streamk(int64_t rows, int64_t K, int B, int sm_count) {
-    (void)rows; (void)K; (void)B; (void)sm_count;
-    return false;
+    const Overrides ov = read_overrides();
+    if (ov.bad || ov.streamk != 1 || B != 1) return false;
+    SkLaunch l;
+    return plan_streamk(rows, K, B, sm_count, &l) == GEMV_OK;
 }
 
 }  // namespace gemv

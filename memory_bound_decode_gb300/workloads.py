@@ -75,11 +75,19 @@ class DecodeStep:
         self.xs: list[tuple[torch.Tensor, int]] = []
         H, I, V = spec["hidden"], spec["intermediate"], spec["vocab"]
         Q, KV = spec["q_rows"], spec["kv_rows"]
+        L = spec["layers"]
+        # Every activation vector lives in one buffer and every output in
+        # another (views at 16-byte multiples), so a step's inputs and outputs
+        # each cross the host link as one copy (gemv_plan_launch_host_io).
+        self.x_arena = torch.empty(L * (H + I) + H, dtype=torch.bfloat16, device=device)
+        self.y_arena = torch.empty(L * (Q + 2 * KV + H + 2 * I + H) + V, dtype=torch.float32, device=device)
+        self._x_off = 0
+        self._y_off = 0
         group = 0
         for l in range(spec["layers"]):
             base = 16 * l
-            xh = inputs.activations(1, H, seed=seed, index=base + 14, device=device)
-            xi = inputs.activations(1, I, seed=seed, index=base + 15, device=device)
+            xh = self._x_view(inputs.activations(1, H, seed=seed, index=base + 14, device=device))
+            xi = self._x_view(inputs.activations(1, I, seed=seed, index=base + 15, device=device))
             self.xs += [(xh, base + 14), (xi, base + 15)]
             group += 1
             for j, (nm, n) in enumerate([("q", Q), ("k", KV), ("v", KV)]):
@@ -90,12 +98,21 @@ class DecodeStep:
             self._add(f"l{l}.up_proj", I, H, xh, group, seed, base + 5)
             self._add(f"l{l}.down_proj", H, I, xi, 0, seed, base + 6)
         base = 16 * spec["layers"]
-        xl = inputs.activations(1, H, seed=seed, index=base + 1, device=device)
+        xl = self._x_view(inputs.activations(1, H, seed=seed, index=base + 1, device=device))
         self.xs.append((xl, base + 1))
         self._add("lm_head", V, H, xl, 0, seed, base)
+        assert self._x_off == self.x_arena.numel() and self._y_off == self.y_arena.numel()
+
+    def _x_view(self, x: torch.Tensor) -> torch.Tensor:
+        n = x.shape[1]
+        v = self.x_arena[self._x_off:self._x_off + n].view(1, n)
+        v.copy_(x)
+        self._x_off += n
+        return v
 
     def _add(self, name, N, K, x, group, seed, index):
-        y = torch.empty((1, N), dtype=torch.float32, device=self.device)
+        y = self.y_arena[self._y_off:self._y_off + N].view(1, N)
+        self._y_off += N
         if self.weights == "bf16":
             ldw = inputs.padded_ldw(K)
             W = inputs.weight(N, K, ldw, seed=seed, index=index, device=self.device)

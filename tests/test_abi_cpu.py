@@ -287,3 +287,61 @@ def test_multicast_copy_geometry(L, N, K):
 
 def test_device_status_rejects_null(L):
     assert L.gemv_device_status(None, 0) == binding.GEMV_ERR_INVALID
+
+
+# ---- sweep knobs (GEMV_FORCE_SPLIT, GEMV_FORCE_VARIANT): read on every plan
+
+
+@pytest.mark.parametrize("kw,S", [(1, 1), (2, 1), (1, 2), (4, 2), (2, 4), (8, 8)])
+def test_force_split(L, monkeypatch, kw, S):
+    default = binding.gemv_query_launch(4096, 14336, 1, GB300_SMS)
+    monkeypatch.setenv("GEMV_FORCE_SPLIT", f"{kw}x{S}")
+    q = binding.gemv_query_launch(4096, 14336, 1, GB300_SMS)
+    assert q["warps_per_row"] == kw and q["splits"] == S
+    assert q["rows_per_cta"] == 8 // kw
+    assert q["kslice"] * q["splits"] >= 14336 and q["kslice"] % 256 == 0
+    assert q["mcast"] == (2 if S == 1 else 1)
+    # the tensor-core path and the quantised kernels take it as well
+    t = binding.gemv_query_launch(4096, 14336, 16, GB300_SMS)
+    assert t["warps_per_row"] == kw and t["splits"] == S
+    f = binding.gemv_fp8_query_launch(4096, 14336, 1, GB300_SMS)
+    assert f["warps_per_row"] == kw and f["splits"] == S
+    monkeypatch.delenv("GEMV_FORCE_SPLIT")
+    assert binding.gemv_query_launch(4096, 14336, 1, GB300_SMS) == default
+
+
+@pytest.mark.parametrize("bad", ["3x1", "2x16", "2", "x2", "2x", "2x2x", "a"])
+def test_force_split_rejects(L, monkeypatch, bad):
+    monkeypatch.setenv("GEMV_FORCE_SPLIT", bad)
+    info = binding.gemv_launch_info()
+    assert L.gemv_query_launch(4096, 14336, 1, GB300_SMS, ctypes.byref(info)) == binding.GEMV_ERR_INVALID
+
+
+def test_force_variant(L, monkeypatch):
+    assert binding.gemv_query_launch(4096, 14336, 1, GB300_SMS)["mcast"] == 2
+    assert binding.gemv_query_launch(1024, 4096, 1, GB300_SMS)["mcast"] == 1
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", "mcast=1")
+    assert binding.gemv_query_launch(4096, 14336, 1, GB300_SMS)["mcast"] == 1
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", "mcast=4")
+    q = binding.gemv_query_launch(4096, 14336, 1, GB300_SMS)
+    assert q["mcast"] == 4 and q["grid"] % 4 == 0
+    assert binding.gemv_query_launch(1024, 4096, 1, GB300_SMS)["mcast"] == 4   # below the size rule
+    assert binding.gemv_query_launch(4096, 14336, 2, GB300_SMS)["mcast"] == 1  # batch 2: no multicast
+    # the quantised kernels' deep and standard instances
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", "unroll=4")
+    assert binding.gemv_fp8_query_launch(4096, 14336, 1, GB300_SMS)["unroll"] == 4
+    assert binding.gemv_w4_query_launch(4096, 14336, 1, GB300_SMS)["unroll"] == 4
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", "unroll=8")
+    assert binding.gemv_fp8_query_launch(128256, 4096, 1, GB300_SMS)["unroll"] == 8
+    assert binding.gemv_w4_query_launch(128256, 4096, 4, GB300_SMS)["unroll"] == 8
+    assert binding.gemv_w4_query_launch(128256, 4096, 16, GB300_SMS)["unroll"] == 4   # no deep instance
+    # stream-K for batch-1 BF16 calls
+    assert binding.gemv_query_launch_ex(4096, 4096, 1, GB300_SMS, 0)["path"] == 0
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", "streamk=1,mcast=2")
+    assert binding.gemv_query_launch_ex(4096, 4096, 1, GB300_SMS, 0)["path"] == 3
+    assert binding.gemv_query_launch_ex(4096, 4096, 2, GB300_SMS, 0)["path"] == 1
+    assert binding.gemv_query_launch_ex(16, 65536, 1, GB300_SMS, 0)["path"] == 0      # x too long for it
+    for bad in ["mcast=3", "unroll=2", "streamk=2", "foo=1", "mcast", "mcast=", "mcast=2,,x=1"]:
+        monkeypatch.setenv("GEMV_FORCE_VARIANT", bad)
+        info = binding.gemv_launch_info()
+        assert L.gemv_query_launch(4096, 14336, 1, GB300_SMS, ctypes.byref(info)) == binding.GEMV_ERR_INVALID, bad

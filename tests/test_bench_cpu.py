@@ -1,14 +1,13 @@
 """Host-side logic of bench.py and the workload definitions, on the CPU: the
-JSON contract of the reference arm, the byte accounting of the decode step and
-the multi-rank combination (world size 2 over gloo)."""
+JSON contract of the reference arm, the byte accounting of the decode step,
+the split of the timed steps into CUDA graphs, and the refusal of multi-rank
+launches."""
 import json
 import os
-import socket
 import subprocess
 import sys
 
 import pytest
-import torch.multiprocessing as mp
 
 import bench
 from memory_bound_decode_gb300 import workloads
@@ -92,32 +91,40 @@ def test_clock_sampler_without_nvidia_smi(monkeypatch):
     assert info["samples"] == 0 and info["sm_mhz"] is None
 
 
-def _free_port():
-    with socket.socket() as s:
-        s.bind(("127.0.0.1", 0))
-        return s.getsockname()[1]
+def test_multi_rank_launch_exits_before_cuda():
+    """The path runs on one GPU: a multi-rank launch (WORLD_SIZE > 1, as
+    torchrun sets it) or --gpus > 1 stops with an error before torch or the
+    library is imported."""
+    code = ("import os, sys; sys.path.insert(0, %r); import bench; rc = bench.main(%s); "
+            "print(rc, 'torch' in sys.modules, 'memory_bound_decode_gb300.binding' in sys.modules)")
+    for env, argv in [({"WORLD_SIZE": "2", "RANK": "0"}, "[]"), ({"WORLD_SIZE": "2", "RANK": "1"}, "[]"),
+                      ({}, "['--gpus', '2']")]:
+        out = subprocess.run([sys.executable, "-c", code % (ROOT, argv)], capture_output=True, text=True,
+                             timeout=120, cwd=ROOT, env=dict(os.environ, **env))
+        assert out.returncode == 0, out.stderr
+        assert out.stdout.split() == ["2", "False", "False"], out.stdout
+        assert "one GPU only" in out.stderr
+    # the same through the script's own exit status
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "1"], capture_output=True,
+                         text=True, timeout=120, cwd=ROOT, env=dict(os.environ, WORLD_SIZE="2"))
+    assert out.returncode != 0 and "one GPU only" in out.stderr
 
 
-def _rank_main(rank, world, port, q):
-    import torch.distributed as dist
-    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
-                            world_size=world)
-    got = bench.max_over_ranks(1.5 + rank, dist, "cpu")
-    dist.barrier()
-    dist.destroy_process_group()
-    q.put((rank, got))
+@pytest.mark.parametrize("steps", [1, 3, 4, 5, 20, 255, 256, 257, 1000, 20000])
+@pytest.mark.parametrize("copies", [1, 2, 4, 7])
+def test_graph_partition(steps, copies):
+    a, q, r = bench.graph_partition(steps, copies, 256)
+    assert q * a + r == steps and 0 <= r
+    assert a % copies == 0 and a <= max(256, copies)
+    if q:
+        assert r < a
+    seq = [i % copies for _ in range(q) for i in range(a)] + [i % copies for i in range(r)]
+    assert len(seq) == steps
+    if copies > 1:
+        assert all(u != v for u, v in zip(seq, seq[1:]))
 
 
-def test_max_over_ranks_gloo_world2():
-    ctx = mp.get_context("spawn")
-    q = ctx.Queue()
-    port = _free_port()
-    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
-    for p in procs:
-        p.start()
-    res = dict(q.get(timeout=120) for _ in procs)
-    for p in procs:
-        p.join(timeout=60)
-        assert p.exitcode == 0
-    assert res == {0: 2.5, 1: 2.5}
-    assert bench.max_over_ranks(3.0, None, "cpu") == 3.0
+def test_no_collective_in_bench():
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    for word in ("init_process_group", "torch.distributed", "all_reduce"):
+        assert word not in src

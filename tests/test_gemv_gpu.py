@@ -74,6 +74,26 @@ def test_parity_skinny_batch(N, K, B):
     gu.assert_parity(y, y_ref, s, f"B={B}")
 
 
+@pytest.mark.parametrize("B", [2, 3, 4, 8, 16])
+@pytest.mark.parametrize("N,K", [(4096, 14336), (1000, 4096), (33, 65537)])
+def test_tensor_core_wide_dynamic_range(N, K, B):
+    """The batch 2..16 path runs on the tensor cores, whose internal addition
+    order and rounding the PTX ISA leaves open. Rows mixing columns scaled by
+    1e4 and by 1e-4 (and weight rows scaled by 1e3 or 1e-3) put products of
+    very different magnitude into one dot product; every element must still be
+    within 1e-5 of the sum of the products' magnitudes."""
+    W, x, ldw = make(N, K, B, seed=N + K + 7 * B)
+    g = inputs.generator(N + K, 5, DEV)
+    col = torch.where(torch.rand(K, generator=g, device=DEV) < 0.5, 1e4, 1e-4)
+    row = torch.where(torch.rand(N, generator=g, device=DEV) < 0.5, 1e3, 1e-3)
+    x = (x.float() * col[None, :]).to(torch.bfloat16)
+    W2 = W.clone()
+    W2[:, :K] = (W[:, :K].float() * row[:, None]).to(torch.bfloat16)
+    y = gu.gemv(W2, x, K)
+    y_ref, s = gu.reference(W2, x, K)
+    gu.assert_parity(y, y_ref, s, f"dynamic range N={N} K={K} B={B}")
+
+
 @pytest.mark.parametrize("N,K,B", [(7, 129, 1), (4097, 4103, 3), (33, 65537, 1), (1, 8191, 16),
                                    (128256, 4096, 1), (4096, 14336, 16)])
 def test_integer_inputs_are_exact(N, K, B):
