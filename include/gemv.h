@@ -285,6 +285,21 @@ int gemv_plan_launch_host_io(gemv_plan *plan, const void *x_host, void *x_dev, i
 /* Number of kernel launches one gemv_plan_launch performs (after fusion). */
 int gemv_plan_num_launches(const gemv_plan *plan);
 
+/*
+ * 1 if the plan's launches are independent, 0 if not (or plan is NULL).
+ * gemv_plan_create compares the device byte ranges every projection reads (x,
+ * W, the scales) and writes (y): when no launch writes memory that another
+ * launch of the plan reads or writes, and no launch uses the stream-K option
+ * (whose launches share the plan's workspace), the launches do not wait for
+ * the preceding grid before they touch x and y, so each one's start overlaps
+ * its predecessor's end ("GPU performance chains", "Launch gaps in a decode
+ * step"). The graph as a whole still starts after the work before it on the
+ * stream and ends before the work after it. A plan with any such overlap keeps
+ * every wait. Setting GEMV_FORCE_VARIANT=planwait=1 before gemv_plan_create
+ * keeps the waits in any plan, for comparison.
+ */
+int gemv_plan_independent(const gemv_plan *plan);
+
 /* Release a plan and its graph. NULL is ignored. Not while a launch runs. */
 void gemv_plan_destroy(gemv_plan *plan);
 

@@ -40,7 +40,8 @@ EXPORTED = [
     "gemv_bf16", "gemv_bf16_ex", "gemv_bf16_host_io", "gemv_bf16_multi", "gemv_bf16_multi_ex",
     "gemv_bf16_multi_host_io",
     "gemv_plan_create", "gemv_plan_capture",
-    "gemv_plan_launch", "gemv_plan_launch_host_io", "gemv_plan_num_launches", "gemv_plan_destroy",
+    "gemv_plan_launch", "gemv_plan_launch_host_io", "gemv_plan_num_launches", "gemv_plan_independent",
+    "gemv_plan_destroy",
     "gemv_query_launch", "gemv_query_launch_ex", "gemv_workspace_release", "gemv_device_status",
     "gemv_bf16_streamk_noalloc",
     "gemv_debug_write_count",
@@ -142,6 +143,7 @@ def _load(path: str) -> ctypes.CDLL:
                                           ctypes.POINTER(vp), i64, ctypes.c_int,
                                           ctypes.POINTER(gemv_options), vp]
     L.gemv_plan_num_launches.argtypes = [vp]
+    L.gemv_plan_independent.argtypes = [vp]
     L.gemv_plan_destroy.argtypes = [vp]
     L.gemv_plan_destroy.restype = None
     L.gemv_query_launch.argtypes = [i64, i64, ctypes.c_int, ctypes.c_int,
@@ -393,6 +395,10 @@ class Plan:
 
     def num_launches(self) -> int:
         return lib().gemv_plan_num_launches(self._h)
+
+    def independent(self) -> bool:
+        """Whether the plan's launches run without waiting for each other (see gemv.h)."""
+        return bool(lib().gemv_plan_independent(self._h))
 
     def destroy(self) -> None:
         if self._h is not None and self._h.value:

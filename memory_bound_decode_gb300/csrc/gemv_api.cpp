@@ -447,7 +447,55 @@ struct gemv_plan {
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
     Workspace ws;   // stream-K launches of this plan (run one after another)
+    bool independent = false;   // launches skip the wait for the preceding grid
 };
+
+namespace {
+
+// Byte range [lo, hi) of device memory one projection reads or writes.
+struct Extent {
+    uintptr_t lo, hi;
+    size_t launch;
+};
+
+bool overlap(const Extent& a, const Extent& b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// Whether no launch of the plan writes memory that another of its launches
+// reads or writes: then none depends on another, and each may start its work
+// without waiting for the preceding grid ("GPU performance chains", "Launch
+// gaps in a decode step": the gap between dependent kernels is the cost; an
+// independent kernel has none to pay). launch_of[q] is the launch projection
+// q belongs to. Stream-K launches share the plan's workspace, so a plan with
+// one is never independent.
+bool plan_is_independent(const gemv_proj* projs, int nproj, const std::vector<size_t>& launch_of,
+                         const std::vector<Prepared>& launches) {
+    for (const Prepared& pr : launches)
+        if (pr.sk) return false;
+    std::vector<Extent> reads, writes;
+    auto ext = [](const void* p, int64_t bytes, size_t l) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+        return Extent{a, a + static_cast<uintptr_t>(bytes), l};
+    };
+    for (int i = 0; i < nproj; ++i) {
+        const gemv_proj& q = projs[i];
+        const size_t l = launch_of[static_cast<size_t>(i)];
+        reads.push_back(ext(q.x, static_cast<int64_t>(q.B) * q.K * 2, l));
+        const int64_t wbytes = q.weight_kind == GEMV_WEIGHT_BF16 ? q.N * q.ldw * 2 : q.N * q.ldw;
+        reads.push_back(ext(q.W, wbytes, l));
+        if (q.weight_kind == GEMV_WEIGHT_INT4) reads.push_back(ext(q.S, q.N * q.lds * 2, l));
+        if (q.weight_kind == GEMV_WEIGHT_FP8) reads.push_back(ext(q.S, q.N * 4, l));
+        writes.push_back(ext(q.y, static_cast<int64_t>(q.B) * q.N * 4, l));
+    }
+    for (const Extent& w : writes) {
+        for (const Extent& r : reads)
+            if (r.launch != w.launch && overlap(w, r)) return false;
+        for (const Extent& v : writes)
+            if (v.launch != w.launch && overlap(w, v)) return false;
+    }
+    return true;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -585,7 +633,9 @@ int gemv_plan_create(const gemv_proj* projs, int nproj, gemv_plan** out) {
 
     gemv_plan* plan = new (std::nothrow) gemv_plan;
     if (!plan) return GEMV_ERR_NOMEM;
+    std::vector<size_t> launch_of;
     try {
+        launch_of.resize(static_cast<size_t>(nproj));
         int i = 0;
         while (i < nproj) {
             const gemv_proj& a = projs[i];
@@ -615,13 +665,17 @@ int gemv_plan_create(const gemv_proj* projs, int nproj, gemv_plan** out) {
                 delete plan;
                 return rc;
             }
+            for (int q = i; q < j; ++q) launch_of[static_cast<size_t>(q)] = plan->launches.size();
             plan->launches.push_back(pr);
             i = j;
         }
+        plan->independent = !gemv::plan_force_wait() && plan_is_independent(projs, nproj, launch_of, plan->launches);
     } catch (const std::bad_alloc&) {
         delete plan;
         return GEMV_ERR_NOMEM;
     }
+    if (plan->independent)
+        for (Prepared& pr : plan->launches) pr.p.flags |= gemv::kFlagNoWait;
     int64_t need_part = 0, need_tickets = 0;
     for (const Prepared& pr : plan->launches) {
         if (!pr.sk) continue;
@@ -704,6 +758,8 @@ int gemv_plan_launch_host_io(gemv_plan* plan, const void* x_host, void* x_dev, i
 int gemv_plan_num_launches(const gemv_plan* plan) {
     return plan ? static_cast<int>(plan->launches.size()) : 0;
 }
+
+int gemv_plan_independent(const gemv_plan* plan) { return plan && plan->independent ? 1 : 0; }
 
 void gemv_plan_destroy(gemv_plan* plan) {
     if (!plan) return;

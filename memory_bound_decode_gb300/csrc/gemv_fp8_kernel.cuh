@@ -187,7 +187,7 @@ gemv_fp8_kernel(const __grid_constant__ Params p) {
     F8Range rg = f8_range(nslots, kw, kq);
     rg_begin = rg.j_begin;
     issue(ch.c0, 0, rg.my_slots);
-    pdl_wait_prerequisites();
+    if (!(p.flags & kFlagNoWait)) pdl_wait_prerequisites();
     stage_x(xs, xstride, p.x, B, K, ch.c0, ch.nv);
 
 #pragma unroll 1

@@ -48,7 +48,7 @@ struct Params {
     int32_t xstride;  // shared-memory elements per staged x row (>= kchunk)
     int32_t batch;    // B
     int32_t nbuf;     // x buffers (2 when the K-range takes more than one chunk)
-    int32_t flags;    // kFlagRmsNorm
+    int32_t flags;    // kFlagRmsNorm, kFlagNoWait
     float rms_eps;    // epsilon of the RMSNorm prologue
     int32_t mcast;    // CUDA-core kernel, batch 1, one K chunk, no K split: CTAs of a cluster along
                       // the rows that share one multicast copy of x (1: every CTA stages its own)
@@ -69,6 +69,12 @@ constexpr int kMcastMinVectors = 1024;
 // Scale each output row b by (mean_k x[b][k]^2 + rms_eps)^(-1/2) (RMSNorm
 // prologue; the norm's elementwise weight is folded into W).
 constexpr int32_t kFlagRmsNorm = 1;
+// Skip the wait for the preceding grid (programmatic dependent launch): set
+// only on the launches of a plan none of whose launches writes memory that
+// another of its launches reads or writes, so that neighbouring launches may
+// run at the same time (the graph as a whole still starts after, and ends
+// before, the stream work around it).
+constexpr int32_t kFlagNoWait = 2;
 
 // Shared floats after the partial sums: per-warp sums of squares of x
 // [kWarps][kMaxBatch], the CTA's sums [kMaxBatch], the row scales [kMaxBatch]
@@ -132,6 +138,11 @@ struct Launch {
     int32_t nbuf;
     int32_t mcast;     // CTAs sharing one multicast copy of x (cluster along the rows); 1: none
 };
+
+// Sweep knob of the planner (GEMV_FORCE_VARIANT planwait=1): every launch of
+// a plan waits for the preceding grid even when the plan's launches are
+// independent.
+bool plan_force_wait();
 
 // Returns 0 and fills `out`, or a negative GEMV_ERR_* code.
 int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind = kWeightBf16);

@@ -189,7 +189,7 @@ gemv_bf16_kernel(const __grid_constant__ Params p) {
 #pragma unroll
     for (int r = 0; r < RPW; ++r) wp[r] = wrow[r] + ch.c0 + 8 * static_cast<int64_t>(v0);
     issue_batch<RPW, UJ, true>(wv, ok, wp, v0, rg.my_steps, ch.nv, ch.nfull, ch.tail_m);
-    pdl_wait_prerequisites();
+    if (!(p.flags & kFlagNoWait)) pdl_wait_prerequisites();
     if constexpr (mcast) {
         // Every CTA of the cluster has initialised its mbarrier; rank 0 copies
         // the whole vectors of x into all of them (pieces of at most 32 KB);

@@ -192,7 +192,7 @@ gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
     const uint16_t* p0 = w0row + ch.c0 + 8 * static_cast<int64_t>(v);
     const uint16_t* p1 = w1row + ch.c0 + 8 * static_cast<int64_t>(v);
     mma_issue<UJ, true>(w0, w1, ok, p0, p1, v, rg.my_blocks, ch);
-    pdl_wait_prerequisites();
+    if (!(p.flags & kFlagNoWait)) pdl_wait_prerequisites();
     stage_x_rows(xs, xstride, p.x, B, K, ch.c0, ch.nv);
 
 #pragma unroll 1

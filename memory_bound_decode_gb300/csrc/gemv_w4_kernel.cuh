@@ -214,7 +214,7 @@ gemv_w4_kernel(const __grid_constant__ Params p) {
     W4Range rg = w4_range(ngroups, kw, kq);
     rg_begin = rg.j_begin;
     issue(ch.c0, 0, rg.my_groups);
-    pdl_wait_prerequisites();
+    if (!(p.flags & kFlagNoWait)) pdl_wait_prerequisites();
     stage_x<true>(xs, xstride, p.x, B, K, ch.c0, ch.nv);
 
 #pragma unroll 1

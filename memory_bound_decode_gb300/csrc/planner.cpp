@@ -26,7 +26,9 @@
 //                               instance applies), unroll=<4|8> (INT4 / FP8:
 //                               the standard or the deep instance, where the
 //                               deep one applies), streamk=<0|1> (batch-1 BF16
-//                               calls: the stream-K kernel or not).
+//                               calls: the stream-K kernel or not), planwait=1
+//                               (every launch of a plan waits for the
+//                               preceding grid, even in an independent plan).
 // A value the planner cannot use makes every plan fail with GEMV_ERR_INVALID,
 // so that a mistyped sweep stops instead of timing the default.
 #include <cstdint>
@@ -45,6 +47,7 @@ struct Overrides {
     int mcast = 0;             // 0: the rules decide
     int unroll = 0;            // 0: the rules decide
     int streamk = -1;          // -1: the rules decide
+    int planwait = 0;          // 1: plans keep every wait for the preceding grid
     bool bad = false;
 };
 
@@ -88,6 +91,8 @@ Overrides read_overrides() {
                 o.unroll = static_cast<int>(v);
             } else if (num && klen == 7 && std::strncmp(p, "streamk", 7) == 0 && (v == 0 || v == 1)) {
                 o.streamk = static_cast<int>(v);
+            } else if (num && klen == 8 && std::strncmp(p, "planwait", 8) == 0 && (v == 0 || v == 1)) {
+                o.planwait = static_cast<int>(v);
             } else {
                 o.bad = true;
                 break;
@@ -339,6 +344,11 @@ int plan_streamk(int64_t rows, int64_t K, int B, int sm_count, SkLaunch* out) {
     out->part_floats = 2 * (warps > 0 ? warps : 1);
     out->tickets = rows - rounds * grid_warps > 0 ? rows - rounds * grid_warps : 1;
     return GEMV_OK;
+}
+
+bool plan_force_wait() {
+    const Overrides ov = read_overrides();
+    return !ov.bad && ov.planwait == 1;
 }
 
 // The default grid measured faster than the stream-K grid on every decode

@@ -178,3 +178,71 @@ def test_multi_host_io_matches_device_call():
                                            check=False) == binding.GEMV_ERR_INVALID
     assert binding.gemv_bf16_multi_host_io(segs, None, x_dev, y_host, K, 1,
                                            check=False) == binding.GEMV_ERR_INVALID
+
+
+def test_plan_independence_and_ordering(monkeypatch):
+    """A plan whose launches touch disjoint outputs runs them without waiting
+    for each other; a plan where one launch writes what another reads or
+    writes keeps every wait, and its launches take effect in list order."""
+    N, K = 4096, 4096
+    W1 = inputs.weight(N, K, seed=30, device=DEV)
+    W2 = inputs.weight(N, K, seed=31, device=DEV)
+    x1 = inputs.activations(1, K, seed=30, index=5, device=DEV)
+    x2 = inputs.activations(1, K, seed=31, index=5, device=DEV)
+    ya = torch.empty((1, N), device=DEV)
+    yb = torch.empty((1, N), device=DEV)
+    s = torch.cuda.Stream()
+
+    # disjoint: independent, both results right
+    p = binding.Plan([(W1, x1, ya, N, K, K, 1, 0), (W2, x2, yb, N, K, K, 1, 0)])
+    assert p.independent()
+    p.capture(s)
+    ya.fill_(float("nan"))
+    yb.fill_(float("nan"))
+    torch.cuda.synchronize()
+    p.launch(s)
+    s.synchronize()
+    for W, x, y in ((W1, x1, ya), (W2, x2, yb)):
+        y_ref, sc = gu.reference(W, x, K)
+        gu.assert_parity(y.cpu().numpy(), y_ref, sc, "independent plan")
+    p.destroy()
+
+    # the same y written twice: dependent; the later launch's result stays
+    p = binding.Plan([(W1, x1, ya, N, K, K, 1, 0), (W2, x2, ya, N, K, K, 1, 0)])
+    assert not p.independent()
+    p.capture(s)
+    for _ in range(3):
+        ya.fill_(float("nan"))
+        torch.cuda.synchronize()
+        p.launch(s)
+        s.synchronize()
+        y_ref, sc = gu.reference(W2, x2, K)
+        gu.assert_parity(ya.cpu().numpy(), y_ref, sc, "write after write")
+    p.destroy()
+
+    # a launch whose output overlaps a later launch's x, or its weights
+    buf = torch.empty(N, device=DEV)
+    xs = buf.view(torch.bfloat16)[:K].view(1, K)
+    p = binding.Plan([(W1, x1, buf.view(1, N), N, K, K, 1, 0), (W2, xs, yb, N, K, K, 1, 0)])
+    assert not p.independent()
+    p.destroy()
+    Wbuf = torch.empty((N, K), dtype=torch.bfloat16, device=DEV)
+    p = binding.Plan([(W1, x1, Wbuf.view(-1).view(torch.float32)[:N].view(1, N), N, K, K, 1, 0),
+                      (Wbuf, x2, yb, N, K, K, 1, 0)])
+    assert not p.independent()
+    p.destroy()
+
+    # the sweep knob keeps the waits in an independent plan
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", "planwait=1")
+    p = binding.Plan([(W1, x1, ya, N, K, K, 1, 0), (W2, x2, yb, N, K, K, 1, 0)])
+    assert not p.independent()
+    p.destroy()
+    monkeypatch.delenv("GEMV_FORCE_VARIANT")
+
+    # the decode step's projections are independent (each reads its own x)
+    spec = workloads.decode_step_spec(layers=2, hidden=512, intermediate=1536, vocab=2000, q_rows=512, kv_rows=128)
+    step = workloads.DecodeStep(spec, seed=32, device=DEV)
+    plan = step.plan()
+    assert plan.independent()
+    assert not step.plan(streamk=True).independent()   # stream-K launches share a workspace
+    plan.destroy()
