@@ -950,6 +950,7 @@ int gemv_fp8_query_launch(int64_t N, int64_t K, int B, int sm_count, gemv_launch
 int gemv_w4_query_launch(int64_t N, int64_t K, int B, int sm_count, gemv_launch_info* out) {
     if (!out) return GEMV_ERR_INVALID;
     if (K < gemv::kW4Group || K % gemv::kW4Group != 0) return GEMV_ERR_INVALID;
+    std::memset(out, 0, sizeof *out);
     Launch l;
     int rc = gemv::plan_launch(N, K, B, sm_count, &l, gemv::kWeightInt4);
     if (rc != GEMV_OK) return rc;
