@@ -57,11 +57,73 @@ __device__ __forceinline__ void issue_batch(uint4 (&wv)[UJ][RPW], bool (&ok)[UJ]
     }
 }
 
+// Two FP32 values in one 64-bit register pair, for the packed multiply-add.
+__device__ __forceinline__ uint64_t pack_f32x2(uint32_t lo_bits, uint32_t hi_bits) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo_bits), "r"(hi_bits));
+    return r;
+}
+__device__ __forceinline__ float2 unpack_f32x2(uint64_t v) {
+    float2 f;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
+    return f;
+}
+// d = a * b + d on both halves (fma.rn.f32x2: one instruction, two FP32
+// multiply-adds, each rounded as an fmaf).
+__device__ __forceinline__ void fma_f32x2(uint64_t& d, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
 // Multiply-add one batch into the running sums. The batch is summed into a
 // fresh partial first (blocked summation), then added to acc.
+//
+// Batches of two or more rows of x use the packed FP32 multiply-add: the
+// BF16 pair of one 32-bit word (columns 2q and 2q + 1) widens into one
+// register pair, and one fma.rn.f32x2 adds both products into a pair of
+// partial sums (even columns, odd columns), halving the multiply-add
+// instructions. The two partials are added at the end of the batch, so the
+// rounding chain is shorter than the scalar one. Batch 1 keeps the scalar
+// form (its stream is HBM-bound; its results stay bit for bit as they were).
 template <int B, int RPW, int UJ, bool PRED>
 __device__ __forceinline__ void consume_batch(float (&acc)[RPW][B], const uint4 (&wv)[UJ][RPW],
                                               const bool (&ok)[UJ], const uint16_t* xl, int xstride) {
+    if constexpr (B >= 2) {
+        uint64_t t2[RPW][B];
+#pragma unroll
+        for (int r = 0; r < RPW; ++r)
+#pragma unroll
+            for (int b = 0; b < B; ++b) t2[r][b] = 0ull;   // (+0.0f, +0.0f)
+#pragma unroll
+        for (int u = 0; u < UJ; ++u) {
+            if (PRED && !ok[u]) continue;
+            uint64_t wp[RPW][4];
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) {
+                const uint32_t w[4] = {wv[u][r].x, wv[u][r].y, wv[u][r].z, wv[u][r].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) wp[r][q] = pack_f32x2(w[q] << 16, w[q] & 0xffff0000u);
+            }
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const uint4 xr = *reinterpret_cast<const uint4*>(xl + b * xstride + 256 * u);
+                const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint64_t xp = pack_f32x2(xw[q] << 16, xw[q] & 0xffff0000u);
+#pragma unroll
+                    for (int r = 0; r < RPW; ++r) fma_f32x2(t2[r][b], wp[r][q], xp);
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RPW; ++r)
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const float2 h = unpack_f32x2(t2[r][b]);
+                acc[r][b] += h.x + h.y;
+            }
+        return;
+    }
     float t[RPW][B];
 #pragma unroll
     for (int r = 0; r < RPW; ++r)
