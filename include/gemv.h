@@ -295,8 +295,15 @@ int gemv_plan_num_launches(const gemv_plan *plan);
  * its predecessor's end ("GPU performance chains", "Launch gaps in a decode
  * step"). The graph as a whole still starts after the work before it on the
  * stream and ends before the work after it. A plan with any such overlap keeps
- * every wait. Setting GEMV_FORCE_VARIANT=planwait=1 before gemv_plan_create
- * keeps the waits in any plan, for comparison.
+ * every wait. In an independent plan of two or more launches, the batch-1
+ * launches are also planned to run alongside their neighbours rather than to
+ * fill the GPU alone: each asks for one streaming warp per SM, so K is split
+ * only for very few rows, and the INT4 and FP8 kernels take their standard
+ * instance. Results stay within the same tolerance (partial sums combine in a
+ * fixed order either way; the bits may differ from a direct call of the same
+ * projection, which may split K). Setting GEMV_FORCE_VARIANT=planwait=1
+ * before gemv_plan_create keeps the waits (and the single-launch planning) in
+ * any plan, for comparison.
  */
 int gemv_plan_independent(const gemv_plan *plan);
 

@@ -8,6 +8,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <utility>
 #include <vector>
 
 #include <cuda_runtime.h>
@@ -218,7 +219,7 @@ int prepare_streamk(const gemv_segment* segs, int nsegs, int64_t total, const vo
 
 // Validate a group of segments sharing x, K, B and plan one launch over them.
 int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B, int flags, float eps,
-            int sm_count, Prepared* out) {
+            int sm_count, Prepared* out, bool overlap = false) {
     if (!segs || nsegs < 1 || nsegs > GEMV_MAX_SEGMENTS) return GEMV_ERR_INVALID;
     int rc = check_common(x, K, B);
     if (rc != GEMV_OK) return rc;
@@ -237,7 +238,7 @@ int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B
         return GEMV_OK;
     Launch l;
     const int kind = (flags & GEMV_FLAG_CUDA_CORES) ? gemv::kWeightBf16CudaCores : gemv::kWeightBf16;
-    if ((rc = gemv::plan_launch(total, K, B, sm_count, &l, kind)) != GEMV_OK) return rc;
+    if ((rc = gemv::plan_launch(total, K, B, sm_count, &l, kind, overlap)) != GEMV_OK) return rc;
 
     Params p;
     std::memset(&p, 0, sizeof p);
@@ -288,7 +289,7 @@ struct QSeg {
 // Plan one launch over INT4 (kind gemv::kWeightInt4) or FP8 (gemv::kWeightFp8)
 // segments sharing x, K and B.
 int prepare_quant(int kind, const QSeg* segs, int nsegs, const void* x, int64_t K, int B, int flags, float eps,
-                  int sm_count, Prepared* out) {
+                  int sm_count, Prepared* out, bool overlap = false) {
     if (nsegs < 1 || nsegs > GEMV_MAX_SEGMENTS) return GEMV_ERR_INVALID;
     int64_t total = 0;
     for (int i = 0; i < nsegs; ++i) {
@@ -296,7 +297,7 @@ int prepare_quant(int kind, const QSeg* segs, int nsegs, const void* x, int64_t 
         if (total > 0x7fffffffLL) return GEMV_ERR_INVALID;
     }
     Launch l;
-    int rc = gemv::plan_launch(total, K, B, sm_count, &l, kind);
+    int rc = gemv::plan_launch(total, K, B, sm_count, &l, kind, overlap);
     if (rc != GEMV_OK) return rc;
     Params p;
     std::memset(&p, 0, sizeof p);
@@ -465,12 +466,9 @@ bool overlap(const Extent& a, const Extent& b) { return a.lo < b.hi && b.lo < a.
 // without waiting for the preceding grid ("GPU performance chains", "Launch
 // gaps in a decode step": the gap between dependent kernels is the cost; an
 // independent kernel has none to pay). launch_of[q] is the launch projection
-// q belongs to. Stream-K launches share the plan's workspace, so a plan with
-// one is never independent.
-bool plan_is_independent(const gemv_proj* projs, int nproj, const std::vector<size_t>& launch_of,
-                         const std::vector<Prepared>& launches) {
-    for (const Prepared& pr : launches)
-        if (pr.sk) return false;
+// q belongs to. (Stream-K launches also share the plan's workspace; the
+// caller checks for them.)
+bool plan_is_independent(const gemv_proj* projs, int nproj, const std::vector<size_t>& launch_of) {
     std::vector<Extent> reads, writes;
     auto ext = [](const void* p, int64_t bytes, size_t l) {
         const uintptr_t a = reinterpret_cast<uintptr_t>(p);
@@ -633,11 +631,12 @@ int gemv_plan_create(const gemv_proj* projs, int nproj, gemv_plan** out) {
 
     gemv_plan* plan = new (std::nothrow) gemv_plan;
     if (!plan) return GEMV_ERR_NOMEM;
-    std::vector<size_t> launch_of;
     try {
-        launch_of.resize(static_cast<size_t>(nproj));
-        int i = 0;
-        while (i < nproj) {
+        // Launches: runs of adjacent projections of one fuse group with the
+        // same x, K, B, options and weight kind (at most GEMV_MAX_SEGMENTS).
+        std::vector<std::pair<int, int>> groups;
+        std::vector<size_t> launch_of(static_cast<size_t>(nproj));
+        for (int i = 0; i < nproj;) {
             const gemv_proj& a = projs[i];
             int j = i + 1;
             if (a.fuse_group > 0) {
@@ -647,29 +646,56 @@ int gemv_plan_create(const gemv_proj* projs, int nproj, gemv_plan** out) {
                        projs[j].weight_kind == a.weight_kind)
                     ++j;
             }
-            Prepared pr;
-            const float eps = (a.flags & GEMV_FLAG_RMSNORM) ? a.rms_eps : 0.f;
-            if (a.weight_kind == GEMV_WEIGHT_BF16) {
-                gemv_segment segs[GEMV_MAX_SEGMENTS];
-                for (int q = i; q < j; ++q)
-                    segs[q - i] = gemv_segment{projs[q].W, projs[q].y, projs[q].N, projs[q].ldw};
-                rc = prepare(segs, j - i, a.x, a.K, a.B, a.flags, eps, sm_count, &pr);
-            } else {
-                QSeg segs[GEMV_MAX_SEGMENTS];
-                for (int q = i; q < j; ++q)
-                    segs[q - i] = QSeg{projs[q].W, projs[q].S, projs[q].y, projs[q].N, projs[q].ldw, projs[q].lds};
-                rc = prepare_quant(a.weight_kind == GEMV_WEIGHT_INT4 ? gemv::kWeightInt4 : gemv::kWeightFp8, segs,
-                                   j - i, a.x, a.K, a.B, a.flags, eps, sm_count, &pr);
-            }
-            if (rc != GEMV_OK) {
-                delete plan;
-                return rc;
-            }
-            for (int q = i; q < j; ++q) launch_of[static_cast<size_t>(q)] = plan->launches.size();
-            plan->launches.push_back(pr);
+            for (int q = i; q < j; ++q) launch_of[static_cast<size_t>(q)] = groups.size();
+            groups.emplace_back(i, j);
             i = j;
         }
-        plan->independent = !gemv::plan_force_wait() && plan_is_independent(projs, nproj, launch_of, plan->launches);
+        bool independent = !gemv::plan_force_wait() && plan_is_independent(projs, nproj, launch_of);
+        for (int q = 0; q < nproj && independent; ++q)
+            if (projs[q].flags & GEMV_FLAG_STREAMK) independent = false;
+
+        // Plan every launch; with overlap, as a member of an independent plan
+        // of several launches (gemv::plan_launch).
+        auto build = [&](bool overlap) -> int {
+            plan->launches.clear();
+            for (const auto& grp : groups) {
+                const int i = grp.first, j = grp.second;
+                const gemv_proj& a = projs[i];
+                Prepared pr;
+                const float eps = (a.flags & GEMV_FLAG_RMSNORM) ? a.rms_eps : 0.f;
+                int r;
+                if (a.weight_kind == GEMV_WEIGHT_BF16) {
+                    gemv_segment segs[GEMV_MAX_SEGMENTS];
+                    for (int q = i; q < j; ++q)
+                        segs[q - i] = gemv_segment{projs[q].W, projs[q].y, projs[q].N, projs[q].ldw};
+                    r = prepare(segs, j - i, a.x, a.K, a.B, a.flags, eps, sm_count, &pr, overlap);
+                } else {
+                    QSeg segs[GEMV_MAX_SEGMENTS];
+                    for (int q = i; q < j; ++q)
+                        segs[q - i] = QSeg{projs[q].W, projs[q].S, projs[q].y, projs[q].N, projs[q].ldw, projs[q].lds};
+                    r = prepare_quant(a.weight_kind == GEMV_WEIGHT_INT4 ? gemv::kWeightInt4 : gemv::kWeightFp8, segs,
+                                      j - i, a.x, a.K, a.B, a.flags, eps, sm_count, &pr, overlap);
+                }
+                if (r != GEMV_OK) return r;
+                plan->launches.push_back(pr);
+            }
+            return GEMV_OK;
+        };
+        const bool overlap = independent && groups.size() >= 2;
+        rc = build(overlap);
+        // A launch the planner sent to the stream-K kernel (its sweep knob)
+        // shares the plan's workspace: then every launch waits, planned alone.
+        bool any_sk = false;
+        for (const Prepared& pr : plan->launches) any_sk = any_sk || pr.sk;
+        if (rc == GEMV_OK && any_sk) {
+            independent = false;
+            if (overlap) rc = build(false);
+        }
+        if (rc != GEMV_OK) {
+            delete plan;
+            return rc;
+        }
+        plan->independent = independent;
     } catch (const std::bad_alloc&) {
         delete plan;
         return GEMV_ERR_NOMEM;

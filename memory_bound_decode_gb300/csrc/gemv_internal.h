@@ -145,7 +145,10 @@ struct Launch {
 bool plan_force_wait();
 
 // Returns 0 and fills `out`, or a negative GEMV_ERR_* code.
-int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind = kWeightBf16);
+// overlap: the launch belongs to an independent plan of several launches
+// (see gemv_plan_create), whose neighbours run alongside it.
+int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind = kWeightBf16,
+                bool overlap = false);
 
 // Stream-K launch (batch 1): the grid is one wave of GW warps. Rows (of all
 // segments, numbered consecutively) that fill whole rounds of GW are taken

@@ -122,34 +122,34 @@ __device__ __forceinline__ void consume_batch(float (&acc)[RPW][B], const uint4 
                 const float2 h = unpack_f32x2(t2[r][b]);
                 acc[r][b] += h.x + h.y;
             }
-        return;
-    }
-    float t[RPW][B];
+    } else {
+        float t[RPW][B];
 #pragma unroll
-    for (int r = 0; r < RPW; ++r)
+        for (int r = 0; r < RPW; ++r)
 #pragma unroll
-        for (int b = 0; b < B; ++b) t[r][b] = 0.f;
+            for (int b = 0; b < B; ++b) t[r][b] = 0.f;
 #pragma unroll
-    for (int u = 0; u < UJ; ++u) {
-        if (PRED && !ok[u]) continue;
-        float wf[RPW][8];
+        for (int u = 0; u < UJ; ++u) {
+            if (PRED && !ok[u]) continue;
+            float wf[RPW][8];
 #pragma unroll
-        for (int r = 0; r < RPW; ++r) unpack8(wv[u][r], wf[r]);
+            for (int r = 0; r < RPW; ++r) unpack8(wv[u][r], wf[r]);
 #pragma unroll
-        for (int b = 0; b < B; ++b) {
-            const uint4 xr = *reinterpret_cast<const uint4*>(xl + b * xstride + 256 * u);
-            float xf[8];
-            unpack8(xr, xf);
+            for (int b = 0; b < B; ++b) {
+                const uint4 xr = *reinterpret_cast<const uint4*>(xl + b * xstride + 256 * u);
+                float xf[8];
+                unpack8(xr, xf);
 #pragma unroll
-            for (int r = 0; r < RPW; ++r)
+                for (int r = 0; r < RPW; ++r)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) t[r][b] = fmaf(wf[r][e], xf[e], t[r][b]);
+                    for (int e = 0; e < 8; ++e) t[r][b] = fmaf(wf[r][e], xf[e], t[r][b]);
+            }
         }
+#pragma unroll
+        for (int r = 0; r < RPW; ++r)
+#pragma unroll
+            for (int b = 0; b < B; ++b) acc[r][b] += t[r][b];
     }
-#pragma unroll
-    for (int r = 0; r < RPW; ++r)
-#pragma unroll
-        for (int b = 0; b < B; ++b) acc[r][b] += t[r][b];
 }
 
 // This warp's contiguous range of warp-steps (32 vectors each) within a chunk.
