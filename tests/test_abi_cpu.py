@@ -345,3 +345,26 @@ def test_force_variant(L, monkeypatch):
         monkeypatch.setenv("GEMV_FORCE_VARIANT", bad)
         info = binding.gemv_launch_info()
         assert L.gemv_query_launch(4096, 14336, 1, GB300_SMS, ctypes.byref(info)) == binding.GEMV_ERR_INVALID, bad
+
+
+def test_host_io_calls_reject_before_any_copy(L):
+    """The host-to-host entry points validate their arguments before touching
+    the device (checked here without a GPU)."""
+    seg = binding.gemv_segment(A16, A16, 8, 8)
+    segs = (binding.gemv_segment * 1)(seg)
+    yh = (ctypes.c_void_p * 1)(A16)
+    ynull = (ctypes.c_void_p * 1)(None)
+    # NULL host buffers, too many segments, a NULL segment destination
+    assert L.gemv_bf16_multi_host_io(segs, 1, None, A16, yh, 8, 1, None, None) == binding.GEMV_ERR_INVALID
+    assert L.gemv_bf16_multi_host_io(segs, 1, A16, A16, None, 8, 1, None, None) == binding.GEMV_ERR_INVALID
+    assert L.gemv_bf16_multi_host_io(segs, 1, A16, A16, ynull, 8, 1, None, None) == binding.GEMV_ERR_INVALID
+    assert L.gemv_bf16_multi_host_io(segs, 9, A16, A16, yh, 8, 1, None, None) == binding.GEMV_ERR_INVALID
+    # device-side arguments follow the gemv_bf16_multi rules
+    assert L.gemv_bf16_multi_host_io(segs, 1, A16, A16 + 1, yh, 8, 1, None, None) == binding.GEMV_ERR_ALIGN
+    assert L.gemv_bf16_multi_host_io(segs, 1, A16, A16, yh, 8, 17, None, None) == binding.GEMV_ERR_INVALID
+    # plans: a NULL plan, negative sizes
+    assert L.gemv_plan_launch_host_io(None, A16, A16, 16, A16, A16, 16, None) == binding.GEMV_ERR_INVALID
+    assert L.gemv_plan_independent(None) == 0
+    # the single-matrix host-io call
+    assert L.gemv_bf16_host_io(A16, None, A16, A16, A16, 8, 8, 1, 8, None, None) == binding.GEMV_ERR_INVALID
+    assert L.gemv_bf16_host_io(A16, A16, A16, A16, A16, 8, 8, 1, 12, None, None) == binding.GEMV_ERR_ALIGN
