@@ -254,6 +254,8 @@ int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B
     l.row_tiles = tiles;
     // The bulk copy reads x from a 16-byte boundary, and only from this GPU's memory.
     if (l.mcast > 1 && (!aligned(x, 16) || !on_current_device(x))) l.mcast = 1;
+    // The bulk copies of x read from a 16-byte boundary, and only from this GPU's memory.
+    if (l.xbulk && (!aligned(x, 16) || !on_current_device(x))) l.xbulk = 0;
     l.grid = l.mcast > 1 ? (tiles + l.mcast - 1) / l.mcast * l.mcast : tiles * l.splits;
     if (l.grid > 0x7fffffffLL) return GEMV_ERR_UNSUPPORTED;
     p.x = static_cast<const uint16_t*>(x);
@@ -1030,8 +1032,13 @@ int gemv_last_cuda_error(void) { return g_last_cuda_error; }
 int gemv_device_status(unsigned int* bits, int reset) {
     if (!bits) return GEMV_ERR_INVALID;
     *bits = 0;
-    cudaError_t e = gemv::read_fma_status(bits, reset != 0);
+    // Each kernel translation unit keeps its own status word.
+    unsigned int b1 = 0, b2 = 0, b3 = 0;
+    cudaError_t e = gemv::read_fma_status(&b1, reset != 0);
+    if (e == cudaSuccess) e = gemv::read_mma_status_nb1(&b2, reset != 0);
+    if (e == cudaSuccess) e = gemv::read_mma_status_nb2(&b3, reset != 0);
     if (e != cudaSuccess) return cuda_fail(e);
+    *bits = b1 | b2 | b3;
     return GEMV_OK;
 }
 

@@ -153,6 +153,14 @@ __device__ __forceinline__ void bulk_copy_multicast(void* dst, const void* src, 
                  :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)), "h"(mask) : "memory");
 }
 
+// Copy `bytes` (a multiple of 16, both addresses 16-byte aligned) from global
+// memory into this CTA's shared memory at `dst`, completing `bytes`
+// transactions on the mbarrier `bar` (the Tensor Memory Accelerator's 1-D copy).
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+}
+
 // 16-byte asynchronous global->shared copy of `nbytes` (2..16) bytes; the rest
 // of the 16 bytes is zero-filled. Both addresses 16-byte aligned.
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src, int nbytes) {

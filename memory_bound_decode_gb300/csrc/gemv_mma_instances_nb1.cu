@@ -9,4 +9,6 @@ cudaError_t launch_mma_nb1(const Params& p, const Launch& l, cudaStream_t s, boo
 
 cudaError_t prepare_mma_nb1() { return prepare_mma<1>(); }
 
+cudaError_t read_mma_status_nb1(unsigned int* bits, bool reset) { return read_mma_status(bits, reset); }
+
 }  // namespace gemv

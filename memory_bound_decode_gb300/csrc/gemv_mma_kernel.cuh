@@ -136,12 +136,29 @@ __device__ __forceinline__ void mma_consume(float (&acc)[NB][4], const uint4 (&w
 
 // CHUNKED: as for the CUDA-core kernel, a separate instance for K-ranges
 // staged in several chunks.
-template <int NB, int UJ, bool CHUNKED>
+// XB (one chunk; x 16-byte aligned, in this GPU's memory, K a multiple of 8):
+// x is copied into shared memory by the Tensor Memory Accelerator, one bulk
+// copy per x row issued by one thread and counted on an mbarrier, instead of
+// 16-byte asynchronous copies from every thread. Those copies queue behind
+// the first batch of W loads the warps have just issued; the bulk copies do
+// not, so x arrives while that batch is still landing.
+template <int NB, int UJ, bool CHUNKED, bool XB = false>
 __global__ void __launch_bounds__(kThreads)
 gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
 
     pdl_launch_dependents();
+
+    // The bulk copy's mbarrier sits in the 16 bytes before x; every thread
+    // must see it initialised before it waits on it.
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(smem_raw);
+    if constexpr (XB) {
+        if (threadIdx.x == 0) {
+            mbar_init(mbar, 1);
+            fence_mbar_init_cluster();
+        }
+        __syncthreads();
+    }
 
     const int S = p.splits;
     if (S > 1) cluster_arrive_relaxed();   // see combine_and_store
@@ -167,8 +184,8 @@ gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
 
     const int xstride = p.xstride;
     const int xbuf = B * xstride;
-    uint16_t* xs = reinterpret_cast<uint16_t*>(smem_raw);
-    float* red = reinterpret_cast<float*>(smem_raw + static_cast<size_t>(p.nbuf) * xbuf * 2);
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem_raw + kMmaSmemHead);
+    float* red = reinterpret_cast<float*>(smem_raw + kMmaSmemHead + static_cast<size_t>(p.nbuf) * xbuf * 2);
     float* cpart = red + rows_per_cta * (B + 1) * kw;
     float* misc = cpart + rows_per_cta * B + kMaxSplits;   // cpart: cluster slots, see combine_and_store
     const bool norm = (p.flags & kFlagRmsNorm) != 0;
@@ -193,7 +210,25 @@ gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
     const uint16_t* p1 = w1row + ch.c0 + 8 * static_cast<int64_t>(v);
     mma_issue<UJ, true>(w0, w1, ok, p0, p1, v, rg.my_blocks, ch);
     if (!(p.flags & kFlagNoWait)) pdl_wait_prerequisites();
-    stage_x_rows(xs, xstride, p.x, B, K, ch.c0, ch.nv);
+    bool x_ok = true;   // false when the wait for the bulk copy of x ran out
+    if constexpr (XB) {
+        // K % 8 == 0: the chunk is whole 16-byte vectors; rows b < B only.
+        const uint32_t row_bytes = 16u * static_cast<uint32_t>(ch.nv);
+        if (threadIdx.x == 0) {
+            mbar_arrive_expect_tx(mbar, row_bytes * static_cast<uint32_t>(B));
+            for (int b = 0; b < B; ++b) {
+                const unsigned char* src = reinterpret_cast<const unsigned char*>(p.x + static_cast<int64_t>(b) * K + ch.c0);
+                unsigned char* dst = reinterpret_cast<unsigned char*>(xs + static_cast<int64_t>(b) * xstride);
+                for (uint32_t off = 0; off < row_bytes; off += 32768u) {
+                    const uint32_t n = row_bytes - off < 32768u ? row_bytes - off : 32768u;
+                    bulk_copy(dst + off, src + off, n, mbar);
+                }
+            }
+        }
+        x_ok = mbar_wait_bounded(mbar, 0);
+    } else {
+        stage_x_rows(xs, xstride, p.x, B, K, ch.c0, ch.nv);
+    }
 
 #pragma unroll 1
     for (int c = 0;; ++c) {
@@ -205,10 +240,10 @@ gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
             nch = chunk_at(next_c0, k1, p.kchunk, K);
             stage_x_rows(xs + ((c + 1) & 1) * xbuf, xstride, p.x, B, K, nch.c0, nch.nv);
             cp_async_wait<1>();
-        } else {
+        } else if constexpr (!XB) {
             cp_async_wait<0>();
         }
-        __syncthreads();
+        if constexpr (!XB) __syncthreads();   // with XB the mbarrier wait made x visible
 
         mma_consume<NB, UJ, true>(acc, w0, w1, ok, xrow0, xstride, v, g, B);
         int j = UJ;
@@ -243,7 +278,8 @@ gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
     }
 
     // acc[nb] holds D[row g][b], D[row g][b+1], D[row g+8][b], D[row g+8][b+1]
-    // with b = 8*nb + 2t.
+    // with b = 8*nb + 2t. A CTA whose copy of x did not arrive in time stores
+    // NaN (and has set the status bit) rather than sums over an incomplete x.
     const int rl0 = gw * kMmaRows + g;
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
@@ -251,16 +287,22 @@ gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
         for (int i = 0; i < 4; ++i) {
             const int b = nb * 8 + 2 * t + (i & 1);
             const int rl = rl0 + ((i & 2) ? 8 : 0);
-            if (b < B) red[red_index(kq, rows_per_cta, rl, B, b)] = acc[nb][i];
+            if (b < B) red[red_index(kq, rows_per_cta, rl, B, b)] = x_ok ? acc[nb][i] : __uint_as_float(0x7fc00000u);
         }
     }
     combine_and_store(red, cpart, misc, rows_per_cta, B, kw, S, split, sg.tile_local * rows_per_cta, sg.N, sg.y,
                       norm, K, p.rms_eps, p.wc);
+    // After a timed-out wait the copy may still be in flight into this CTA's
+    // shared memory: wait for it once more (bounded) before leaving.
+    if constexpr (XB) {
+        if (!x_ok) mbar_wait_bounded(mbar, 0);
+    }
 }
 
 template <int NB>
 cudaError_t launch_mma(const Params& p, const Launch& l, cudaStream_t s, bool pdl) {
     if (l.nbuf > 1) return launch_kernel(gemv_bf16_mma_kernel<NB, kMmaUnroll, true>, p, l, s, pdl);
+    if (l.xbulk) return launch_kernel(gemv_bf16_mma_kernel<NB, kMmaUnroll, false, true>, p, l, s, pdl);
     return launch_kernel(gemv_bf16_mma_kernel<NB, kMmaUnroll, false>, p, l, s, pdl);
 }
 
@@ -269,8 +311,20 @@ cudaError_t prepare_mma() {
     cudaError_t e = cudaFuncSetAttribute(gemv_bf16_mma_kernel<NB, kMmaUnroll, true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
     if (e != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(gemv_bf16_mma_kernel<NB, kMmaUnroll, false, true>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem)) != cudaSuccess)
+        return e;
     return cudaFuncSetAttribute(gemv_bf16_mma_kernel<NB, kMmaUnroll, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+}
+
+// Status bits this translation unit's kernels recorded (bulk-copy waits that
+// ran out), cleared when `reset`.
+inline cudaError_t read_mma_status(unsigned int* bits, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(bits, g_device_status, sizeof(unsigned int));
+    if (e != cudaSuccess || !reset || *bits == 0) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_device_status, &zero, sizeof(unsigned int));
 }
 
 }  // namespace gemv

@@ -124,3 +124,29 @@ def test_multicast_only_from_device_memory_and_under_capture():
     torch.cuda.synchronize()
     assert np.array_equal(y.cpu().numpy().view(np.uint32), y_dev.view(np.uint32))
     assert binding.gemv_device_status(reset=True) == 0
+
+
+@pytest.mark.parametrize("B", [2, 5, 8, 16])
+@pytest.mark.parametrize("N,K", [(4096, 14336), (1000, 4096), (300, 12288)])
+def test_tensor_core_bulk_x_copy(N, K, B):
+    """Batches of 2..16 copy x into shared memory with bulk copies when x is
+    16-byte aligned device memory of this GPU and K is a multiple of 8; x in
+    pinned host memory takes the per-thread staging. Same bits either way,
+    both against the oracle, and no wait ran out."""
+    ldw = inputs.padded_ldw(K)
+    W = inputs.weight(N, K, ldw, seed=N + B, device=DEV)
+    x = inputs.activations(B, K, seed=K + B, device=DEV)
+
+    def run_b(xx):
+        buf, y = gu.guarded_y(B, N)
+        binding.gemv_bf16(W, xx, y, N, K, B, ldw)
+        torch.cuda.synchronize()
+        gu.check_guards(buf)
+        return y.cpu().numpy()
+
+    y_dev = run_b(x)
+    y_host = run_b(x.cpu().pin_memory())
+    assert np.array_equal(y_dev.view(np.uint32), y_host.view(np.uint32))
+    y_ref, sc = gu.reference(W, x, K)
+    gu.assert_parity(y_dev, y_ref, sc, f"bulk x N={N} K={K} B={B}")
+    assert binding.gemv_device_status(reset=True) == 0
