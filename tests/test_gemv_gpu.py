@@ -248,3 +248,34 @@ def test_host_io_pinned_and_pageable(pinned):
         y_host.fill_(float("nan"))
         binding.gemv_bf16_host_io(W, x_host, y_host, torch.empty_like(x), y_dev, N, K, B, ldw)
         gu.assert_parity(y_host.numpy(), y_ref, sc, f"pinned={pinned} repeat")
+
+
+@pytest.mark.parametrize("xkind", ["pinned", "pageable", "pinned_unaligned"])
+@pytest.mark.parametrize("N,K,B", [(4096, 14336, 1), (1000, 4096, 4), (4097, 4103, 3), (70000, 4096, 1)])
+def test_host_io_matches_device_call(N, K, B, xkind):
+    """gemv_bf16_host_io (host x in, GEMV, host y out, synchronized) gives the
+    bits of the device-resident call on the same inputs, whichever way x comes
+    in (a copy kernel from 16-byte aligned mapped pinned memory, else a DMA
+    copy) and y goes out (stored straight into mapped memory up to 256 KB, else
+    copied back)."""
+    W, x, ldw = make(N, K, B, seed=N + K)
+    y_ref = torch.empty((B, N), device=DEV)
+    binding.gemv_bf16(W, x, y_ref, N, K, B, ldw)
+    if xkind == "pinned":
+        xh = x.cpu().pin_memory()
+    elif xkind == "pageable":
+        xh = x.cpu()
+    else:
+        raw = torch.empty(B * K + 1, dtype=torch.bfloat16).pin_memory()
+        raw[1:] = x.cpu().reshape(-1)
+        xh = raw[1:].view(B, K)           # 2 bytes past a 16-byte boundary
+    yh = torch.full((B, N), float("nan")).pin_memory()
+    x_dev = torch.empty_like(x)
+    y_dev = torch.empty((B, N), device=DEV)
+    s = torch.cuda.Stream()
+    for _ in range(2):                    # twice in a row: the same bits
+        yh.fill_(float("nan"))
+        binding.gemv_bf16_host_io(W, xh, yh, x_dev, y_dev, N, K, B, ldw, stream=s)
+        assert torch.equal(yh.view(torch.int32), y_ref.cpu().view(torch.int32))
+    y_o, sc = gu.reference(W, x, K)
+    gu.assert_parity(yh.numpy(), y_o, sc, f"host io {xkind}")
