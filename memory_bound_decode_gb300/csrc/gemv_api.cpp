@@ -321,6 +321,8 @@ int prepare_quant(int kind, const QSeg* segs, int nsegs, const void* x, int64_t 
     l.row_tiles = tiles;
     l.grid = tiles * l.splits;
     if (l.grid > 0x7fffffffLL) return GEMV_ERR_UNSUPPORTED;
+    // The bulk copies of x read from a 16-byte boundary, and only from this GPU's memory.
+    if (l.xbulk && (!aligned(x, 16) || !on_current_device(x))) l.xbulk = 0;
     p.x = static_cast<const uint16_t*>(x);
     p.K = K;
     p.kslice = l.kslice;
@@ -1033,12 +1035,13 @@ int gemv_device_status(unsigned int* bits, int reset) {
     if (!bits) return GEMV_ERR_INVALID;
     *bits = 0;
     // Each kernel translation unit keeps its own status word.
-    unsigned int b1 = 0, b2 = 0, b3 = 0;
+    unsigned int b1 = 0, b2 = 0, b3 = 0, b4 = 0;
     cudaError_t e = gemv::read_fma_status(&b1, reset != 0);
     if (e == cudaSuccess) e = gemv::read_mma_status_nb1(&b2, reset != 0);
     if (e == cudaSuccess) e = gemv::read_mma_status_nb2(&b3, reset != 0);
+    if (e == cudaSuccess) e = gemv::read_fp8_status(&b4, reset != 0);
     if (e != cudaSuccess) return cuda_fail(e);
-    *bits = b1 | b2 | b3;
+    *bits = b1 | b2 | b3 | b4;
     return GEMV_OK;
 }
 

@@ -161,6 +161,29 @@ __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t b
                  :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
 }
 
+// x by bulk copies (one thread, one copy per x row, in pieces of at most
+// 32 KB), counted on the mbarrier `bar`: rows b < B of x[b][c0 .. c0 + 8 nv)
+// into xs (row stride xstride elements). Needs x 16-byte aligned, K a multiple
+// of 8, c0 a multiple of 8 and xstride a multiple of 8, so that every piece
+// starts and ends on a 16-byte boundary on both sides. Thread 0 arms the
+// barrier with the byte count and issues the copies; every thread then waits
+// with mbar_wait_bounded (the barrier was initialised, and made visible to the
+// CTA, before).
+__device__ __forceinline__ void bulk_stage_x(uint64_t* bar, uint16_t* xs, int xstride, const uint16_t* x, int B,
+                                             int64_t K, int64_t c0, int nv) {
+    if (threadIdx.x != 0) return;
+    const uint32_t row_bytes = 16u * static_cast<uint32_t>(nv);
+    mbar_arrive_expect_tx(bar, row_bytes * static_cast<uint32_t>(B));
+    for (int b = 0; b < B; ++b) {
+        const unsigned char* src = reinterpret_cast<const unsigned char*>(x + static_cast<int64_t>(b) * K + c0);
+        unsigned char* dst = reinterpret_cast<unsigned char*>(xs + static_cast<int64_t>(b) * xstride);
+        for (uint32_t off = 0; off < row_bytes; off += 32768u) {
+            const uint32_t n = row_bytes - off < 32768u ? row_bytes - off : 32768u;
+            bulk_copy(dst + off, src + off, n, bar);
+        }
+    }
+}
+
 // 16-byte asynchronous global->shared copy of `nbytes` (2..16) bytes; the rest
 // of the 16 bytes is zero-filled. Both addresses 16-byte aligned.
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src, int nbytes) {

@@ -14,6 +14,8 @@ cudaError_t launch_fp8_batch(int B, const Params& p, const Launch& l, cudaStream
     return launch_fp8_uj<2, kF8Unroll>(p, l, s, pdl);
 }
 
+cudaError_t read_fp8_status(unsigned int* bits, bool reset) { return read_fp8_status_tu(bits, reset); }
+
 cudaError_t prepare_fp8_all() {
     cudaError_t e = prepare_fp8_uj<1, kF8Unroll>();
     if (e != cudaSuccess) return e;

@@ -28,8 +28,8 @@
 // physical columns (one 16-byte shared-memory read of x per two words). Each
 // batch of UJ slots is summed into a fresh FP32 tile before it is added to the
 // running sums (blocked accumulation); the row scale multiplies the final
-// sums. x is staged per CTA with asynchronous copies (rows padded so the eight
-// batch rows of a warp's read fall on different banks), the first batch of
+// sums. x is staged per CTA with bulk or asynchronous copies (rows padded so
+// the eight batch rows of a warp's read fall on different banks), the first batch of
 // loads goes out before the programmatic-dependent-launch wait, and partial
 // sums combine in a fixed order over warps and cluster CTAs.
 #pragma once
@@ -69,12 +69,25 @@ __device__ __forceinline__ F8Range f8_range(int nslots, int kw, int kq) {
     return r;
 }
 
-template <int NB, int UJ, bool CHUNKED>
+// XB (one chunk, x 16-byte aligned in this GPU's memory): x is copied into
+// shared memory by bulk copies counted on an mbarrier (bulk_stage_x), which do
+// not queue behind the code loads the warps have just issued, instead of
+// 16-byte asynchronous copies from every thread.
+template <int NB, int UJ, bool CHUNKED, bool XB = false>
 __global__ void __launch_bounds__(kThreads)
 gemv_fp8_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
 
     pdl_launch_dependents();
+
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(smem_raw);   // the 16 bytes before x
+    if constexpr (XB) {
+        if (threadIdx.x == 0) {
+            mbar_init(mbar, 1);
+            fence_mbar_init_cluster();
+        }
+        __syncthreads();
+    }
 
     const int S = p.splits;
     if (S > 1) cluster_arrive_relaxed();   // see combine_and_store
@@ -106,8 +119,8 @@ gemv_fp8_kernel(const __grid_constant__ Params p) {
 
     const int xstride = p.xstride;
     const int xbuf = B * xstride;
-    uint16_t* xs = reinterpret_cast<uint16_t*>(smem_raw);
-    float* red = reinterpret_cast<float*>(smem_raw + static_cast<size_t>(p.nbuf) * xbuf * 2);
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem_raw + kBulkSmemHead);
+    float* red = reinterpret_cast<float*>(smem_raw + kBulkSmemHead + static_cast<size_t>(p.nbuf) * xbuf * 2);
     float* cpart = red + rows_per_cta * (B + 1) * kw;
     float* misc = cpart + rows_per_cta * B + kMaxSplits;   // cpart: cluster slots, see combine_and_store
     const bool norm = (p.flags & kFlagRmsNorm) != 0;
@@ -188,7 +201,13 @@ gemv_fp8_kernel(const __grid_constant__ Params p) {
     rg_begin = rg.j_begin;
     issue(ch.c0, 0, rg.my_slots);
     if (!(p.flags & kFlagNoWait)) pdl_wait_prerequisites();
-    stage_x(xs, xstride, p.x, B, K, ch.c0, ch.nv);
+    bool x_ok = true;   // false when the wait for the bulk copy of x ran out
+    if constexpr (XB) {
+        bulk_stage_x(mbar, xs, xstride, p.x, B, K, ch.c0, ch.nv);   // K % 64 == 0: whole vectors
+        x_ok = mbar_wait_bounded(mbar, 0);
+    } else {
+        stage_x(xs, xstride, p.x, B, K, ch.c0, ch.nv);
+    }
 
 #pragma unroll 1
     for (int c = 0;; ++c) {
@@ -200,10 +219,10 @@ gemv_fp8_kernel(const __grid_constant__ Params p) {
             nch = chunk_at(next_c0, k1, p.kchunk, K);
             stage_x(xs + ((c + 1) & 1) * xbuf, xstride, p.x, B, K, nch.c0, nch.nv);
             cp_async_wait<1>();
-        } else {
+        } else if constexpr (!XB) {
             cp_async_wait<0>();
         }
-        __syncthreads();
+        if constexpr (!XB) __syncthreads();   // with XB the mbarrier wait made x visible
 
         const int my = rg.my_slots;
 #pragma unroll 1
@@ -247,16 +266,24 @@ gemv_fp8_kernel(const __grid_constant__ Params p) {
         for (int i = 0; i < 4; ++i) {
             const int b = nb * 8 + 2 * t + (i & 1);
             const int rl = rl0 + ((i & 2) ? 8 : 0);
-            if (b < B) red[red_index(kq, rows_per_cta, rl, B, b)] = acc[nb][i] * ((i & 2) ? rs1 : rs0);
+            // A CTA whose copy of x did not arrive in time stores NaN (and
+            // has set the status bit) rather than sums over an incomplete x.
+            if (b < B)
+                red[red_index(kq, rows_per_cta, rl, B, b)] =
+                    x_ok ? acc[nb][i] * ((i & 2) ? rs1 : rs0) : __uint_as_float(0x7fc00000u);
         }
     }
     combine_and_store(red, cpart, misc, rows_per_cta, B, kw, S, split, sg.tile_local * rows_per_cta, sg.N, sg.y,
                       norm, K, p.rms_eps, p.wc);
+    if constexpr (XB) {
+        if (!x_ok) mbar_wait_bounded(mbar, 0);   // the copy may still be in flight: wait once more
+    }
 }
 
 template <int NB, int UJ>
 cudaError_t launch_fp8_uj(const Params& p, const Launch& l, cudaStream_t s, bool pdl) {
     if (l.nbuf > 1) return launch_kernel(gemv_fp8_kernel<NB, UJ, true>, p, l, s, pdl);
+    if (l.xbulk) return launch_kernel(gemv_fp8_kernel<NB, UJ, false, true>, p, l, s, pdl);
     return launch_kernel(gemv_fp8_kernel<NB, UJ, false>, p, l, s, pdl);
 }
 
@@ -265,8 +292,19 @@ cudaError_t prepare_fp8_uj() {
     cudaError_t e = cudaFuncSetAttribute(gemv_fp8_kernel<NB, UJ, true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
     if (e != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(gemv_fp8_kernel<NB, UJ, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kMaxDynSmem)) != cudaSuccess)
+        return e;
     return cudaFuncSetAttribute(gemv_fp8_kernel<NB, UJ, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+}
+
+// Status bits this translation unit's kernels recorded, cleared when `reset`.
+inline cudaError_t read_fp8_status_tu(unsigned int* bits, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(bits, g_device_status, sizeof(unsigned int));
+    if (e != cudaSuccess || !reset || *bits == 0) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_device_status, &zero, sizeof(unsigned int));
 }
 
 }  // namespace gemv

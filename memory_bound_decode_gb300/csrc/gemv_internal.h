@@ -59,8 +59,9 @@ struct Params {
 // x: its mbarrier (16 to keep x 16-byte aligned). Planned for every CUDA-core
 // launch; the other instances leave them unused.
 constexpr int kFmaSmemHead = 16;
-// The same for the BF16 tensor-core kernel: the mbarrier of its bulk copy of x.
-constexpr int kMmaSmemHead = 16;
+// The same for the BF16 tensor-core and FP8 kernels: the mbarrier of their
+// bulk copy of x.
+constexpr int kBulkSmemHead = 16;
 // Multicast x for batch 1 when the launch has no K split and x is at least
 // this many 16-byte vectors, i.e. K >= 8,192 (measured: down_proj, x = 28 KB,
 // 18.25 -> 17.94 us with clusters of 2; with x = 8 KB the launches with and
@@ -139,7 +140,7 @@ struct Launch {
     int32_t xstride;
     int32_t nbuf;
     int32_t mcast;     // CTAs sharing one multicast copy of x (cluster along the rows); 1: none
-    int32_t xbulk;     // tensor-core path: x copied by bulk copies (one chunk, aligned rows)
+    int32_t xbulk;     // BF16 tensor-core and FP8 paths: x copied by bulk copies (one chunk, aligned rows)
 };
 
 // Sweep knob of the planner (GEMV_FORCE_VARIANT planwait=1): every launch of
@@ -222,6 +223,7 @@ cudaError_t prepare_kernels(int device);   // per-device function attributes
 cudaError_t read_fma_status(unsigned int* bits, bool reset);
 cudaError_t read_mma_status_nb1(unsigned int* bits, bool reset);
 cudaError_t read_mma_status_nb2(unsigned int* bits, bool reset);
+cudaError_t read_fp8_status(unsigned int* bits, bool reset);
 cudaError_t launch_probe_read(const void* src, int64_t bytes, float* sink, int grid,
                               cudaStream_t s);
 

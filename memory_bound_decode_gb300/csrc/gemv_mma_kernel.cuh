@@ -184,8 +184,8 @@ gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
 
     const int xstride = p.xstride;
     const int xbuf = B * xstride;
-    uint16_t* xs = reinterpret_cast<uint16_t*>(smem_raw + kMmaSmemHead);
-    float* red = reinterpret_cast<float*>(smem_raw + kMmaSmemHead + static_cast<size_t>(p.nbuf) * xbuf * 2);
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem_raw + kBulkSmemHead);
+    float* red = reinterpret_cast<float*>(smem_raw + kBulkSmemHead + static_cast<size_t>(p.nbuf) * xbuf * 2);
     float* cpart = red + rows_per_cta * (B + 1) * kw;
     float* misc = cpart + rows_per_cta * B + kMaxSplits;   // cpart: cluster slots, see combine_and_store
     const bool norm = (p.flags & kFlagRmsNorm) != 0;
@@ -212,19 +212,7 @@ gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
     if (!(p.flags & kFlagNoWait)) pdl_wait_prerequisites();
     bool x_ok = true;   // false when the wait for the bulk copy of x ran out
     if constexpr (XB) {
-        // K % 8 == 0: the chunk is whole 16-byte vectors; rows b < B only.
-        const uint32_t row_bytes = 16u * static_cast<uint32_t>(ch.nv);
-        if (threadIdx.x == 0) {
-            mbar_arrive_expect_tx(mbar, row_bytes * static_cast<uint32_t>(B));
-            for (int b = 0; b < B; ++b) {
-                const unsigned char* src = reinterpret_cast<const unsigned char*>(p.x + static_cast<int64_t>(b) * K + ch.c0);
-                unsigned char* dst = reinterpret_cast<unsigned char*>(xs + static_cast<int64_t>(b) * xstride);
-                for (uint32_t off = 0; off < row_bytes; off += 32768u) {
-                    const uint32_t n = row_bytes - off < 32768u ? row_bytes - off : 32768u;
-                    bulk_copy(dst + off, src + off, n, mbar);
-                }
-            }
-        }
+        bulk_stage_x(mbar, xs, xstride, p.x, B, K, ch.c0, ch.nv);   // K % 8 == 0: whole vectors
         x_ok = mbar_wait_bounded(mbar, 0);
     } else {
         stage_x_rows(xs, xstride, p.x, B, K, ch.c0, ch.nv);

@@ -291,7 +291,7 @@ int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight
     if (ov.mcast > 0) mcast = (mcast_ok && K >= 8 && row_tiles >= ov.mcast) ? ov.mcast : 1;
     const int64_t grid = mcast > 1 ? round_up(row_tiles, mcast) : row_tiles * splits;
     if (grid > 0x7fffffffLL) return GEMV_ERR_UNSUPPORTED;
-    const int64_t smem = (path == kPathFma ? kFmaSmemHead : path == kPathMma ? kMmaSmemHead : 0) +
+    const int64_t smem = (path == kPathFma ? kFmaSmemHead : (path == kPathMma || path == kPathFp8) ? kBulkSmemHead : 0) +
                          nbuf * static_cast<int64_t>(B) * xstride * 2 +
                          rows_per_cta * (B + 1) * kw * 4 + (rows_per_cta * B + kMaxSplits) * 4 + kMiscFloats * 4;
     if (smem > kMaxDynSmem) return GEMV_ERR_UNSUPPORTED;
@@ -310,9 +310,9 @@ int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight
     out->xstride = static_cast<int32_t>(xstride);
     out->nbuf = nbuf;
     out->mcast = mcast;
-    // Tensor-core path with x in one chunk of whole 16-byte vectors: bulk
-    // copies of x (the front end checks the pointer itself).
-    out->xbulk = (path == kPathMma && nbuf == 1 && K % 8 == 0) ? 1 : 0;
+    // BF16 tensor-core and FP8 paths with x in one chunk of whole 16-byte
+    // vectors: bulk copies of x (the front end checks the pointer itself).
+    out->xbulk = ((path == kPathMma || path == kPathFp8) && nbuf == 1 && K % 8 == 0) ? 1 : 0;
     return GEMV_OK;
 }
 

@@ -128,3 +128,27 @@ def test_fp8_rejects_streamk_and_bad_k():
     assert binding.gemv_fp8_bf16(Wq, S, x, y, 64, 128, 1, 128, options=opt, check=False) == \
         binding.GEMV_ERR_UNSUPPORTED
     assert binding.gemv_fp8_bf16(Wq, S, x, y, 64, 96, 1, 128, check=False) == binding.GEMV_ERR_INVALID
+
+
+@pytest.mark.parametrize("N,K,B", [(4096, 14336, 1), (1000, 4096, 4), (300, 12288, 16)])
+def test_fp8_bulk_x_copy(N, K, B):
+    """x in this GPU's memory, 16-byte aligned, is copied into shared memory by
+    bulk copies; x in pinned host memory by per-thread copies. Same bits, both
+    against the oracle, and no wait ran out."""
+    Wq, S = inputs.fp8_weight(N, K, seed=N + B, device=DEV)
+    x = inputs.activations(B, K, seed=K + B, device=DEV)
+
+    def run_x(xx):
+        buf, y = gu.guarded_y(B, N)
+        binding.gemv_fp8_bf16(Wq, S, xx, y, N, K, B, Wq.shape[1])
+        torch.cuda.synchronize()
+        gu.check_guards(buf)
+        return y.cpu().numpy()
+
+    y_dev = run_x(x)
+    y_host = run_x(x.cpu().pin_memory())
+    assert np.array_equal(y_dev.view(np.uint32), y_host.view(np.uint32))
+    y_ref, sc = oracle.gemv_fp8(Wq.cpu().numpy(), S.cpu().numpy(), inputs.bits(x), K,
+                                threads=oracle.default_threads())
+    gu.assert_parity(y_dev, y_ref, sc, f"fp8 bulk x N={N} K={K} B={B}")
+    assert binding.gemv_device_status(reset=True) == 0
