@@ -250,6 +250,20 @@ int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight
         while (splits < kMaxSplits && warps_for(kw, splits) < target_warps && room(kw, splits)) splits *= 2;
     }
 
+    // BF16 tensor-core path with one warp along K (nothing left to trade
+    // below): split K further, up to a full cluster of 8 CTAs, while the CTA's
+    // x slice would not fit in one staged chunk. Chunked x costs a barrier and
+    // a copy round per chunk; measured, B = 16 on N x 14,336 (us, chunked /
+    // one chunk): N = 4,864 49.6 / 36.1, N = 9,728 67.5 / 60.9, N = 19,456
+    // 130.2 / 107.7. Where x already fits, more splits only cost (B = 2 on
+    // 4,864 x 14,336: 24.4 us with 4 CTAs along K, 30.6 with 8), so they stay.
+    if (path == kPathMma && ov.kw == 0 && !overlap && kw == 1) {
+        auto xbytes = [&](int s_) { return static_cast<int64_t>(B) * (cdiv(K, s_) + xpad) * 2; };
+        int s2 = splits;
+        while (s2 < kMaxSplits && xbytes(s2) > kXBudgetBytes && room(kw, s2)) s2 *= 2;
+        if (xbytes(s2) <= kXBudgetBytes) splits = s2;   // only where x then fits one chunk
+    }
+
     // On the BF16 and INT4 tensor-core paths, trade warps along K for CTAs
     // along K while the CTA's x slice does not fit in one staged chunk (same
     // warps, fewer x bytes per CTA, no chunk barriers). The FP8 kernel measured

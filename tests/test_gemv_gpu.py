@@ -66,7 +66,7 @@ def test_parity_full_size(name, N, K):
 
 
 @pytest.mark.parametrize("B", [1, 2, 4, 8, 16])
-@pytest.mark.parametrize("N,K", [(4096, 4096), (4096, 14336), (4864, 14336)])
+@pytest.mark.parametrize("N,K", [(4096, 4096), (4096, 14336), (4864, 14336), (28672, 4096)])
 def test_parity_skinny_batch(N, K, B):
     W, x, _ = make(N, K, B, seed=2)
     y = gu.gemv(W, x, K)
