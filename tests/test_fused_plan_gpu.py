@@ -20,6 +20,7 @@ def _segments(rows, K, seed):
 
 @pytest.mark.parametrize("rows,K,B", [
     ((4096, 1024, 1024), 4096, 1),      # Q, K, V
+    ((4096, 1024, 1024), 4096, 4),      # Q, K, V at batch 4 (tensor cores, x by bulk copies)
     ((14336, 14336), 4096, 1),          # gate, up
     ((7, 33, 1, 100), 4103, 3),         # ragged segments
     ((5,) * 8, 129, 2),                 # the most segments one launch takes
