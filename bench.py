@@ -529,7 +529,9 @@ def time_workload(torch, wk, args, stream, gpu_index: int, isolated: int = 20) -
 def time_e2e(torch, binding, wk, steps: int, stream) -> dict | None:
     """The same workload end to end through the public C entry points with
     host buffers: every step copies its inputs in from pinned host memory,
-    runs, copies its outputs back and waits (host wall clock)."""
+    runs, copies its outputs back and waits (host wall clock): gemv_bf16_host_io,
+    gemv_bf16_multi_host_io, or gemv_plan_launch_host_io (the decode step, and
+    a one-projection plan for quantised weights)."""
     sh = stream.cuda_stream
     if isinstance(wk, StepWorkload):
         d = wk.data
@@ -558,15 +560,19 @@ def time_e2e(torch, binding, wk, steps: int, stream) -> dict | None:
                 binding.gemv_bf16_multi_host_io([(W, y, n_, wk.ldw) for W, y, n_ in zip(Ws, wk.ys, wk.rows)],
                                                 x_host, x_dev, y_host, wk.K, wk.B, rms_eps=wk.rms_eps,
                                                 stream=sh, streamk=wk.streamk, cuda_cores=wk.cuda_cores)
-            else:   # quantised weights: the binding's copy, launch, copy, wait
-                x_dev.copy_(x_host, non_blocking=True)
-                wk.step(i, stream, x_dev)
-                for yh, yd in zip(y_host, wk.ys):
-                    yh.copy_(yd, non_blocking=True)
-                stream.synchronize()
+            else:   # quantised weights: a one-projection plan per weight copy, host to host
+                plans[i % wk.copies].launch_host_io(x_host, x_dev, h2d, wk.ys[0], y_host[0], d2h, sh)
         h2d = int(x_host.numel() * x_host.element_size())
         d2h = int(sum(y.numel() * y.element_size() for y in y_host))
         n = max(10, min(steps, 2000))
+        plans = []
+        if not bf16:
+            kind = binding.GEMV_WEIGHT_INT4 if wk.w4 else binding.GEMV_WEIGHT_FP8
+            for Ws in wk.Ws:
+                Wq, S = Ws[0]
+                plans.append(binding.Plan([(Wq, x_dev, wk.ys[0], wk.N, wk.K, wk.ldq, wk.B, 0, wk.rms_eps, False, kind,
+                                            S, wk.lds if wk.w4 else 0)]))
+                plans[-1].capture(torch.cuda.Stream())
     with torch.cuda.stream(stream):
         for i in range(5):
             e2e_step(i)
