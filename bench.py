@@ -363,15 +363,31 @@ class GemvWorkload:
 class StepWorkload:
     """The full decode-step projection set replayed as one CUDA graph."""
 
-    def __init__(self, device, stream, rms_eps=None, streamk=False, weights="bf16"):
+    def __init__(self, device, stream, rms_eps=None, streamk=False, weights="bf16", data=None,
+                 keep_waits=False):
         from memory_bound_decode_gb300 import workloads as wl
         self.spec = wl.decode_step_spec()
         self.weights = weights
-        self.data = wl.DecodeStep(self.spec, seed=0, device=device, weights=weights)
+        self.data = data if data is not None else wl.DecodeStep(self.spec, seed=0, device=device, weights=weights)
         self.rms_eps = rms_eps
         self.streamk = streamk
+        self.keep_waits = keep_waits
         self.w4, self.fp8 = weights == "int4", weights == "fp8"
-        self.plan = self.data.plan(rms_eps=rms_eps, streamk=streamk)
+        if keep_waits:
+            # every launch waits for the preceding grid, as if each projection
+            # read the previous one's output (the planner's planwait knob,
+            # read when the plan is created)
+            saved = os.environ.get("GEMV_FORCE_VARIANT")
+            os.environ["GEMV_FORCE_VARIANT"] = (saved + "," if saved else "") + "planwait=1"
+            try:
+                self.plan = self.data.plan(rms_eps=rms_eps, streamk=streamk)
+            finally:
+                if saved is None:
+                    del os.environ["GEMV_FORCE_VARIANT"]
+                else:
+                    os.environ["GEMV_FORCE_VARIANT"] = saved
+        else:
+            self.plan = self.data.plan(rms_eps=rms_eps, streamk=streamk)
         self.plan.capture(stream)
         self.bytes_per_step = (wl.step_bytes_formula(self.spec) if weights == "bf16"
                                else self.data.algorithmic_bytes())
@@ -624,8 +640,22 @@ def target_entry(torch, binding, name: str, args, stream, device, l2, peak, read
            "clocks": t["clocks"]}
     if isinstance(wk, StepWorkload):
         out["launches_per_step"] = wk.launches_per_step
+        out["independent_launches"] = wk.plan.independent()
     if not args.no_e2e:
         out["e2e"] = time_e2e(torch, binding, wk, args.steps, stream)
+    if isinstance(wk, StepWorkload):
+        # The same step with every launch waiting for the preceding grid (as
+        # if the projections were chained), on the same weights.
+        dep = StepWorkload(device, torch.cuda.Stream(), wk.rms_eps, wk.streamk, wk.weights, data=wk.data,
+                           keep_waits=True)
+        td = time_workload(torch, dep, args, stream, gpu_index)
+        per = td["seconds"] / args.steps
+        gd = dep.bytes_per_step / per / 1e9
+        out["with_every_wait"] = {"us_per_step": round(per * 1e6, 3), "gbs": round(gd, 2), "frac": round(gd / peak, 4),
+                                  "met": gd / peak >= TARGETS[name], "independent_launches": dep.plan.independent(),
+                                  "clocks": td["clocks"]}
+        dep.plan.destroy()
+        del dep
     del wk
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
