@@ -347,6 +347,19 @@ typedef struct {
                                 Tensor Memory Accelerator); 1: each CTA copies
                                 its own. A call whose x is not 16-byte aligned
                                 falls back to 1                                   */
+    int32_t xbox;            /* path 1, B > 8, x in one chunk, K a multiple of
+                                32: x is copied by the Tensor Memory Accelerator
+                                as tensor boxes of 8 MMA blocks (256 columns) of
+                                all B rows, in pieces each counted on its own
+                                mbarrier (1: narrow boxes, landing block-major;
+                                2: wide boxes, landing row-major); 0: one bulk
+                                copy per x row (K a multiple of 8) or 16-byte
+                                copies from every thread. A call whose x is not
+                                16-byte aligned memory of this GPU, or that has
+                                the RMSNorm prologue, falls back to 0 (and
+                                smem_bytes to that of the row layout)             */
+    int32_t xpieces;         /* xbox > 0: pieces per warp group along K           */
+    int32_t xboxes_per_piece;/* xbox > 0: boxes per piece                         */
 } gemv_launch_info;
 
 int gemv_query_launch(int64_t N, int64_t K, int B, int sm_count,

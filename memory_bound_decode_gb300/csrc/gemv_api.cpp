@@ -95,9 +95,50 @@ constexpr size_t kMappedYMaxBytes = 256 * 1024;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// cuTensorMapEncodeTiled, looked up once through the runtime (the library
+// links no driver library of its own); null where the driver lacks it.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return static_cast<EncodeTiledFn>(nullptr);
+        }
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// The 3-D view of x [B][K] that the tensor-core kernel copies tensor boxes
+// through. Narrow (K a multiple of 32): 32 columns x B rows x K / 32 blocks
+// (row stride 2K bytes, block stride 64 bytes), boxes of 32 x B x 8 bpp. Wide
+// (K a multiple of 256): 256 columns x B rows x K / 256, boxes of
+// 256 x B x bpp. Zero fill past the end. False if the driver rejects it.
+bool encode_x_boxes(CUtensorMap* map, const void* x, int64_t K, int B, int bpp, bool wide) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const int64_t w = wide ? 256 : 32;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(w), static_cast<cuuint64_t>(B),
+                                static_cast<cuuint64_t>(K / w)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(w) * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(w), static_cast<cuuint32_t>(B),
+                               static_cast<cuuint32_t>(wide ? bpp : 8 * bpp)};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box, elem,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Whether p points into device memory of the current device: the x multicast
-// copies from there only (a pointer into mapped host or managed memory takes
-// the per-CTA staging instead).
+// and the tensor copies of x read from there only (a pointer into mapped host
+// or managed memory takes the per-CTA staging instead).
 bool on_current_device(const void* p) {
     cudaPointerAttributes a;
     if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
@@ -254,6 +295,13 @@ int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B
     l.row_tiles = tiles;
     // The bulk copy reads x from a 16-byte boundary, and only from this GPU's memory.
     if (l.mcast > 1 && (!aligned(x, 16) || !on_current_device(x))) l.mcast = 1;
+    // The tensor copies of x read from a 16-byte boundary, and only from this
+    // GPU's memory; the RMSNorm statistic reads x staged row by row.
+    if (l.xbox && ((flags & GEMV_FLAG_RMSNORM) || !aligned(x, 16) || !on_current_device(x) ||
+                   !encode_x_boxes(&p.xmap, x, K, B, l.xbpp, l.xbox == 2))) {
+        l.xbox = 0;
+        l.smem_bytes = l.smem_rows;
+    }
     // The bulk copies of x read from a 16-byte boundary, and only from this GPU's memory.
     if (l.xbulk && (!aligned(x, 16) || !on_current_device(x))) l.xbulk = 0;
     l.grid = l.mcast > 1 ? (tiles + l.mcast - 1) / l.mcast * l.mcast : tiles * l.splits;
@@ -271,6 +319,9 @@ int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B
     p.flags = (flags & GEMV_FLAG_RMSNORM) ? gemv::kFlagRmsNorm : 0;
     p.rms_eps = eps;
     p.mcast = l.mcast > 1 ? l.mcast : 1;
+    p.xper = l.xbox ? l.xper : 0;
+    p.xbpp = l.xbox ? l.xbpp : 0;
+    p.xwide = l.xbox == 2 ? 1 : 0;
     p.wc = g_write_count;
     out->p = p;
     out->l = l;
@@ -414,6 +465,9 @@ void fill_info(const Launch& l, gemv_launch_info* out) {
     out->xstride = l.xstride;
     out->nbuf = l.nbuf;
     out->mcast = l.mcast;
+    out->xbox = l.xbox;
+    out->xpieces = l.xbox ? l.xper : 0;
+    out->xboxes_per_piece = l.xbox ? l.xbpp : 0;
 }
 
 }  // namespace

@@ -184,6 +184,79 @@ __device__ __forceinline__ void bulk_stage_x(uint64_t* bar, uint16_t* xs, int xs
     }
 }
 
+// ---- x as tensor boxes, in pieces with one mbarrier each -----------------------
+//
+// The tensor-core kernel stages x with the Tensor Memory Accelerator's tensor
+// copies (cp.async.bulk.tensor) through a 3-D view of x, so that one copy
+// moves a whole piece (all B rows of several 256-column boxes), where one copy
+// per row and piece would cost the issuing thread tens of nanoseconds each.
+// Each piece is counted on its own mbarrier, so a warp waits only for the
+// piece its next batch reads: the first piece lands in a fraction of the time
+// the whole slice takes, and the rest land while the warps stream W.
+//   narrow: 32 columns (one MMA block) x B rows x K / 32 blocks; a box lands
+//     block-major, [block][row][32 columns]: rows of one block are 64 bytes
+//     apart, so the two rows a quarter-warp reads for its x fragments fall in
+//     different banks;
+//   wide: 256 columns x B rows x K / 256; a box lands [row][256 columns]
+//     (rows 512 bytes apart: those two rows share banks), in fewer and longer
+//     requests.
+// Geometry: warp group kq of the kw groups along K takes the blocks
+// [kq * span, (kq + 1) * span) of the CTA's slice; its range is cut into `per`
+// pieces of `bpp` boxes of 8 blocks (one batch of UJ = 8 blocks per box), so a
+// batch never reads two pieces. Piece r of group kq is counted on mbarrier
+// kq * per + r and lands at xs + (kq * per + r) * bpp * 8 * B * 32. Boxes past
+// the end of the tensor are zero-filled by the copy engine.
+
+__device__ __forceinline__ void xpieces_init(uint64_t* bars) {
+    if (threadIdx.x == 0) {
+        for (int q = 0; q < kMaxXPieces; ++q) mbar_init(bars + q, 1);
+        fence_mbar_init_cluster();
+    }
+}
+
+// 3-D tensor copy of one box at coordinates (0, 0, blk) into shared memory,
+// completing its bytes on the mbarrier `bar`. `map` is the kernel parameter
+// holding the tensor map (param space, so no proxy fence is needed).
+__device__ __forceinline__ void tensor_copy_3d(void* dst, const void* map, int blk, uint64_t* bar) {
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4}], [%5];"
+                 :: "r"(smem_addr(dst)), "l"(map), "r"(0), "r"(0), "r"(blk), "r"(smem_addr(bar)) : "memory");
+}
+
+// Thread 0 arms every piece's mbarrier with its bytes and issues its copy,
+// piece 0 of every group first. blk0: the slice's first block (column / 32);
+// wide boxes are addressed in units of 8 blocks (blk0 and span multiples of 8).
+__device__ __forceinline__ void stage_x_boxes(uint64_t* bars, const void* map, int kw, int span, int per, int bpp,
+                                              uint16_t* xs, int B, int64_t blk0, bool wide) {
+    if (threadIdx.x != 0) return;
+    const int piece_elems = bpp * 8 * B * 32;
+    const uint32_t piece_bytes = 2u * static_cast<uint32_t>(piece_elems);
+    for (int r = 0; r < per; ++r) {
+        for (int kq = 0; kq < kw; ++kq) {
+            uint64_t* bar = bars + kq * per + r;
+            mbar_arrive_expect_tx(bar, piece_bytes);
+            const int64_t blk = blk0 + kq * span + r * 8 * bpp;
+            tensor_copy_3d(xs + static_cast<int64_t>(kq * per + r) * piece_elems, map,
+                           static_cast<int>(wide ? blk / 8 : blk), bar);
+        }
+    }
+}
+
+// Wait (bounded) for pieces next .. r of this warp's group (`gbars` = its
+// first barrier); false if a wait ran out.
+__device__ __forceinline__ bool xpieces_wait(uint64_t* gbars, int& next, int r) {
+    bool ok = true;
+    for (; next <= r; ++next) ok = mbar_wait_bounded(gbars + next, 0) && ok;
+    return ok;
+}
+
+// Wait (bounded) for the first n barriers.
+__device__ __forceinline__ bool xpieces_wait_all(uint64_t* bars, int n) {
+    bool ok = true;
+    for (int q = 0; q < n; ++q) ok = mbar_wait_bounded(bars + q, 0) && ok;
+    return ok;
+}
+
 // 16-byte asynchronous global->shared copy of `nbytes` (2..16) bytes; the rest
 // of the 16 bytes is zero-filled. Both addresses 16-byte aligned.
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src, int nbytes) {

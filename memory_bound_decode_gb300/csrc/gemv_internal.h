@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>   // CUtensorMap (the type only; the library calls no driver API directly)
 #include <cuda_runtime.h>
 
 namespace gemv {
@@ -52,16 +53,23 @@ struct Params {
     float rms_eps;    // epsilon of the RMSNorm prologue
     int32_t mcast;    // CUDA-core kernel, batch 1, one K chunk, no K split: CTAs of a cluster along
                       // the rows that share one multicast copy of x (1: every CTA stages its own)
+    int32_t xper;     // BF16 tensor-core kernel, x as tensor boxes: pieces per warp group along K
+    int32_t xbpp;     // ... and boxes of 8 blocks (256 columns) per piece
+    int32_t xwide;    // ... 1: boxes of 256 columns x B rows, 0: of 32 columns x B rows (stage_x_boxes)
     WriteCount wc;
+    CUtensorMap xmap; // ... and the 3-D view of x the boxes are copied through (stage_x_boxes)
 };
 
+// The BF16 tensor-core kernel's x, copied as tensor boxes, lands in up to
+// kMaxXPieces pieces, each counted on its own mbarrier (see stage_x_boxes).
+constexpr int kMaxXPieces = 8;
 // Bytes at the start of the multicast instance's dynamic shared memory before
 // x: its mbarrier (16 to keep x 16-byte aligned). Planned for every CUDA-core
 // launch; the other instances leave them unused.
 constexpr int kFmaSmemHead = 16;
-// The same for the BF16 tensor-core and FP8 kernels: the mbarrier of their
-// bulk copy of x.
-constexpr int kBulkSmemHead = 16;
+// The same for the BF16 tensor-core and FP8 kernels: the mbarriers of their
+// copies of x (x starts 128-byte aligned, as a tensor copy needs).
+constexpr int kBulkSmemHead = 128;
 // Multicast x for batch 1 when the launch has no K split and x is at least
 // this many 16-byte vectors, i.e. K >= 8,192 (measured: down_proj, x = 28 KB,
 // 18.25 -> 17.94 us with clusters of 2; with x = 8 KB the launches with and
@@ -140,7 +148,12 @@ struct Launch {
     int32_t xstride;
     int32_t nbuf;
     int32_t mcast;     // CTAs sharing one multicast copy of x (cluster along the rows); 1: none
-    int32_t xbulk;     // BF16 tensor-core and FP8 paths: x copied by bulk copies (one chunk, aligned rows)
+    int32_t xbulk;     // FP8 path: x copied by bulk copies (one chunk, aligned rows)
+    int32_t xbox;      // BF16 tensor-core path: x copied as tensor boxes (one chunk, K % 32 == 0):
+                       // 1 narrow boxes (32 columns), 2 wide boxes (256 columns)
+    int32_t xper;      // ... pieces per warp group along K
+    int32_t xbpp;      // ... boxes of 8 blocks per piece
+    int32_t smem_rows; // shared memory of the same launch with x staged row by row (no boxes)
 };
 
 // Sweep knob of the planner (GEMV_FORCE_VARIANT planwait=1): every launch of

@@ -49,12 +49,14 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 struct MmaRange {
     int j_begin;
     int my_blocks;
+    int span;   // blocks per warp group along K
 };
 
 __device__ __forceinline__ MmaRange mma_range(const Chunk& c, int kw, int kq) {
     const int nblk = (c.nv + 3) >> 2;
     const int span = (nblk + kw - 1) / kw;
     MmaRange r;
+    r.span = span;
     r.j_begin = kq * span;
     const int j_end = (r.j_begin + span < nblk) ? r.j_begin + span : nblk;
     r.my_blocks = j_end > r.j_begin ? j_end - r.j_begin : 0;
@@ -86,14 +88,19 @@ __device__ __forceinline__ void mma_issue(uint4 (&w0)[UJ], uint4 (&w1)[UJ], bool
     }
 }
 
-template <int NB, bool PRED>
+// x fragment of vector vu (block vu / 4, lane column 8 (vu % 4)) for batch
+// rows g and g + 8: rows `xstride` elements apart; blocks 32 elements apart
+// (rows of x staged whole) or, BOXL (x as tensor boxes), boxes of 8 blocks
+// 256 B elements apart and blocks within a box `bstride` apart.
+template <int NB, bool PRED, bool BOXL>
 __device__ __forceinline__ void load_xfrag(uint4 (&xr)[NB], bool ok, const uint16_t* xrow0, int xstride,
-                                           int vu, int g, int B) {
+                                           int vu, int g, int B, int bstride) {
+    const int off = BOXL ? (vu >> 5) * (256 * B) + ((vu >> 2) & 7) * bstride + 8 * (vu & 3) : 8 * vu;
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
         xr[nb] = make_uint4(0u, 0u, 0u, 0u);
         if ((nb * 8 + g < B) && (!PRED || ok))
-            xr[nb] = *reinterpret_cast<const uint4*>(xrow0 + nb * 8 * xstride + 8 * vu);
+            xr[nb] = *reinterpret_cast<const uint4*>(xrow0 + nb * 8 * xstride + off);
     }
 }
 
@@ -101,10 +108,10 @@ __device__ __forceinline__ void load_xfrag(uint4 (&xr)[NB], bool ok, const uint1
 // read from shared memory while block u's MMAs run, and even and odd blocks
 // accumulate into separate tiles, so neither the shared-memory latency nor
 // the MMA latency is exposed block after block.
-template <int NB, int UJ, bool PRED>
+template <int NB, int UJ, bool PRED, bool BOXL>
 __device__ __forceinline__ void mma_consume(float (&acc)[NB][4], const uint4 (&w0)[UJ], const uint4 (&w1)[UJ],
                                             const bool (&ok)[UJ], const uint16_t* xrow0, int xstride,
-                                            int v, int g, int B) {
+                                            int v, int g, int B, int bstride) {
     float t[2][NB][4];
 #pragma unroll
     for (int h = 0; h < 2; ++h)
@@ -113,11 +120,13 @@ __device__ __forceinline__ void mma_consume(float (&acc)[NB][4], const uint4 (&w
 #pragma unroll
             for (int i = 0; i < 4; ++i) t[h][nb][i] = 0.f;
     uint4 xr[NB];
-    load_xfrag<NB, PRED>(xr, ok[0], xrow0, xstride, v, g, B);
+    load_xfrag<NB, PRED, BOXL>(xr, ok[0], xrow0, xstride, v, g, B, bstride);
 #pragma unroll
     for (int u = 0; u < UJ; ++u) {
         uint4 xn[NB];
-        if (u + 1 < UJ) load_xfrag<NB, PRED>(xn, ok[u + 1 < UJ ? u + 1 : u], xrow0, xstride, v + 4 * (u + 1), g, B);
+        if (u + 1 < UJ)
+            load_xfrag<NB, PRED, BOXL>(xn, ok[u + 1 < UJ ? u + 1 : u], xrow0, xstride, v + 4 * (u + 1), g, B,
+                                       bstride);
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
             mma_bf16_16816(t[u & 1][nb], w0[u].x, w1[u].x, w0[u].y, w1[u].y, xr[nb].x, xr[nb].y);
@@ -134,29 +143,40 @@ __device__ __forceinline__ void mma_consume(float (&acc)[NB][4], const uint4 (&w
         for (int i = 0; i < 4; ++i) acc[nb][i] += t[0][nb][i] + t[1][nb][i];
 }
 
+// How x reaches shared memory (one chunk; x 16-byte aligned, in this GPU's
+// memory, for the two copy-engine forms).
+constexpr int kXCopy = 0;   // 16-byte asynchronous copies from every thread
+constexpr int kXBulk = 1;   // one bulk copy per x row (K a multiple of 8), one mbarrier
+constexpr int kXBox = 2;    // tensor boxes in pieces, one mbarrier each (stage_x_boxes; K a multiple of 32)
+
 // CHUNKED: as for the CUDA-core kernel, a separate instance for K-ranges
-// staged in several chunks.
-// XB (one chunk; x 16-byte aligned, in this GPU's memory, K a multiple of 8):
-// x is copied into shared memory by the Tensor Memory Accelerator, one bulk
-// copy per x row issued by one thread and counted on an mbarrier, instead of
-// 16-byte asynchronous copies from every thread. Those copies queue behind
-// the first batch of W loads the warps have just issued; the bulk copies do
-// not, so x arrives while that batch is still landing.
-template <int NB, int UJ, bool CHUNKED, bool XB = false>
+// staged in several chunks (always with kXCopy).
+// XM = kXBulk / kXBox: x is copied by the Tensor Memory Accelerator, issued by
+// one thread. The per-thread copies of kXCopy queue behind the first batch of
+// W loads the warps have just issued; the copy engine's do not, so x arrives
+// while that batch is still landing. With kXBox (more than 8 rows of x, whose
+// slice is the largest) a warp starts as soon as the piece its first batch
+// reads has landed.
+template <int NB, int UJ, bool CHUNKED, int XM = kXCopy>
 __global__ void __launch_bounds__(kThreads)
 gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
+    constexpr bool XBULK = XM == kXBulk, XBOX = XM == kXBox;
 
     pdl_launch_dependents();
 
-    // The bulk copy's mbarrier sits in the 16 bytes before x; every thread
-    // must see it initialised before it waits on it.
+    // The copy engine's mbarriers sit in the bytes before x; every thread
+    // must see them initialised before it waits on one.
     uint64_t* mbar = reinterpret_cast<uint64_t*>(smem_raw);
-    if constexpr (XB) {
+    if constexpr (XBULK) {
         if (threadIdx.x == 0) {
             mbar_init(mbar, 1);
             fence_mbar_init_cluster();
         }
+        __syncthreads();
+    }
+    if constexpr (XBOX) {
+        xpieces_init(mbar);
         __syncthreads();
     }
 
@@ -185,7 +205,8 @@ gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
     const int xstride = p.xstride;
     const int xbuf = B * xstride;
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem_raw + kBulkSmemHead);
-    float* red = reinterpret_cast<float*>(smem_raw + kBulkSmemHead + static_cast<size_t>(p.nbuf) * xbuf * 2);
+    const int xregion = XBOX ? kw * p.xper * p.xbpp * 8 * B * 32 : p.nbuf * xbuf;   // x elements staged
+    float* red = reinterpret_cast<float*>(smem_raw + kBulkSmemHead + static_cast<size_t>(xregion) * 2);
     float* cpart = red + rows_per_cta * (B + 1) * kw;
     float* misc = cpart + rows_per_cta * B + kMaxSplits;   // cpart: cluster slots, see combine_and_store
     const bool norm = (p.flags & kFlagRmsNorm) != 0;
@@ -210,17 +231,39 @@ gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
     const uint16_t* p1 = w1row + ch.c0 + 8 * static_cast<int64_t>(v);
     mma_issue<UJ, true>(w0, w1, ok, p0, p1, v, rg.my_blocks, ch);
     if (!(p.flags & kFlagNoWait)) pdl_wait_prerequisites();
-    bool x_ok = true;   // false when the wait for the bulk copy of x ran out
-    if constexpr (XB) {
+    bool x_ok = true;   // false when a wait for a copy of x ran out (or x could not be copied)
+    // kXBox: this warp group's x, its first piece barrier, the next piece to
+    // wait for and the blocks per piece.
+    const uint16_t* xgroup = xs;
+    uint64_t* gbars = mbar;
+    int xnext = 0;
+    int piece_blocks = 1;
+    if constexpr (XBOX) {
+        const int group_elems = p.xper * p.xbpp * 8 * B * 32;
+        xgroup = xs + static_cast<int64_t>(kq) * group_elems;
+        gbars = mbar + kq * p.xper;
+        piece_blocks = 8 * p.xbpp;
+        if ((smem_addr(xs) & 127) == 0) {   // a tensor copy needs a 128-byte aligned destination
+            stage_x_boxes(mbar, &p.xmap, kw, rg.span, p.xper, p.xbpp, xs, B, ch.c0 / 32, p.xwide != 0);
+        } else {
+            x_ok = false;
+            xnext = p.xper;   // nothing was issued: wait for nothing
+            if (threadIdx.x == 0) atomicOr(&g_device_status, kStatusWaitTimeout);
+        }
+    } else if constexpr (XBULK) {
         bulk_stage_x(mbar, xs, xstride, p.x, B, K, ch.c0, ch.nv);   // K % 8 == 0: whole vectors
         x_ok = mbar_wait_bounded(mbar, 0);
     } else {
         stage_x_rows(xs, xstride, p.x, B, K, ch.c0, ch.nv);
     }
 
+    // x row stride in shared memory, and (kXBox) the stride of blocks within a box.
+    const int xrs = XBOX ? (p.xwide ? 256 : 32) : xstride;
+    const int xbs = p.xwide ? 32 : B * 32;
 #pragma unroll 1
     for (int c = 0;; ++c) {
-        const uint16_t* xrow0 = xs + (c & 1) * xbuf + g * xstride;
+        const uint16_t* xrow0 = XBOX ? xgroup + g * xrs : xs + (c & 1) * xbuf + g * xstride;
+        int xv = XBOX ? t : v;   // the lane's x vector index: in the group's boxes or the chunk
         const int64_t next_c0 = ch.c0 + p.kchunk;
         const bool more = CHUNKED && next_c0 < k1;
         Chunk nch{};
@@ -228,32 +271,36 @@ gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
             nch = chunk_at(next_c0, k1, p.kchunk, K);
             stage_x_rows(xs + ((c + 1) & 1) * xbuf, xstride, p.x, B, K, nch.c0, nch.nv);
             cp_async_wait<1>();
-        } else if constexpr (!XB) {
+        } else if constexpr (XM == kXCopy) {
             cp_async_wait<0>();
         }
-        if constexpr (!XB) __syncthreads();   // with XB the mbarrier wait made x visible
+        if constexpr (XM == kXCopy) __syncthreads();   // otherwise the mbarrier waits make x visible
 
-        mma_consume<NB, UJ, true>(acc, w0, w1, ok, xrow0, xstride, v, g, B);
+        if constexpr (XBOX) x_ok = xpieces_wait(gbars, xnext, 0) && x_ok;
+        mma_consume<NB, UJ, true, XBOX>(acc, w0, w1, ok, xrow0, xrs, xv, g, B, xbs);
         int j = UJ;
         auto advance = [&]() {
             p0 += 32 * UJ;
             p1 += 32 * UJ;
             v += 4 * UJ;
+            xv += 4 * UJ;
         };
         advance();
 #pragma unroll 1
         for (; j + UJ <= rg.my_blocks && (v - t) + 4 * UJ <= ch.nfull; j += UJ) {
             mma_issue<UJ, false>(w0, w1, ok, p0, p1, v, UJ, ch);
-            mma_consume<NB, UJ, false>(acc, w0, w1, ok, xrow0, xstride, v, g, B);
+            if constexpr (XBOX) x_ok = xpieces_wait(gbars, xnext, j / piece_blocks) && x_ok;
+            mma_consume<NB, UJ, false, XBOX>(acc, w0, w1, ok, xrow0, xrs, xv, g, B, xbs);
             advance();
         }
 #pragma unroll 1
         for (; j < rg.my_blocks; j += UJ) {
             mma_issue<UJ, true>(w0, w1, ok, p0, p1, v, rg.my_blocks - j, ch);
-            mma_consume<NB, UJ, true>(acc, w0, w1, ok, xrow0, xstride, v, g, B);
+            if constexpr (XBOX) x_ok = xpieces_wait(gbars, xnext, j / piece_blocks) && x_ok;
+            mma_consume<NB, UJ, true, XBOX>(acc, w0, w1, ok, xrow0, xrs, xv, g, B, xbs);
             advance();
         }
-        if (norm) xsq_accumulate(xs + (c & 1) * xbuf, xstride, B, ch.nv, misc, c == 0);
+        if (norm) xsq_accumulate(xs + (c & 1) * xbuf, xstride, B, ch.nv, misc, c == 0);   // never with kXBox
         if (!more) break;
 
         ch = nch;
@@ -280,17 +327,26 @@ gemv_bf16_mma_kernel(const __grid_constant__ Params p) {
     }
     combine_and_store(red, cpart, misc, rows_per_cta, B, kw, S, split, sg.tile_local * rows_per_cta, sg.N, sg.y,
                       norm, K, p.rms_eps, p.wc);
-    // After a timed-out wait the copy may still be in flight into this CTA's
-    // shared memory: wait for it once more (bounded) before leaving.
-    if constexpr (XB) {
+    // Pieces no warp of this CTA read (ranges shorter than the planned ones),
+    // and, after a timed-out wait, copies still in flight: every issued copy
+    // has landed before the CTA leaves (bounded waits).
+    if constexpr (XBOX) {
+        if ((smem_addr(xs) & 127) == 0) xpieces_wait_all(mbar, kw * p.xper);
+    }
+    if constexpr (XBULK) {
         if (!x_ok) mbar_wait_bounded(mbar, 0);
     }
 }
 
+// The tensor-box instance exists for more than 8 rows of x (NB = 2) only.
 template <int NB>
 cudaError_t launch_mma(const Params& p, const Launch& l, cudaStream_t s, bool pdl) {
     if (l.nbuf > 1) return launch_kernel(gemv_bf16_mma_kernel<NB, kMmaUnroll, true>, p, l, s, pdl);
-    if (l.xbulk) return launch_kernel(gemv_bf16_mma_kernel<NB, kMmaUnroll, false, true>, p, l, s, pdl);
+    if constexpr (NB == 2) {
+        if (l.xbox) return launch_kernel(gemv_bf16_mma_kernel<NB, kMmaUnroll, false, kXBox>, p, l, s, pdl);
+    }
+    if (l.xbox) return cudaErrorInvalidValue;
+    if (l.xbulk) return launch_kernel(gemv_bf16_mma_kernel<NB, kMmaUnroll, false, kXBulk>, p, l, s, pdl);
     return launch_kernel(gemv_bf16_mma_kernel<NB, kMmaUnroll, false>, p, l, s, pdl);
 }
 
@@ -299,9 +355,14 @@ cudaError_t prepare_mma() {
     cudaError_t e = cudaFuncSetAttribute(gemv_bf16_mma_kernel<NB, kMmaUnroll, true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
     if (e != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(gemv_bf16_mma_kernel<NB, kMmaUnroll, false, true>,
+    if ((e = cudaFuncSetAttribute(gemv_bf16_mma_kernel<NB, kMmaUnroll, false, kXBulk>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem)) != cudaSuccess)
         return e;
+    if constexpr (NB == 2) {
+        if ((e = cudaFuncSetAttribute(gemv_bf16_mma_kernel<NB, kMmaUnroll, false, kXBox>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem)) != cudaSuccess)
+            return e;
+    }
     return cudaFuncSetAttribute(gemv_bf16_mma_kernel<NB, kMmaUnroll, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
 }

@@ -28,7 +28,12 @@
 //                               deep one applies), streamk=<0|1> (batch-1 BF16
 //                               calls: the stream-K kernel or not), planwait=1
 //                               (every launch of a plan waits for the
-//                               preceding grid, even in an independent plan).
+//                               preceding grid, even in an independent plan),
+//                               xbox=<0|1|2> (BF16 tensor-core path, more than
+//                               8 rows of x: x staged by bulk copies per row,
+//                               as narrow or as wide tensor boxes, where boxes
+//                               apply), xpieces=<1..8> (the most mbarrier-counted
+//                               pieces of those boxes per CTA).
 // A value the planner cannot use makes every plan fail with GEMV_ERR_INVALID,
 // so that a mistyped sweep stops instead of timing the default.
 #include <cstdint>
@@ -48,6 +53,8 @@ struct Overrides {
     int unroll = 0;            // 0: the rules decide
     int streamk = -1;          // -1: the rules decide
     int planwait = 0;          // 1: plans keep every wait for the preceding grid
+    int xbox = -1;             // -1: the rules decide
+    int xpieces = 0;           // 0: kMaxXPieces
     bool bad = false;
 };
 
@@ -93,6 +100,10 @@ Overrides read_overrides() {
                 o.streamk = static_cast<int>(v);
             } else if (num && klen == 8 && std::strncmp(p, "planwait", 8) == 0 && (v == 0 || v == 1)) {
                 o.planwait = static_cast<int>(v);
+            } else if (num && klen == 4 && std::strncmp(p, "xbox", 4) == 0 && v >= 0 && v <= 2) {
+                o.xbox = static_cast<int>(v);
+            } else if (num && klen == 7 && std::strncmp(p, "xpieces", 7) == 0 && v >= 1 && v <= kMaxXPieces) {
+                o.xpieces = static_cast<int>(v);
             } else {
                 o.bad = true;
                 break;
@@ -327,6 +338,53 @@ int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight
     // BF16 tensor-core and FP8 paths with x in one chunk of whole 16-byte
     // vectors: bulk copies of x (the front end checks the pointer itself).
     out->xbulk = ((path == kPathMma || path == kPathFp8) && nbuf == 1 && K % 8 == 0) ? 1 : 0;
+    out->xbox = 0;
+    out->xper = 0;
+    out->xbpp = 0;
+    out->smem_rows = static_cast<int32_t>(smem);
+    // BF16 tensor-core path with more than 8 rows of x (the largest slices) in
+    // a grid of one wave (every CTA waits for its x at the same moment, with
+    // the HBM idle), x in one chunk and K a multiple of 32 (whole blocks, so
+    // the 3-D view of x stays inside every row): x as tensor boxes of 8
+    // blocks, in up to kMaxXPieces pieces (stage_x_boxes), where the box
+    // layout needs no more CTAs' worth of shared memory per SM than the padded
+    // rows. Wide boxes (256 columns) need K a multiple of 256 and warp groups
+    // that start on a box. The front end checks the pointer and builds the
+    // tensor map. Measured (us, row bulk copies / boxes, graph-replayed
+    // chains) at B = 16: 4096 x 14336 22.4-22.7 / 22.0-22.4, 6144 x 4096
+    // 12.6 / 12.1-12.2, 4096 x 4096 8.7 / 8.3-8.5; grids of several waves
+    // lost (28672 x 4096 55.8 / 56.5, 128256 x 4096 197.2 / 200.5: there the
+    // later CTAs' copies overlap other CTAs' streams, and the boxes' shorter
+    // requests cost), and so did 8 rows and fewer (within 3% either way).
+    constexpr int64_t kMmaCtasByRegs = 2;   // up to 128 registers per thread at 256 threads
+    if (path == kPathMma && nbuf == 1 && K % 32 == 0 && B > 8 && ov.xbox != 0 &&
+        (grid <= kMmaCtasByRegs * sm_count || ov.xbox > 0)) {
+        const int64_t nblk = kslice / 32;
+        const int64_t span = cdiv(nblk, kw);
+        const int64_t boxes = cdiv(span, 8);                    // per warp group
+        const int cap = (ov.xpieces > 0 ? ov.xpieces : kMaxXPieces) / kw;
+        const int64_t per = boxes < cap ? boxes : (cap > 0 ? cap : 1);
+        const int64_t bpp = cdiv(boxes, per);
+        const int64_t region = static_cast<int64_t>(kw) * per * bpp * 8 * B * 32 * 2;
+        const int64_t smem_box = kBulkSmemHead + region + rows_per_cta * (B + 1) * kw * 4 +
+                                 (rows_per_cta * B + kMaxSplits) * 4 + kMiscFloats * 4;
+        // CTAs per SM: by shared memory, and at most 2 by registers.
+        constexpr int64_t kSmemPerSm = 228 * 1024, kReservedPerCta = 1024;
+        auto ctas = [&](int64_t b) {
+            const int64_t c = kSmemPerSm / (b + kReservedPerCta);
+            return c < kMmaCtasByRegs ? c : kMmaCtasByRegs;
+        };
+        const bool fits = smem_box <= kMaxDynSmem && 8 * bpp <= 256 && ctas(smem_box) >= ctas(smem);
+        // (every K-slice as long as the first where groups split it, so that the
+        // kernel's group starts, taken from its own slice, stay on a box)
+        const bool wide_ok = K % 256 == 0 && span % 8 == 0 && (kw == 1 || K % kslice == 0);
+        if (fits && (ov.xbox != 2 || wide_ok)) {
+            out->xbox = ov.xbox == 2 ? 2 : 1;
+            out->xper = static_cast<int32_t>(per);
+            out->xbpp = static_cast<int32_t>(bpp);
+            out->smem_bytes = static_cast<int32_t>(smem_box);
+        }
+    }
     return GEMV_OK;
 }
 

@@ -341,7 +341,22 @@ def test_force_variant(L, monkeypatch):
     assert binding.gemv_query_launch_ex(4096, 4096, 1, GB300_SMS, 0)["path"] == 3
     assert binding.gemv_query_launch_ex(4096, 4096, 2, GB300_SMS, 0)["path"] == 1
     assert binding.gemv_query_launch_ex(16, 65536, 1, GB300_SMS, 0)["path"] == 0      # x too long for it
-    for bad in ["mcast=3", "unroll=2", "streamk=2", "foo=1", "mcast", "mcast=", "mcast=2,,x=1"]:
+    # x of more than 8 rows as tensor boxes (narrow by default), pieces capped by xpieces
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", "")
+    q = binding.gemv_query_launch(4096, 14336, 16, GB300_SMS)
+    assert (q["xbox"], q["xpieces"], q["xboxes_per_piece"]) == (1, 7, 1)
+    assert binding.gemv_query_launch(4096, 14336, 8, GB300_SMS)["xbox"] == 0   # 8 rows: row copies
+    assert binding.gemv_query_launch(4096, 14352, 16, GB300_SMS)["xbox"] == 0  # K % 32 != 0
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", "xbox=2")
+    assert binding.gemv_query_launch(4096, 14336, 16, GB300_SMS)["xbox"] == 2
+    assert binding.gemv_query_launch(4096, 14368, 16, GB300_SMS)["xbox"] == 0  # wide needs K % 256 == 0
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", "xbox=0")
+    assert binding.gemv_query_launch(4096, 14336, 16, GB300_SMS)["xbox"] == 0
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", "xpieces=2")
+    q = binding.gemv_query_launch(4096, 14336, 16, GB300_SMS)
+    assert (q["xbox"], q["xpieces"], q["xboxes_per_piece"]) == (1, 2, 4)
+    for bad in ["mcast=3", "unroll=2", "streamk=2", "foo=1", "mcast", "mcast=", "mcast=2,,x=1", "xbox=3",
+                "xpieces=0", "xpieces=9"]:
         monkeypatch.setenv("GEMV_FORCE_VARIANT", bad)
         info = binding.gemv_launch_info()
         assert L.gemv_query_launch(4096, 14336, 1, GB300_SMS, ctypes.byref(info)) == binding.GEMV_ERR_INVALID, bad

@@ -80,7 +80,17 @@ def test_shared_memory_holds_the_combine_areas():
     for kind, N, K, B, q in launches():
         rows, kw = q["rows_per_cta"], q["warps_per_row"]
         if kind in ("bf16", "cc") and q["path"] in (0, 1):
-            need = (q["nbuf"] * B * q["xstride"] * 2 + rows * (B + 1) * kw * 4
+            if q["xbox"]:
+                # x as tensor boxes: kw groups x pieces x boxes of 8 blocks x B rows x 32 columns
+                xbytes = kw * q["xpieces"] * q["xboxes_per_piece"] * 8 * B * 32 * 2
+                assert q["nbuf"] == 1 and q["xpieces"] * kw <= 8, (kind, N, K, B, q)
+                # every warp group's blocks fit its pieces
+                nblk = q["kslice"] // 32
+                span = -(-nblk // kw)
+                assert q["xpieces"] * q["xboxes_per_piece"] * 8 >= span, (kind, N, K, B, q)
+            else:
+                xbytes = q["nbuf"] * B * q["xstride"] * 2
+            need = (xbytes + rows * (B + 1) * kw * 4
                     + (rows * B + K_MAX_SPLITS) * 4 + misc * 4)
             assert q["smem_bytes"] >= need, (kind, N, K, B, q)
         assert q["smem_bytes"] <= 112 * 1024

@@ -57,3 +57,22 @@ def test_forced_quantised_launches(monkeypatch, knobs, kind, N, K, B):
                                    threads=oracle.default_threads())
     torch.cuda.synchronize()
     gu.assert_parity(y.cpu().numpy(), y_ref, s, f"{kind} {knobs} N={N} K={K} B={B}")
+
+
+@pytest.mark.parametrize("variant", ["", "xbox=1", "xbox=2", "xbox=0", "xpieces=1", "xpieces=2", "xpieces=3",
+                                     "xbox=2,xpieces=2"])
+@pytest.mark.parametrize("N,K,B", [(4096, 14336, 16), (1000, 4096, 9), (333, 8192, 13), (4097, 4128, 16),
+                                   (2048, 14368, 11), (64, 65536, 16)])
+def test_x_as_tensor_boxes(monkeypatch, variant, N, K, B):
+    """More than 8 rows of x on the tensor cores: x copied as narrow or wide
+    tensor boxes in any number of pieces (or by row copies) gives the oracle's
+    result; shapes with ragged rows, K a multiple of 32 but not of 256, K-slices
+    of unequal length and odd batch sizes."""
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", variant)
+    W = inputs.weight(N, K, seed=N + B, device=DEV)
+    x = inputs.activations(B, K, seed=K + B, device=DEV)
+    q = binding.gemv_query_launch(N, K, B, _sms())
+    y = gu.gemv(W, x, K)
+    y_ref, s = gu.reference(W, x, K)
+    gu.assert_parity(y, y_ref, s, f"{variant} N={N} K={K} B={B} launch={q}")
+    assert binding.gemv_device_status(reset=True) == 0
