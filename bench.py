@@ -92,6 +92,8 @@ KERNEL_FILES = {   # the sources that make up each kernel family's launches
            "gemv_w4_instances.cu", "gemv_dispatch.cu"),
     "f8": ("gemv_internal.h", "gemv_common.cuh", "gemv_mma_kernel.cuh", "gemv_fp8_kernel.cuh",
            "gemv_fp8_instances.cu", "gemv_dispatch.cu"),
+    "tc": ("gemv_internal.h", "gemv_common.cuh", "gemv_tc_kernel.cuh", "gemv_tc_instances.cu",
+           "gemv_dispatch.cu"),
     "sk": ("gemv_internal.h", "gemv_common.cuh", "gemv_kernel.cuh", "gemv_streamk_kernel.cuh",
            "gemv_streamk_instances.cu", "gemv_dispatch.cu"),
 }
@@ -704,6 +706,8 @@ def run_ours(args) -> dict:
                 wk.N, wk.K, wk.B, sms,
                 binding.GEMV_FLAG_STREAMK if family == "sk" else
                 binding.GEMV_FLAG_CUDA_CORES if wk.cuda_cores else 0)
+    if launch and launch.get("path") == 5:
+        family = "tc"   # the planner chose the tcgen05 kernel for this shape
     src_hash = kernel_source_hash(family, launch)
     traffic = profiled_traffic(args.workload, src_hash)
     knobs = {k: v for k, v in os.environ.items() if k in ("GEMV_FORCE_SPLIT", "GEMV_FORCE_VARIANT", "GEMV_PDL")}
@@ -729,6 +733,7 @@ def run_ours(args) -> dict:
                      "kernel": ("gemv_w4_kernel (INT4 codes, BF16 tensor cores)" if family == "w4"
                                 else "gemv_fp8_kernel (E4M3 codes, BF16 tensor cores)" if family == "f8"
                                 else "gemv_streamk_kernel (CUDA cores, one-wave grid)" if family == "sk"
+                                else "gemv_tc_kernel (tcgen05, accumulator in tensor memory)" if family == "tc"
                                 else "gemv_bf16_kernel (CUDA cores)" if wk.B == 1 or family == "fma"
                                 else "gemv_bf16_mma_kernel (BF16 tensor cores)"),
                      "kernel_source_hash": src_hash},

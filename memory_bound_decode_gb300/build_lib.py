@@ -30,6 +30,7 @@ SOURCES = [
     "gemv_mma_instances_nb2.cu",
     "gemv_w4_instances.cu",
     "gemv_fp8_instances.cu",
+    "gemv_tc_instances.cu",
     "gemv_streamk_instances.cu",
     "gemv_noalloc.cu",
     "gemv_dispatch.cu",
@@ -37,6 +38,7 @@ SOURCES = [
     "gemv_api.cpp",
 ]
 HEADERS = ["gemv_internal.h", "gemv_common.cuh", "gemv_kernel.cuh", "gemv_mma_kernel.cuh", "gemv_w4_kernel.cuh",
+           "gemv_tc_kernel.cuh",
            "gemv_streamk_kernel.cuh", "gemv_fp8_kernel.cuh", os.path.join("..", "..", "include", "gemv.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

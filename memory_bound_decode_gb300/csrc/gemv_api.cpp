@@ -136,6 +136,29 @@ bool encode_x_boxes(CUtensorMap* map, const void* x, int64_t K, int B, int bpp, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The tcgen05 kernel's two 2-D views: W [N][ldw] in boxes of 64 columns x 128
+// rows and x [B][K] in boxes of 64 columns x 16 rows, both with the 128-byte
+// swizzle its shared-memory descriptors expect; columns past K and rows past N
+// (W) or B (x) are zero-filled. False if the driver rejects either.
+bool encode_tc_maps(CUtensorMap* wmap, CUtensorMap* xmap, const void* W, int64_t N, int64_t ldw, const void* x,
+                    int64_t K, int B) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint32_t elem[2] = {1, 1};
+    const cuuint64_t wdims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N)};
+    const cuuint64_t wstride[1] = {static_cast<cuuint64_t>(ldw) * 2};
+    const cuuint32_t wbox[2] = {64, static_cast<cuuint32_t>(gemv::kTcRows)};
+    const cuuint64_t xdims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(B)};
+    const cuuint64_t xstride[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t xbox[2] = {64, static_cast<cuuint32_t>(gemv::kTcN)};
+    return fn(wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), wdims, wstride, wbox, elem,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
+           fn(xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), xdims, xstride, xbox, elem,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Whether p points into device memory of the current device: the x multicast
 // and the tensor copies of x read from there only (a pointer into mapped host
 // or managed memory takes the per-CTA staging instead).
@@ -279,10 +302,19 @@ int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B
         return GEMV_OK;
     Launch l;
     const int kind = (flags & GEMV_FLAG_CUDA_CORES) ? gemv::kWeightBf16CudaCores : gemv::kWeightBf16;
-    if ((rc = gemv::plan_launch(total, K, B, sm_count, &l, kind, overlap)) != GEMV_OK) return rc;
+    // The tcgen05 kernel takes one weight matrix without the RMSNorm prologue,
+    // W and x in this GPU's memory (its tensor copies read from there only), x
+    // rows of whole 16-byte vectors.
+    const bool allow_tc = nsegs == 1 && B >= 2 && kind == gemv::kWeightBf16 && !(flags & GEMV_FLAG_RMSNORM) &&
+                          K % 8 == 0 && aligned(x, 16) && on_current_device(x) && on_current_device(segs[0].W);
+    if ((rc = gemv::plan_launch(total, K, B, sm_count, &l, kind, overlap, allow_tc)) != GEMV_OK) return rc;
 
     Params p;
     std::memset(&p, 0, sizeof p);
+    if (l.path == gemv::kPathTc &&
+        !encode_tc_maps(&p.wmap, &p.xmap, segs[0].W, segs[0].N, segs[0].ldw, x, K, B)) {
+        if ((rc = gemv::plan_launch(total, K, B, sm_count, &l, kind, overlap, false)) != GEMV_OK) return rc;
+    }
     int64_t tiles = 0;
     for (int i = 0; i < nsegs; ++i) {
         p.seg[i].W = static_cast<const uint16_t*>(segs[i].W);
@@ -969,7 +1001,8 @@ int gemv_query_launch(int64_t N, int64_t K, int B, int sm_count, gemv_launch_inf
     if (!out) return GEMV_ERR_INVALID;
     std::memset(out, 0, sizeof *out);
     Launch l;
-    int rc = gemv::plan_launch(N, K, B, sm_count, &l);
+    // As a call with one weight matrix and aligned operands in this GPU's memory.
+    int rc = gemv::plan_launch(N, K, B, sm_count, &l, gemv::kWeightBf16, false, B >= 2 && K % 8 == 0);
     if (rc != GEMV_OK) return rc;
     fill_info(l, out);
     return GEMV_OK;
@@ -1089,13 +1122,14 @@ int gemv_device_status(unsigned int* bits, int reset) {
     if (!bits) return GEMV_ERR_INVALID;
     *bits = 0;
     // Each kernel translation unit keeps its own status word.
-    unsigned int b1 = 0, b2 = 0, b3 = 0, b4 = 0;
+    unsigned int b1 = 0, b2 = 0, b3 = 0, b4 = 0, b5 = 0;
     cudaError_t e = gemv::read_fma_status(&b1, reset != 0);
     if (e == cudaSuccess) e = gemv::read_mma_status_nb1(&b2, reset != 0);
     if (e == cudaSuccess) e = gemv::read_mma_status_nb2(&b3, reset != 0);
     if (e == cudaSuccess) e = gemv::read_fp8_status(&b4, reset != 0);
+    if (e == cudaSuccess) e = gemv::read_tc_status(&b5, reset != 0);
     if (e != cudaSuccess) return cuda_fail(e);
-    *bits = b1 | b2 | b3 | b4;
+    *bits = b1 | b2 | b3 | b4 | b5;
     return GEMV_OK;
 }
 

@@ -16,12 +16,15 @@ cudaError_t launch_w4_batch(int B, const Params& p, const Launch& l, cudaStream_
 cudaError_t prepare_w4_all();
 cudaError_t launch_fp8_batch(int B, const Params& p, const Launch& l, cudaStream_t s, bool pdl);
 cudaError_t prepare_fp8_all();
+cudaError_t launch_tc_batch(const Params& p, const Launch& l, cudaStream_t s, bool pdl);
+cudaError_t prepare_tc_all();
 
 cudaError_t launch_gemv(int B, const Params& p, const Launch& l, cudaStream_t s, bool pdl) {
     if (B < 1 || B > kMaxBatch) return cudaErrorInvalidValue;
     if (l.path == kPathFma) return launch_fma_batch(B, p, l, s, pdl);
     if (l.path == kPathW4) return launch_w4_batch(B, p, l, s, pdl);
     if (l.path == kPathFp8) return launch_fp8_batch(B, p, l, s, pdl);
+    if (l.path == kPathTc) return launch_tc_batch(p, l, s, pdl);
     return mma_nblocks(B) == 1 ? launch_mma_nb1(p, l, s, pdl) : launch_mma_nb2(p, l, s, pdl);
 }
 
@@ -32,6 +35,7 @@ cudaError_t prepare_kernels(int /*device: attributes apply to the current device
     if ((e = prepare_w4_all()) != cudaSuccess) return e;
     if ((e = prepare_fp8_all()) != cudaSuccess) return e;
     if ((e = prepare_streamk()) != cudaSuccess) return e;
+    if ((e = prepare_tc_all()) != cudaSuccess) return e;
     return prepare_mma_nb2();
 }
 

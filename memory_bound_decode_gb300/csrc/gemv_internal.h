@@ -57,7 +57,9 @@ struct Params {
     int32_t xbpp;     // ... and boxes of 8 blocks (256 columns) per piece
     int32_t xwide;    // ... 1: boxes of 256 columns x B rows, 0: of 32 columns x B rows (stage_x_boxes)
     WriteCount wc;
-    CUtensorMap xmap; // ... and the 3-D view of x the boxes are copied through (stage_x_boxes)
+    CUtensorMap xmap; // ... and the 3-D view of x the boxes are copied through (stage_x_boxes);
+                      // path 5: x as [B][K] in boxes of 64 columns x 16 rows
+    CUtensorMap wmap; // path 5: W as [N][ldw] in boxes of 64 columns x 128 rows
 };
 
 // The BF16 tensor-core kernel's x, copied as tensor boxes, lands in up to
@@ -99,7 +101,23 @@ enum Path : int32_t {
     kPathW4 = 2,        // INT4 weights dequantised to BF16 in registers, tensor-core mma.sync
     kPathStreamK = 3,   // batch 1, one wave of CTAs, warps take balanced ranges of (row, K-unit)
     kPathFp8 = 4,       // FP8 (E4M3) weights widened to BF16 in registers, tensor-core mma.sync
+    kPathTc = 5,        // BF16, 2..16 rows of x: W streamed by tensor copies into a shared-memory
+                        // ring, tcgen05.mma with the accumulator in tensor memory
 };
+
+// The tcgen05 kernel (path 5): a CTA owns 128 weight rows (the MMA's M) and one
+// K-range, streamed in stages of 128 columns (two 64-column tensor boxes of W,
+// two of x, 128-byte swizzle) through a ring of kTcStages stages; x rows are
+// padded to 16 (the MMA's N; rows past B are zero-filled by the copies).
+constexpr int kTcRows = 128;
+constexpr int kTcN = 16;
+constexpr int kTcStageCols = 128;
+constexpr int kTcStages = 2;                     // ring depth unless the tcstages knob says otherwise
+constexpr int kTcWBox = kTcRows * 64 * 2;        // bytes of one W box (64 columns)
+constexpr int kTcXBox = kTcN * 64 * 2;           // bytes of one x box
+constexpr int kTcWStage = 2 * kTcWBox;           // 32 KB
+constexpr int kTcXStage = 2 * kTcXBox;           // 4 KB
+constexpr int32_t kTcMaxDynSmem = 227 * 1024;
 
 // Weight formats the planner knows.
 enum WeightKind : int32_t {
@@ -164,8 +182,15 @@ bool plan_force_wait();
 // Returns 0 and fills `out`, or a negative GEMV_ERR_* code.
 // overlap: the launch belongs to an independent plan of several launches
 // (see gemv_plan_create), whose neighbours run alongside it.
+// allow_tc: the call can take the tcgen05 kernel (one weight matrix, aligned
+// operands, no RMSNorm prologue); the rules (or the tc knob) decide whether it does.
 int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind = kWeightBf16,
-                bool overlap = false);
+                bool overlap = false, bool allow_tc = false);
+
+// Shared memory of a tcgen05 launch with batch B and a ring of `stages` (the
+// ring, the combine areas, the barriers and 1 KB to align the ring to 1,024
+// bytes).
+int64_t tc_smem_bytes(int B, int stages);
 
 // Stream-K launch (batch 1): the grid is one wave of GW warps. Rows (of all
 // segments, numbered consecutively) that fill whole rounds of GW are taken
@@ -237,6 +262,7 @@ cudaError_t read_fma_status(unsigned int* bits, bool reset);
 cudaError_t read_mma_status_nb1(unsigned int* bits, bool reset);
 cudaError_t read_mma_status_nb2(unsigned int* bits, bool reset);
 cudaError_t read_fp8_status(unsigned int* bits, bool reset);
+cudaError_t read_tc_status(unsigned int* bits, bool reset);
 cudaError_t launch_probe_read(const void* src, int64_t bytes, float* sink, int grid,
                               cudaStream_t s);
 

@@ -33,7 +33,11 @@
 //                               8 rows of x: x staged by bulk copies per row,
 //                               as narrow or as wide tensor boxes, where boxes
 //                               apply), xpieces=<1..8> (the most mbarrier-counted
-//                               pieces of those boxes per CTA).
+//                               pieces of those boxes per CTA), tc=<0|1> (BF16,
+//                               2..16 rows of x: the tcgen05 kernel or not, where
+//                               the call allows it; GEMV_FORCE_SPLIT's CTA count
+//                               applies to it, its warp count must be 1),
+//                               tcstages=<2..5> (its ring depth).
 // A value the planner cannot use makes every plan fail with GEMV_ERR_INVALID,
 // so that a mistyped sweep stops instead of timing the default.
 #include <cstdint>
@@ -55,6 +59,8 @@ struct Overrides {
     int planwait = 0;          // 1: plans keep every wait for the preceding grid
     int xbox = -1;             // -1: the rules decide
     int xpieces = 0;           // 0: kMaxXPieces
+    int tc = -1;               // -1: the rules decide
+    int tcstages = 0;          // 0: kTcStages
     bool bad = false;
 };
 
@@ -104,6 +110,10 @@ Overrides read_overrides() {
                 o.xbox = static_cast<int>(v);
             } else if (num && klen == 7 && std::strncmp(p, "xpieces", 7) == 0 && v >= 1 && v <= kMaxXPieces) {
                 o.xpieces = static_cast<int>(v);
+            } else if (num && klen == 2 && std::strncmp(p, "tc", 2) == 0 && (v == 0 || v == 1)) {
+                o.tc = static_cast<int>(v);
+            } else if (num && klen == 8 && std::strncmp(p, "tcstages", 8) == 0 && v >= 2 && v <= 5) {
+                o.tcstages = static_cast<int>(v);
             } else {
                 o.bad = true;
                 break;
@@ -128,11 +138,66 @@ int64_t round_up(int64_t a, int64_t m) { return cdiv(a, m) * m; }
 namespace {
 int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind, int q_unroll,
               const Overrides& ov, bool overlap);
+
+// The tcgen05 kernel: one 128-row tile per CTA, one or two CTAs per SM by the
+// ring's shared memory, only where the row tiles fit one wave; the K-range is
+// split over a cluster of a power of two, up to 8 CTAs, so that the grid
+// fills the SMs (slices of whole 128-column stages). Clusters of 3 and 6 CTAs
+// measured far slower (6144 x 4096 at B = 16: 17.3-18.8 us against 11.4 with
+// 4).
+int plan_tc(int64_t N, int64_t K, int B, int sm_count, Launch* out, const Overrides& ov) {
+    const int stages = ov.tcstages > 0 ? ov.tcstages : kTcStages;
+    const int64_t smem = tc_smem_bytes(B, stages);
+    constexpr int64_t kSmemPerSm = 228 * 1024, kReservedPerCta = 1024;
+    int64_t per_sm = kSmemPerSm / (smem + kReservedPerCta);
+    if (per_sm > 2) per_sm = 2;
+    const int64_t tiles = cdiv(N, kTcRows);
+    if (per_sm < 1 || tiles > per_sm * sm_count || ov.kw > 1) return GEMV_ERR_UNSUPPORTED;
+    int64_t S = ov.splits;
+    if (S == 0) {
+        S = 1;
+        while (S < kMaxSplits && tiles * S * 2 <= per_sm * sm_count) S *= 2;
+    }
+    const int64_t kslice = round_up(cdiv(K, S), kTcStageCols);
+    S = cdiv(K, kslice);
+    out->rows_per_cta = kTcRows;
+    out->row_tiles = tiles;
+    out->grid = tiles * S;
+    out->kslice = kslice;
+    out->kchunk = kslice;
+    out->kw = 1;
+    out->splits = static_cast<int32_t>(S);
+    out->rows_per_warp = kTcRows;
+    out->unroll = stages;
+    out->smem_bytes = static_cast<int32_t>(smem);
+    out->path = kPathTc;
+    out->xstride = 0;
+    out->nbuf = 1;
+    out->mcast = 1;
+    out->xbulk = 0;
+    out->xbox = 0;
+    out->xper = 0;
+    out->xbpp = 0;
+    out->smem_rows = out->smem_bytes;
+    return out->smem_bytes <= kTcMaxDynSmem ? GEMV_OK : GEMV_ERR_UNSUPPORTED;
+}
 }  // namespace
 
-int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind, bool overlap) {
+int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind, bool overlap,
+                bool allow_tc) {
     const Overrides ov = read_overrides();
     if (ov.bad) return GEMV_ERR_INVALID;
+    if (!out || N < 1 || K < 1 || B < 1 || B > kMaxBatch || sm_count < 1) return GEMV_ERR_INVALID;
+    // BF16 with more than 8 rows of x (2..16 with the tc=1 knob): the tcgen05
+    // kernel where the call allows it and its grid of one wave fills the SMs.
+    // Measured (us, graph-replayed chains, register-fed tensor-core kernel /
+    // tcgen05 with a ring of 2 stages): B = 16 on 4096 x 14336 22.2 / 21.2,
+    // 4096 x 4096 8.5 / 8.3, 6144 x 4096 12.2 / 11.4, 28672 x 4096 54.9 / 39.0;
+    // 1024 x 4096 (64 CTAs) 4.4 / 5.6; 4096 x 14336 at B = 8 19.9 / 20.9 and at
+    // B = 2 19.1 / 20.4.
+    if (allow_tc && weight_kind == kWeightBf16 && B >= 2 && ov.tc != 0 && (B > 8 || ov.tc == 1) &&
+        plan_tc(N, K, B, sm_count, out, ov) == GEMV_OK && (ov.tc == 1 || out->grid >= sm_count))
+        return GEMV_OK;
     // A batch-1 launch of an independent plan runs alongside its neighbours
     // (no wait for the preceding grid): it needs only one streaming warp per
     // SM of its own, so K is split only for very few rows, and the quantised

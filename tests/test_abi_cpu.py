@@ -114,6 +114,17 @@ def test_plan_covers_the_problem(L, N, K, B):
     assert q["warps_per_cta"] * 32 == 256
     assert q["warps_per_row"] in (1, 2, 4, 8)
     assert 1 <= q["splits"] <= 8
+    if q["path"] == 5:
+        # the tcgen05 kernel: more than 8 rows of x, 128-row tiles, one wave that fills
+        # the SMs, a power-of-two cluster along K, slices of whole 128-column stages
+        assert B > 8 and q["rows_per_cta"] == 128 and q["warps_per_row"] == 1
+        assert q["row_tiles"] * 128 >= N > (q["row_tiles"] - 1) * 128
+        assert q["grid"] == q["row_tiles"] * q["splits"]
+        assert GB300_SMS <= q["grid"] <= 2 * GB300_SMS
+        assert q["splits"] in (1, 2, 4, 8) and q["kslice"] % 128 == 0
+        assert q["splits"] * q["kslice"] >= K > (q["splits"] - 1) * q["kslice"]
+        assert q["smem_bytes"] <= 227 * 1024
+        return
     # batch 1 on the CUDA cores, batches 2..16 on the BF16 tensor cores (16-row tiles)
     assert q["path"] == (0 if B == 1 else 1)
     assert q["rows_per_warp"] == (1 if B == 1 else 16)
@@ -341,22 +352,36 @@ def test_force_variant(L, monkeypatch):
     assert binding.gemv_query_launch_ex(4096, 4096, 1, GB300_SMS, 0)["path"] == 3
     assert binding.gemv_query_launch_ex(4096, 4096, 2, GB300_SMS, 0)["path"] == 1
     assert binding.gemv_query_launch_ex(16, 65536, 1, GB300_SMS, 0)["path"] == 0      # x too long for it
-    # x of more than 8 rows as tensor boxes (narrow by default), pieces capped by xpieces
+    # more than 8 rows of x: the tcgen05 kernel where its one-wave grid fills the SMs
     monkeypatch.setenv("GEMV_FORCE_VARIANT", "")
     q = binding.gemv_query_launch(4096, 14336, 16, GB300_SMS)
-    assert (q["xbox"], q["xpieces"], q["xboxes_per_piece"]) == (1, 7, 1)
+    assert (q["path"], q["splits"], q["unroll"]) == (5, 8, 2)
+    assert binding.gemv_query_launch(4096, 14336, 8, GB300_SMS)["path"] == 1     # 8 rows
+    assert binding.gemv_query_launch(1024, 4096, 16, GB300_SMS)["path"] == 1     # 64 CTAs only
+    assert binding.gemv_query_launch(128256, 4096, 16, GB300_SMS)["path"] == 1   # several waves
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", "tc=1")
+    q = binding.gemv_query_launch(4096, 14336, 2, GB300_SMS)
+    assert q["path"] == 5
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", "tc=1,tcstages=5")
+    q = binding.gemv_query_launch(4096, 14336, 16, GB300_SMS)
+    assert (q["path"], q["splits"], q["unroll"]) == (5, 4, 5)                     # one CTA per SM
+    # on the register-fed tensor-core path: x of more than 8 rows as tensor boxes
+    # (narrow by default), pieces capped by xpieces
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", "tc=0")
+    q = binding.gemv_query_launch(4096, 14336, 16, GB300_SMS)
+    assert (q["path"], q["xbox"], q["xpieces"], q["xboxes_per_piece"]) == (1, 1, 7, 1)
     assert binding.gemv_query_launch(4096, 14336, 8, GB300_SMS)["xbox"] == 0   # 8 rows: row copies
     assert binding.gemv_query_launch(4096, 14352, 16, GB300_SMS)["xbox"] == 0  # K % 32 != 0
-    monkeypatch.setenv("GEMV_FORCE_VARIANT", "xbox=2")
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", "tc=0,xbox=2")
     assert binding.gemv_query_launch(4096, 14336, 16, GB300_SMS)["xbox"] == 2
     assert binding.gemv_query_launch(4096, 14368, 16, GB300_SMS)["xbox"] == 0  # wide needs K % 256 == 0
-    monkeypatch.setenv("GEMV_FORCE_VARIANT", "xbox=0")
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", "tc=0,xbox=0")
     assert binding.gemv_query_launch(4096, 14336, 16, GB300_SMS)["xbox"] == 0
-    monkeypatch.setenv("GEMV_FORCE_VARIANT", "xpieces=2")
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", "tc=0,xpieces=2")
     q = binding.gemv_query_launch(4096, 14336, 16, GB300_SMS)
     assert (q["xbox"], q["xpieces"], q["xboxes_per_piece"]) == (1, 2, 4)
     for bad in ["mcast=3", "unroll=2", "streamk=2", "foo=1", "mcast", "mcast=", "mcast=2,,x=1", "xbox=3",
-                "xpieces=0", "xpieces=9"]:
+                "xpieces=0", "xpieces=9", "tc=2", "tcstages=1", "tcstages=6"]:
         monkeypatch.setenv("GEMV_FORCE_VARIANT", bad)
         info = binding.gemv_launch_info()
         assert L.gemv_query_launch(4096, 14336, 1, GB300_SMS, ctypes.byref(info)) == binding.GEMV_ERR_INVALID, bad

@@ -59,8 +59,8 @@ def test_forced_quantised_launches(monkeypatch, knobs, kind, N, K, B):
     gu.assert_parity(y.cpu().numpy(), y_ref, s, f"{kind} {knobs} N={N} K={K} B={B}")
 
 
-@pytest.mark.parametrize("variant", ["", "xbox=1", "xbox=2", "xbox=0", "xpieces=1", "xpieces=2", "xpieces=3",
-                                     "xbox=2,xpieces=2"])
+@pytest.mark.parametrize("variant", ["tc=0", "tc=0,xbox=1", "tc=0,xbox=2", "tc=0,xbox=0", "tc=0,xpieces=1",
+                                     "tc=0,xpieces=2", "tc=0,xpieces=3", "tc=0,xbox=2,xpieces=2"])
 @pytest.mark.parametrize("N,K,B", [(4096, 14336, 16), (1000, 4096, 9), (333, 8192, 13), (4097, 4128, 16),
                                    (2048, 14368, 11), (64, 65536, 16)])
 def test_x_as_tensor_boxes(monkeypatch, variant, N, K, B):

@@ -128,11 +128,14 @@ def test_multicast_only_from_device_memory_and_under_capture():
 
 @pytest.mark.parametrize("B", [2, 5, 8, 16])
 @pytest.mark.parametrize("N,K", [(4096, 14336), (1000, 4096), (300, 12288)])
-def test_tensor_core_bulk_x_copy(N, K, B):
-    """Batches of 2..16 copy x into shared memory with bulk copies when x is
-    16-byte aligned device memory of this GPU and K is a multiple of 8; x in
-    pinned host memory takes the per-thread staging. Same bits either way,
-    both against the oracle, and no wait ran out."""
+def test_tensor_core_bulk_x_copy(monkeypatch, N, K, B):
+    """Batches of 2..16 on the register-fed tensor-core kernel copy x into
+    shared memory with bulk copies (or tensor boxes) when x is 16-byte aligned
+    device memory of this GPU and K is a multiple of 8; x in pinned host memory
+    takes the per-thread staging. Same bits either way, both against the
+    oracle, and no wait ran out. (The tcgen05 kernel, which would take the
+    device-memory call at B = 16, is switched off here.)"""
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", "tc=0")
     ldw = inputs.padded_ldw(K)
     W = inputs.weight(N, K, ldw, seed=N + B, device=DEV)
     x = inputs.activations(B, K, seed=K + B, device=DEV)
