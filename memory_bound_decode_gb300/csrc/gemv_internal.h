@@ -111,12 +111,10 @@ enum Path : int32_t {
 // padded to 16 (the MMA's N; rows past B are zero-filled by the copies).
 constexpr int kTcRows = 128;
 constexpr int kTcN = 16;
-constexpr int kTcStageCols = 128;
+constexpr int kTcStageCols = 128;                // stage width unless the tccols knob says otherwise
 constexpr int kTcStages = 2;                     // ring depth unless the tcstages knob says otherwise
 constexpr int kTcWBox = kTcRows * 64 * 2;        // bytes of one W box (64 columns)
 constexpr int kTcXBox = kTcN * 64 * 2;           // bytes of one x box
-constexpr int kTcWStage = 2 * kTcWBox;           // 32 KB
-constexpr int kTcXStage = 2 * kTcXBox;           // 4 KB
 constexpr int32_t kTcMaxDynSmem = 227 * 1024;
 
 // Weight formats the planner knows.
@@ -172,6 +170,7 @@ struct Launch {
     int32_t xper;      // ... pieces per warp group along K
     int32_t xbpp;      // ... boxes of 8 blocks per piece
     int32_t smem_rows; // shared memory of the same launch with x staged row by row (no boxes)
+    int32_t stage_cols;// path 5: columns per ring stage (64 or 128); the ring depth is in `unroll`
 };
 
 // Sweep knob of the planner (GEMV_FORCE_VARIANT planwait=1): every launch of
@@ -187,10 +186,11 @@ bool plan_force_wait();
 int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind = kWeightBf16,
                 bool overlap = false, bool allow_tc = false);
 
-// Shared memory of a tcgen05 launch with batch B and a ring of `stages` (the
-// ring, the combine areas, the barriers and 1 KB to align the ring to 1,024
-// bytes).
-int64_t tc_smem_bytes(int B, int stages);
+// Shared memory of a tcgen05 launch with batch B and a ring of `stages` of
+// `stage_cols` columns (the ring, the combine areas, the barriers and 1 KB to
+// align the ring to 1,024 bytes), and whether that kernel instance exists.
+int64_t tc_smem_bytes(int B, int stages, int stage_cols);
+bool tc_has_instance(int stages, int stage_cols);
 
 // Stream-K launch (batch 1): the grid is one wave of GW warps. Rows (of all
 // segments, numbered consecutively) that fill whole rounds of GW are taken

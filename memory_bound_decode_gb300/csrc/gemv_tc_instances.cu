@@ -9,6 +9,8 @@ cudaError_t prepare_tc_all() { return prepare_tc(); }
 
 cudaError_t read_tc_status(unsigned int* bits, bool reset) { return read_tc_status_tu(bits, reset); }
 
-int64_t tc_smem_bytes(int B, int stages) { return tc_layout(B, stages).total; }
+int64_t tc_smem_bytes(int B, int stages, int stage_cols) { return tc_layout(B, stages, stage_cols).total; }
+
+bool tc_has_instance(int stages, int stage_cols) { return tc_instance(stages, stage_cols); }
 
 }  // namespace gemv

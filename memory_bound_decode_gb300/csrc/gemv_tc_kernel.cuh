@@ -91,6 +91,11 @@ __device__ __forceinline__ void tc_load16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Bytes of one ring stage of SC columns: W (SC / 64 boxes of 64 columns x
+// 128 rows) and x (SC / 64 boxes of 64 columns x 16 rows).
+__host__ __device__ constexpr uint32_t tc_wstage(int sc) { return static_cast<uint32_t>(sc / 64) * kTcWBox; }
+__host__ __device__ constexpr uint32_t tc_xstage(int sc) { return static_cast<uint32_t>(sc / 64) * kTcXBox; }
+
 // Byte offsets of the dynamic shared memory (after aligning its start to
 // 1,024 bytes): the W ring, the x ring, the combine areas, the barriers.
 struct TcLayout {
@@ -99,10 +104,10 @@ struct TcLayout {
 
 __host__ __device__ constexpr uint32_t tc_align(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
-__host__ __device__ inline TcLayout tc_layout(int B, int ns) {
+__host__ __device__ inline TcLayout tc_layout(int B, int ns, int sc) {
     TcLayout L{};
-    L.x_ring = static_cast<uint32_t>(ns) * kTcWStage;
-    L.red = L.x_ring + static_cast<uint32_t>(ns) * kTcXStage;
+    L.x_ring = static_cast<uint32_t>(ns) * tc_wstage(sc);
+    L.red = L.x_ring + static_cast<uint32_t>(ns) * tc_xstage(sc);
     L.cpart = L.red + static_cast<uint32_t>(kTcRows * (B + 1)) * 4u;
     L.misc = L.cpart + static_cast<uint32_t>(kTcRows * B + kMaxSplits) * 4u;
     L.bars = tc_align(L.misc + static_cast<uint32_t>(kMiscFloats) * 4u, 16u);
@@ -111,15 +116,16 @@ __host__ __device__ inline TcLayout tc_layout(int B, int ns) {
     return L;
 }
 
-template <int NS>
-__global__ void __launch_bounds__(kThreads, NS == 2 ? 2 : 1)
+template <int NS, int SC>
+__global__ void __launch_bounds__(kThreads, NS * SC <= 256 ? 2 : 1)
 gemv_tc_kernel(const __grid_constant__ Params p) {
+    constexpr uint32_t WST = tc_wstage(SC), XST = tc_xstage(SC);
     extern __shared__ __align__(1024) unsigned char smem_raw[];
 
     pdl_launch_dependents();
 
     const int B = p.batch;
-    const TcLayout L = tc_layout(B, NS);
+    const TcLayout L = tc_layout(B, NS, SC);
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     const uint32_t ring = smem_addr(sm);
@@ -157,9 +163,9 @@ gemv_tc_kernel(const __grid_constant__ Params p) {
     const int64_t K = p.K;
     const int64_t k0 = static_cast<int64_t>(split) * p.kslice;
     const int64_t k1 = (k0 + p.kslice < K) ? k0 + p.kslice : K;
-    const int nst = static_cast<int>((k1 - k0 + kTcStageCols - 1) / kTcStageCols);
+    const int nst = static_cast<int>((k1 - k0 + SC - 1) / SC);
     const int row0 = static_cast<int>(tile * kTcRows);
-    const uint32_t stage_bytes = static_cast<uint32_t>(kTcWStage + kTcXStage);
+    const uint32_t stage_bytes = WST + XST;
 
     if (threadIdx.x == 0) {
         // Producer. The first stages' W goes out before the wait for the
@@ -169,17 +175,19 @@ gemv_tc_kernel(const __grid_constant__ Params p) {
         for (int i = 0; i < NS; ++i) arms[i] = 0;
         auto issue_w = [&](int s) {
             const int slot = s % NS;
-            const int col = static_cast<int>(k0) + s * kTcStageCols;
-            const uint32_t w = ring + static_cast<uint32_t>(slot) * kTcWStage;
-            tensor_copy_2d(w, &p.wmap, col, row0, full + slot);
-            tensor_copy_2d(w + kTcWBox, &p.wmap, col + 64, row0, full + slot);
+            const int col = static_cast<int>(k0) + s * SC;
+            const uint32_t w = ring + static_cast<uint32_t>(slot) * WST;
+#pragma unroll
+            for (int b = 0; b < SC / 64; ++b)
+                tensor_copy_2d(w + static_cast<uint32_t>(b) * kTcWBox, &p.wmap, col + 64 * b, row0, full + slot);
         };
         auto issue_x = [&](int s) {
             const int slot = s % NS;
-            const int col = static_cast<int>(k0) + s * kTcStageCols;
-            const uint32_t x = ring + L.x_ring + static_cast<uint32_t>(slot) * kTcXStage;
-            tensor_copy_2d(x, &p.xmap, col, 0, full + slot);
-            tensor_copy_2d(x + kTcXBox, &p.xmap, col + 64, 0, full + slot);
+            const int col = static_cast<int>(k0) + s * SC;
+            const uint32_t x = ring + L.x_ring + static_cast<uint32_t>(slot) * XST;
+#pragma unroll
+            for (int b = 0; b < SC / 64; ++b)
+                tensor_copy_2d(x + static_cast<uint32_t>(b) * kTcXBox, &p.xmap, col + 64 * b, 0, full + slot);
         };
         const int npro = nst < NS ? nst : NS;
         for (int s = 0; s < npro; ++s) {
@@ -211,8 +219,8 @@ gemv_tc_kernel(const __grid_constant__ Params p) {
     }
 
     if (threadIdx.x == 32) {
-        // MMA issuer: 8 MMAs of K = 16 per stage (32 bytes along K within a
-        // 128-byte swizzled row; the second box 16 KB (W) / 2 KB (x) on).
+        // MMA issuer: SC / 16 MMAs of K = 16 per stage (32 bytes along K
+        // within a 128-byte swizzled row; each further box 16 KB (W) / 2 KB (x) on).
         int s = 0;
         for (; s < nst; ++s) {
             const int slot = s % NS;
@@ -221,10 +229,10 @@ gemv_tc_kernel(const __grid_constant__ Params p) {
                 break;
             }
             tc_fence_after();
-            const uint32_t w = ring + static_cast<uint32_t>(slot) * kTcWStage;
-            const uint32_t x = ring + L.x_ring + static_cast<uint32_t>(slot) * kTcXStage;
+            const uint32_t w = ring + static_cast<uint32_t>(slot) * WST;
+            const uint32_t x = ring + L.x_ring + static_cast<uint32_t>(slot) * XST;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
+            for (int k = 0; k < SC / 16; ++k) {
                 const uint32_t kb = static_cast<uint32_t>(k >> 2), kk = static_cast<uint32_t>(k & 3) * 32u;
                 tc_mma(tmem, tc_smem_desc(w + kb * kTcWBox + kk), tc_smem_desc(x + kb * kTcXBox + kk), (s | k) != 0);
             }
@@ -263,27 +271,32 @@ gemv_tc_kernel(const __grid_constant__ Params p) {
     }
 }
 
-// Instances by ring depth (Launch::unroll holds it): 2 stages leave room for
-// two CTAs per SM, 3 to 5 take one.
+// Instances by ring depth and stage width (Launch::unroll, Launch::stage_cols):
+// rings of up to 256 columns leave room for two CTAs per SM, deeper ones take one.
+#define GEMV_TC_INSTANCES(X) X(2, 128) X(3, 128) X(4, 128) X(5, 128) X(4, 64) X(8, 64) X(10, 64)
+
 inline cudaError_t launch_tc(const Params& p, const Launch& l, cudaStream_t s, bool pdl) {
-    switch (l.unroll) {
-        case 2: return launch_kernel(gemv_tc_kernel<2>, p, l, s, pdl);
-        case 3: return launch_kernel(gemv_tc_kernel<3>, p, l, s, pdl);
-        case 4: return launch_kernel(gemv_tc_kernel<4>, p, l, s, pdl);
-        case 5: return launch_kernel(gemv_tc_kernel<5>, p, l, s, pdl);
-        default: return cudaErrorInvalidValue;
-    }
+#define GEMV_TC_LAUNCH(ns, sc) \
+    if (l.unroll == ns && l.stage_cols == sc) return launch_kernel(gemv_tc_kernel<ns, sc>, p, l, s, pdl);
+    GEMV_TC_INSTANCES(GEMV_TC_LAUNCH)
+#undef GEMV_TC_LAUNCH
+    return cudaErrorInvalidValue;
 }
 
 inline cudaError_t prepare_tc() {
-    cudaError_t e = cudaFuncSetAttribute(gemv_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcMaxDynSmem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemv_tc_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcMaxDynSmem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemv_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcMaxDynSmem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemv_tc_kernel<5>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcMaxDynSmem);
+    cudaError_t e = cudaSuccess;
+#define GEMV_TC_PREPARE(ns, sc)                                                                            \
+    if (e == cudaSuccess)                                                                                   \
+        e = cudaFuncSetAttribute(gemv_tc_kernel<ns, sc>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                 kTcMaxDynSmem);
+    GEMV_TC_INSTANCES(GEMV_TC_PREPARE)
+#undef GEMV_TC_PREPARE
     return e;
+}
+
+// Whether an instance of this depth and width exists.
+__host__ __device__ constexpr bool tc_instance(int ns, int sc) {
+    return (sc == 128 && ns >= 2 && ns <= 5) || (sc == 64 && (ns == 4 || ns == 8 || ns == 10));
 }
 
 inline cudaError_t read_tc_status_tu(unsigned int* bits, bool reset) {

@@ -37,7 +37,8 @@
 //                               2..16 rows of x: the tcgen05 kernel or not, where
 //                               the call allows it; GEMV_FORCE_SPLIT's CTA count
 //                               applies to it, its warp count must be 1),
-//                               tcstages=<2..5> (its ring depth).
+//                               tcstages=<2..10> and tccols=<64|128> (its ring
+//                               depth and stage width, where an instance exists).
 // A value the planner cannot use makes every plan fail with GEMV_ERR_INVALID,
 // so that a mistyped sweep stops instead of timing the default.
 #include <cstdint>
@@ -61,6 +62,7 @@ struct Overrides {
     int xpieces = 0;           // 0: kMaxXPieces
     int tc = -1;               // -1: the rules decide
     int tcstages = 0;          // 0: kTcStages
+    int tccols = 0;            // 0: kTcStageCols
     bool bad = false;
 };
 
@@ -112,8 +114,10 @@ Overrides read_overrides() {
                 o.xpieces = static_cast<int>(v);
             } else if (num && klen == 2 && std::strncmp(p, "tc", 2) == 0 && (v == 0 || v == 1)) {
                 o.tc = static_cast<int>(v);
-            } else if (num && klen == 8 && std::strncmp(p, "tcstages", 8) == 0 && v >= 2 && v <= 5) {
+            } else if (num && klen == 8 && std::strncmp(p, "tcstages", 8) == 0 && v >= 2 && v <= 10) {
                 o.tcstages = static_cast<int>(v);
+            } else if (num && klen == 6 && std::strncmp(p, "tccols", 6) == 0 && (v == 64 || v == 128)) {
+                o.tccols = static_cast<int>(v);
             } else {
                 o.bad = true;
                 break;
@@ -147,7 +151,9 @@ int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight
 // 4).
 int plan_tc(int64_t N, int64_t K, int B, int sm_count, Launch* out, const Overrides& ov) {
     const int stages = ov.tcstages > 0 ? ov.tcstages : kTcStages;
-    const int64_t smem = tc_smem_bytes(B, stages);
+    const int cols = ov.tccols > 0 ? ov.tccols : kTcStageCols;
+    if (!tc_has_instance(stages, cols)) return GEMV_ERR_UNSUPPORTED;
+    const int64_t smem = tc_smem_bytes(B, stages, cols);
     constexpr int64_t kSmemPerSm = 228 * 1024, kReservedPerCta = 1024;
     int64_t per_sm = kSmemPerSm / (smem + kReservedPerCta);
     if (per_sm > 2) per_sm = 2;
@@ -169,6 +175,7 @@ int plan_tc(int64_t N, int64_t K, int B, int sm_count, Launch* out, const Overri
     out->splits = static_cast<int32_t>(S);
     out->rows_per_warp = kTcRows;
     out->unroll = stages;
+    out->stage_cols = cols;
     out->smem_bytes = static_cast<int32_t>(smem);
     out->path = kPathTc;
     out->xstride = 0;
@@ -407,6 +414,7 @@ int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight
     out->xper = 0;
     out->xbpp = 0;
     out->smem_rows = static_cast<int32_t>(smem);
+    out->stage_cols = 0;
     // BF16 tensor-core path with more than 8 rows of x (the largest slices) in
     // a grid of one wave (every CTA waits for its x at the same moment, with
     // the HBM idle), x in one chunk and K a multiple of 32 (whole blocks, so

@@ -381,7 +381,7 @@ def test_force_variant(L, monkeypatch):
     q = binding.gemv_query_launch(4096, 14336, 16, GB300_SMS)
     assert (q["xbox"], q["xpieces"], q["xboxes_per_piece"]) == (1, 2, 4)
     for bad in ["mcast=3", "unroll=2", "streamk=2", "foo=1", "mcast", "mcast=", "mcast=2,,x=1", "xbox=3",
-                "xpieces=0", "xpieces=9", "tc=2", "tcstages=1", "tcstages=6"]:
+                "xpieces=0", "xpieces=9", "tc=2", "tcstages=1", "tcstages=11", "tccols=96"]:
         monkeypatch.setenv("GEMV_FORCE_VARIANT", bad)
         info = binding.gemv_launch_info()
         assert L.gemv_query_launch(4096, 14336, 1, GB300_SMS, ctypes.byref(info)) == binding.GEMV_ERR_INVALID, bad
