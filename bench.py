@@ -256,12 +256,14 @@ def describe(workload: str):
     if workload in ("down_proj", "k_proj", "o_proj", "lm_head"):
         N, K = wl.SHAPES[workload]
         return "single", [N], K, 1
-    if workload == "qkv":
-        return "fused", [4096, 1024, 1024], 4096, 1
-    if workload == "gate_up":
-        return "fused", [14336, 14336], 4096, 1
-    if workload == "decode_step":
-        return "step", None, None, 1
+    m = re.fullmatch(r"(qkv|gate_up|decode_step)(?::B(\d+))?", workload)
+    if m:
+        B = int(m.group(2)) if m.group(2) else 1
+        if m.group(1) == "qkv":
+            return "fused", [4096, 1024, 1024], 4096, B
+        if m.group(1) == "gate_up":
+            return "fused", [14336, 14336], 4096, B
+        return "step", None, None, B
     m = re.fullmatch(r"skinny:(\d+)x(\d+):B(\d+)", workload)
     if m:
         return "single", [int(m.group(1))], int(m.group(2)), int(m.group(3))
@@ -366,11 +368,13 @@ class StepWorkload:
     """The full decode-step projection set replayed as one CUDA graph."""
 
     def __init__(self, device, stream, rms_eps=None, streamk=False, weights="bf16", data=None,
-                 keep_waits=False):
+                 keep_waits=False, batch=1):
         from memory_bound_decode_gb300 import workloads as wl
         self.spec = wl.decode_step_spec()
         self.weights = weights
-        self.data = data if data is not None else wl.DecodeStep(self.spec, seed=0, device=device, weights=weights)
+        self.data = data if data is not None else wl.DecodeStep(self.spec, seed=0, device=device, weights=weights,
+                                                                batch=batch)
+        batch = self.data.batch
         self.rms_eps = rms_eps
         self.streamk = streamk
         self.keep_waits = keep_waits
@@ -391,11 +395,11 @@ class StepWorkload:
         else:
             self.plan = self.data.plan(rms_eps=rms_eps, streamk=streamk)
         self.plan.capture(stream)
-        self.bytes_per_step = (wl.step_bytes_formula(self.spec) if weights == "bf16"
+        self.bytes_per_step = (wl.step_bytes_formula(self.spec, batch) if weights == "bf16"
                                else self.data.algorithmic_bytes())
         self.launches_per_step = self.plan.num_launches()
         self.x = None
-        self.B = 1
+        self.B = batch
 
     def step(self, i: int, stream, x=None) -> None:
         self.plan.launch(stream)
@@ -406,7 +410,8 @@ class StepWorkload:
         wt = {"bf16": "BF16", "fp8": "FP8 (E4M3, FP32 row scales)",
               "int4": "INT4 (128-col groups, BF16 scales)"}[self.weights]
         return {"workload": "decode step: 32 x {QKV 6144x4096, o 4096x4096, gate_up 28672x4096, "
-                            f"down 4096x14336}} + lm_head 128256x4096, {wt} weights, batch 1, one CUDA graph" + norm,
+                            f"down 4096x14336}} + lm_head 128256x4096, {wt} weights, batch {self.B}, "
+                            "one CUDA graph" + norm,
                 "launches_per_step": self.launches_per_step,
                 "l2": f"inputs larger than L2: {self.data.weight_bytes() / 1e9:.2f} GB of weights per step"}
 
@@ -613,7 +618,7 @@ def make_workload(torch, name: str, device, l2: int):
     _, w4 = split_w4(base)
     if kind == "step":
         return StepWorkload(device, torch.cuda.Stream(), rms_eps, streamk,
-                            "int4" if w4 else "fp8" if fp8 else "bf16")
+                            "int4" if w4 else "fp8" if fp8 else "bf16", batch=B)
     return GemvWorkload(kind, rows, K, B, device, l2, rms_eps, w4, streamk, fp8, cuda_cores)
 
 

@@ -136,26 +136,19 @@ bool encode_x_boxes(CUtensorMap* map, const void* x, int64_t K, int B, int bpp, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The tcgen05 kernel's two 2-D views: W [N][ldw] in boxes of 64 columns x 128
-// rows and x [B][K] in boxes of 64 columns x 16 rows, both with the 128-byte
+// The tcgen05 kernel's 2-D views: W [N][ldw] in boxes of 64 columns x 128 rows
+// and x [B][K] in boxes of 64 columns x 16 rows, both with the 128-byte
 // swizzle its shared-memory descriptors expect; columns past K and rows past N
-// (W) or B (x) are zero-filled. False if the driver rejects either.
-bool encode_tc_maps(CUtensorMap* wmap, CUtensorMap* xmap, const void* W, int64_t N, int64_t ldw, const void* x,
-                    int64_t K, int B) {
+// (W) or B (x) are zero-filled. False if the driver rejects the view.
+bool encode_tc_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows, int64_t ld, int box_rows) {
     const EncodeTiledFn fn = encode_tiled();
     if (!fn) return false;
     const cuuint32_t elem[2] = {1, 1};
-    const cuuint64_t wdims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N)};
-    const cuuint64_t wstride[1] = {static_cast<cuuint64_t>(ldw) * 2};
-    const cuuint32_t wbox[2] = {64, static_cast<cuuint32_t>(gemv::kTcRows)};
-    const cuuint64_t xdims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(B)};
-    const cuuint64_t xstride[1] = {static_cast<cuuint64_t>(K) * 2};
-    const cuuint32_t xbox[2] = {64, static_cast<cuuint32_t>(gemv::kTcN)};
-    return fn(wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), wdims, wstride, wbox, elem,
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t stride[1] = {static_cast<cuuint64_t>(ld) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, stride, box, elem,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
-           fn(xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), xdims, xstride, xbox, elem,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -302,18 +295,21 @@ int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B
         return GEMV_OK;
     Launch l;
     const int kind = (flags & GEMV_FLAG_CUDA_CORES) ? gemv::kWeightBf16CudaCores : gemv::kWeightBf16;
-    // The tcgen05 kernel takes one weight matrix without the RMSNorm prologue,
-    // W and x in this GPU's memory (its tensor copies read from there only), x
-    // rows of whole 16-byte vectors.
-    const bool allow_tc = nsegs == 1 && B >= 2 && kind == gemv::kWeightBf16 && !(flags & GEMV_FLAG_RMSNORM) &&
-                          K % 8 == 0 && aligned(x, 16) && on_current_device(x) && on_current_device(segs[0].W);
+    // The tcgen05 kernel takes calls without the RMSNorm prologue, with W and x
+    // in this GPU's memory (its tensor copies read from there only) and x rows
+    // of whole 16-byte vectors.
+    bool allow_tc = B >= 2 && kind == gemv::kWeightBf16 && !(flags & GEMV_FLAG_RMSNORM) && K % 8 == 0 &&
+                    aligned(x, 16) && on_current_device(x);
+    for (int i = 0; allow_tc && i < nsegs; ++i) allow_tc = on_current_device(segs[i].W);
     if ((rc = gemv::plan_launch(total, K, B, sm_count, &l, kind, overlap, allow_tc)) != GEMV_OK) return rc;
 
     Params p;
     std::memset(&p, 0, sizeof p);
-    if (l.path == gemv::kPathTc &&
-        !encode_tc_maps(&p.wmap, &p.xmap, segs[0].W, segs[0].N, segs[0].ldw, x, K, B)) {
-        if ((rc = gemv::plan_launch(total, K, B, sm_count, &l, kind, overlap, false)) != GEMV_OK) return rc;
+    if (l.path == gemv::kPathTc) {
+        bool ok = encode_tc_map(&p.xmap, x, K, B, K, gemv::kTcN);
+        for (int i = 0; ok && i < nsegs; ++i)
+            ok = encode_tc_map(&p.wmap[i], segs[i].W, K, segs[i].N, segs[i].ldw, gemv::kTcRows);
+        if (!ok && (rc = gemv::plan_launch(total, K, B, sm_count, &l, kind, overlap, false)) != GEMV_OK) return rc;
     }
     int64_t tiles = 0;
     for (int i = 0; i < nsegs; ++i) {

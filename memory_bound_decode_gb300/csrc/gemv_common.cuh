@@ -507,6 +507,7 @@ __device__ __forceinline__ void combine_and_store(const float* red, float* cpart
 
 // Segment of a (possibly fused) launch that owns row tile `tile`.
 struct SegView {
+    int si;              // segment index
     const uint16_t* W;
     float* y;
     int64_t N;
@@ -523,6 +524,7 @@ __device__ __forceinline__ SegView segment_of(const Params& p, int64_t tile) {
     for (int i = 1; i < p.nseg; ++i)
         if (tile >= p.seg[i].tile_begin) si = i;
     SegView s;
+    s.si = si;
     s.W = p.seg[si].W;
     s.y = p.seg[si].y;
     s.N = p.seg[si].N;

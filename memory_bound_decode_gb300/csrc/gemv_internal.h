@@ -59,7 +59,7 @@ struct Params {
     WriteCount wc;
     CUtensorMap xmap; // ... and the 3-D view of x the boxes are copied through (stage_x_boxes);
                       // path 5: x as [B][K] in boxes of 64 columns x 16 rows
-    CUtensorMap wmap; // path 5: W as [N][ldw] in boxes of 64 columns x 128 rows
+    CUtensorMap wmap[kMaxSegs];   // path 5: each segment's W as [N][ldw] in boxes of 64 columns x 128 rows
 };
 
 // The BF16 tensor-core kernel's x, copied as tensor boxes, lands in up to

@@ -12,7 +12,8 @@
 // of W are in flight before the wait for the preceding grid and keep landing
 // while x arrives.
 //
-// Roles in a CTA of 8 warps, one CTA per SM:
+// A CTA's tile belongs to one weight matrix of the launch (up to 8 share x,
+// each with its own tensor map). Roles in a CTA of 8 warps:
 //   thread 0      issues the tensor copies of each stage (W: two boxes of 64
 //                 columns x 128 rows; x: two boxes of 64 columns x 16 rows;
 //                 128-byte swizzle), counted on the stage's "full" mbarrier,
@@ -164,7 +165,9 @@ gemv_tc_kernel(const __grid_constant__ Params p) {
     const int64_t k0 = static_cast<int64_t>(split) * p.kslice;
     const int64_t k1 = (k0 + p.kslice < K) ? k0 + p.kslice : K;
     const int nst = static_cast<int>((k1 - k0 + SC - 1) / SC);
-    const int row0 = static_cast<int>(tile * kTcRows);
+    const SegView sg = segment_of(p, tile);
+    const int row0 = static_cast<int>(sg.tile_local * kTcRows);   // within the segment's W
+    const void* wmap = &p.wmap[sg.si];
     const uint32_t stage_bytes = WST + XST;
 
     if (threadIdx.x == 0) {
@@ -179,7 +182,7 @@ gemv_tc_kernel(const __grid_constant__ Params p) {
             const uint32_t w = ring + static_cast<uint32_t>(slot) * WST;
 #pragma unroll
             for (int b = 0; b < SC / 64; ++b)
-                tensor_copy_2d(w + static_cast<uint32_t>(b) * kTcWBox, &p.wmap, col + 64 * b, row0, full + slot);
+                tensor_copy_2d(w + static_cast<uint32_t>(b) * kTcWBox, wmap, col + 64 * b, row0, full + slot);
         };
         auto issue_x = [&](int s) {
             const int slot = s % NS;
@@ -260,7 +263,6 @@ gemv_tc_kernel(const __grid_constant__ Params p) {
         if (threadIdx.x == 0) atomicOr(&g_device_status, kStatusWaitTimeout);
         for (int i = threadIdx.x; i < kTcRows * (B + 1); i += kThreads) red[i] = __uint_as_float(0x7fc00000u);
     }
-    const SegView sg = segment_of(p, tile);
     combine_and_store(red, cpart, misc, kTcRows, B, 1, S, split, sg.tile_local * kTcRows, sg.N, sg.y, false, K,
                       p.rms_eps, p.wc);
     __syncthreads();

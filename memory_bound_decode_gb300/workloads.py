@@ -65,12 +65,15 @@ class DecodeStep:
     BF16, INT4 (128-column groups, BF16 scales) or FP8 (E4M3, FP32 row scales)
     weights."""
 
-    def __init__(self, spec: dict, seed: int = 0, device="cuda", weights: str = "bf16"):
+    def __init__(self, spec: dict, seed: int = 0, device="cuda", weights: str = "bf16", batch: int = 1):
         if weights not in WEIGHT_KINDS:
             raise ValueError(f"weights must be one of {sorted(WEIGHT_KINDS)}")
+        if not 1 <= batch <= binding.GEMV_MAX_BATCH:
+            raise ValueError("batch must be 1..16")
         self.spec = spec
         self.device = device
         self.weights = weights
+        self.batch = batch
         self.projs: list[Proj] = []
         self.xs: list[tuple[torch.Tensor, int]] = []
         H, I, V = spec["hidden"], spec["intermediate"], spec["vocab"]
@@ -79,15 +82,16 @@ class DecodeStep:
         # Every activation vector lives in one buffer and every output in
         # another (views at 16-byte multiples), so a step's inputs and outputs
         # each cross the host link as one copy (gemv_plan_launch_host_io).
-        self.x_arena = torch.empty(L * (H + I) + H, dtype=torch.bfloat16, device=device)
-        self.y_arena = torch.empty(L * (Q + 2 * KV + H + 2 * I + H) + V, dtype=torch.float32, device=device)
+        self.x_arena = torch.empty(batch * (L * (H + I) + H), dtype=torch.bfloat16, device=device)
+        self.y_arena = torch.empty(batch * (L * (Q + 2 * KV + H + 2 * I + H) + V), dtype=torch.float32,
+                                   device=device)
         self._x_off = 0
         self._y_off = 0
         group = 0
         for l in range(spec["layers"]):
             base = 16 * l
-            xh = self._x_view(inputs.activations(1, H, seed=seed, index=base + 14, device=device))
-            xi = self._x_view(inputs.activations(1, I, seed=seed, index=base + 15, device=device))
+            xh = self._x_view(inputs.activations(batch, H, seed=seed, index=base + 14, device=device))
+            xi = self._x_view(inputs.activations(batch, I, seed=seed, index=base + 15, device=device))
             self.xs += [(xh, base + 14), (xi, base + 15)]
             group += 1
             for j, (nm, n) in enumerate([("q", Q), ("k", KV), ("v", KV)]):
@@ -98,21 +102,21 @@ class DecodeStep:
             self._add(f"l{l}.up_proj", I, H, xh, group, seed, base + 5)
             self._add(f"l{l}.down_proj", H, I, xi, 0, seed, base + 6)
         base = 16 * spec["layers"]
-        xl = self._x_view(inputs.activations(1, H, seed=seed, index=base + 1, device=device))
+        xl = self._x_view(inputs.activations(batch, H, seed=seed, index=base + 1, device=device))
         self.xs.append((xl, base + 1))
         self._add("lm_head", V, H, xl, 0, seed, base)
         assert self._x_off == self.x_arena.numel() and self._y_off == self.y_arena.numel()
 
     def _x_view(self, x: torch.Tensor) -> torch.Tensor:
-        n = x.shape[1]
-        v = self.x_arena[self._x_off:self._x_off + n].view(1, n)
+        B, n = x.shape
+        v = self.x_arena[self._x_off:self._x_off + B * n].view(B, n)
         v.copy_(x)
-        self._x_off += n
+        self._x_off += B * n
         return v
 
     def _add(self, name, N, K, x, group, seed, index):
-        y = self.y_arena[self._y_off:self._y_off + N].view(1, N)
-        self._y_off += N
+        y = self.y_arena[self._y_off:self._y_off + self.batch * N].view(self.batch, N)
+        self._y_off += self.batch * N
         if self.weights == "bf16":
             ldw = inputs.padded_ldw(K)
             W = inputs.weight(N, K, ldw, seed=seed, index=index, device=self.device)
@@ -135,8 +139,8 @@ class DecodeStep:
             return rms_eps if (p.name.endswith(("q_proj", "k_proj", "v_proj", "gate_proj", "up_proj"))
                                or p.name == "lm_head") else None
         kind = WEIGHT_KINDS[self.weights]
-        return binding.Plan([(p.W, p.x, p.y, p.N, p.K, p.ldw, 1, p.group, eps_of(p), streamk, kind, p.S, p.lds)
-                             for p in self.projs], keepalive=self)
+        return binding.Plan([(p.W, p.x, p.y, p.N, p.K, p.ldw, self.batch, p.group, eps_of(p), streamk, kind, p.S,
+                              p.lds) for p in self.projs], keepalive=self)
 
     def outputs(self):
         return [p.y for p in self.projs]
@@ -144,7 +148,7 @@ class DecodeStep:
     def refresh_x(self, seed: int) -> None:
         """Overwrite every activation vector in place (the plan keeps its addresses)."""
         for x, index in self.xs:
-            x.copy_(inputs.activations(1, x.shape[1], seed=seed, index=index, device=self.device))
+            x.copy_(inputs.activations(self.batch, x.shape[1], seed=seed, index=index, device=self.device))
 
     def checks(self):
         for p in self.projs:
@@ -160,14 +164,14 @@ class DecodeStep:
         return p.N * p.K // 2 + 2 * p.N * (p.K // inputs.W4_GROUP)
 
     def algorithmic_bytes(self) -> int:
-        """Sum of weight bytes + K*2 + N*4 over the projections; a fused launch
-        moves its x once, so each launch group counts x once."""
+        """Sum of weight bytes + B*K*2 + B*N*4 over the projections; a fused
+        launch moves its x once, so each launch group counts x once."""
         total = 0
         seen_groups = set()
         for p in self.projs:
-            total += self._wbytes(p) + 4 * p.N
+            total += self._wbytes(p) + 4 * self.batch * p.N
             if p.group == 0 or p.group not in seen_groups:
-                total += 2 * p.K
+                total += 2 * self.batch * p.K
                 seen_groups.add(p.group)
         return total
 
@@ -175,11 +179,12 @@ class DecodeStep:
         return sum(self._wbytes(p) for p in self.projs)
 
 
-def step_bytes_formula(spec: dict) -> int:
-    """Algorithmic bytes of the step with fused groups counted as one GEMV each
-    (QKV 6,144 rows; gate/up 28,672 rows)."""
+def step_bytes_formula(spec: dict, batch: int = 1) -> int:
+    """Algorithmic bytes of the step at `batch` rows of x, with fused groups
+    counted as one GEMV each (QKV 6,144 rows; gate/up 28,672 rows)."""
     H, I, V = spec["hidden"], spec["intermediate"], spec["vocab"]
     Q, KV = spec["q_rows"], spec["kv_rows"]
-    layer = (roofline.algorithmic_bytes(Q + 2 * KV, H) + roofline.algorithmic_bytes(H, H)
-             + roofline.algorithmic_bytes(2 * I, H) + roofline.algorithmic_bytes(H, I))
-    return spec["layers"] * layer + roofline.algorithmic_bytes(V, H)
+    B = batch
+    layer = (roofline.algorithmic_bytes(Q + 2 * KV, H, B) + roofline.algorithmic_bytes(H, H, B)
+             + roofline.algorithmic_bytes(2 * I, H, B) + roofline.algorithmic_bytes(H, I, B))
+    return spec["layers"] * layer + roofline.algorithmic_bytes(V, H, B)

@@ -24,6 +24,10 @@ def _segments(rows, K, seed):
     ((14336, 14336), 4096, 1),          # gate, up
     ((7, 33, 1, 100), 4103, 3),         # ragged segments
     ((5,) * 8, 129, 2),                 # the most segments one launch takes
+    ((4096, 1024, 1024), 4096, 16),     # Q, K, V at batch 16 (the tcgen05 kernel, a tensor map per segment)
+    ((14336, 14336), 4096, 12),         # gate, up at batch 12 (tcgen05)
+    ((100, 257, 3000), 8192, 9),        # ragged segments (tcgen05)
+    ((5,) * 8, 136, 16),                # the most segments, each one partial tile (tcgen05)
 ])
 def test_fused_matches_oracle(rows, K, B):
     Ws, ldw = _segments(rows, K, seed=20)
@@ -91,6 +95,41 @@ def test_plan_errors():
     y_ref, sc = gu.reference(W, x, 64)
     gu.assert_parity(y.cpu().numpy(), y_ref, sc)
     plan.destroy()
+
+
+@pytest.mark.parametrize("batch", [16, 9])
+def test_batched_decode_step_every_element(batch):
+    """A decode step of two layers and the LM head at 16 (9) rows of x: the
+    layers' projections take the tcgen05 kernel (fused QKV and gate/up with a
+    tensor map per segment), the LM head, whose row tiles exceed one wave, the
+    register-fed tensor-core kernel. One captured graph, run end to end through
+    gemv_plan_launch_host_io; every output compared with the FP64 oracle."""
+    spec = workloads.decode_step_spec(layers=2)
+    step = workloads.DecodeStep(spec, seed=1, device=DEV, batch=batch)
+    plan = step.plan()
+    assert plan.num_launches() == 2 * 4 + 1
+    s = torch.cuda.Stream()
+    plan.capture(s)
+    x_host = step.x_arena.cpu().pin_memory()
+    y_host = torch.full(step.y_arena.shape, float("nan"), dtype=torch.float32).pin_memory()
+    step.y_arena.fill_(float("nan"))
+    torch.cuda.synchronize()
+    plan.launch_host_io(x_host, step.x_arena, x_host.numel() * 2, step.y_arena, y_host, y_host.numel() * 4, s)
+    assert torch.equal(y_host.view(torch.int32), step.y_arena.cpu().view(torch.int32))
+    threads = oracle.default_threads()
+    off = 0
+    for name, W, x, y, K in step.checks():
+        N = W.shape[0]
+        assert x.shape == (batch, K) and y.shape == (batch, N)
+        assert y.data_ptr() == step.y_arena.data_ptr() + 4 * off
+        y_ref, sc = oracle.gemv(inputs.bits(W), inputs.bits(x), K, threads=threads)
+        gu.assert_parity(y_host[off:off + batch * N].numpy().reshape(batch, N), y_ref, sc, name)
+        off += batch * N
+    assert off == step.y_arena.numel()
+    assert binding.gemv_device_status(reset=True) == 0
+    plan.destroy()
+    del step
+    torch.cuda.empty_cache()
 
 
 def test_full_decode_step_every_element():
