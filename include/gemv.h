@@ -360,6 +360,9 @@ typedef struct {
                                 smem_bytes to that of the row layout)             */
     int32_t xpieces;         /* xbox > 0: pieces per warp group along K           */
     int32_t xboxes_per_piece;/* xbox > 0: boxes per piece                         */
+    int32_t persistent;      /* path 5: 1 when the grid (fewer CTAs than row
+                                tiles) takes the tiles in turn, each CTA an equal
+                                share, over the whole K (splits == 1)             */
 } gemv_launch_info;
 
 int gemv_query_launch(int64_t N, int64_t K, int B, int sm_count,

@@ -333,6 +333,10 @@ int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B
     // The bulk copies of x read from a 16-byte boundary, and only from this GPU's memory.
     if (l.xbulk && (!aligned(x, 16) || !on_current_device(x))) l.xbulk = 0;
     l.grid = l.mcast > 1 ? (tiles + l.mcast - 1) / l.mcast * l.mcast : tiles * l.splits;
+    if (l.path == gemv::kPathTc && l.tc_persist) {   // equal shares of the tiles within the resident CTAs
+        const int64_t each = (tiles + l.tc_slots - 1) / l.tc_slots;
+        l.grid = (tiles + each - 1) / each;
+    }
     if (l.grid > 0x7fffffffLL) return GEMV_ERR_UNSUPPORTED;
     p.x = static_cast<const uint16_t*>(x);
     p.K = K;
@@ -496,6 +500,7 @@ void fill_info(const Launch& l, gemv_launch_info* out) {
     out->xbox = l.xbox;
     out->xpieces = l.xbox ? l.xper : 0;
     out->xboxes_per_piece = l.xbox ? l.xbpp : 0;
+    out->persistent = (l.path == gemv::kPathTc && l.tc_persist) ? 1 : 0;
 }
 
 }  // namespace

@@ -171,6 +171,8 @@ struct Launch {
     int32_t xbpp;      // ... boxes of 8 blocks per piece
     int32_t smem_rows; // shared memory of the same launch with x staged row by row (no boxes)
     int32_t stage_cols;// path 5: columns per ring stage (64 or 128); the ring depth is in `unroll`
+    int32_t tc_persist;// path 5: the persistent form (a fixed grid taking row tiles in turn, no K split)
+    int32_t tc_slots;  // ... CTAs resident at once (the grid takes equal shares of the tiles within them)
 };
 
 // Sweep knob of the planner (GEMV_FORCE_VARIANT planwait=1): every launch of
@@ -191,6 +193,9 @@ int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weig
 // align the ring to 1,024 bytes), and whether that kernel instance exists.
 int64_t tc_smem_bytes(int B, int stages, int stage_cols);
 bool tc_has_instance(int stages, int stage_cols);
+// Shared memory of the persistent tcgen05 launch with that ring (the ring, its
+// barriers, 1 KB of alignment); -1 where no such instance exists.
+int64_t tcp_smem_bytes(int stages, int stage_cols);
 
 // Stream-K launch (batch 1): the grid is one wave of GW warps. Rows (of all
 // segments, numbered consecutively) that fill whole rounds of GW are taken

@@ -13,4 +13,8 @@ int64_t tc_smem_bytes(int B, int stages, int stage_cols) { return tc_layout(B, s
 
 bool tc_has_instance(int stages, int stage_cols) { return tc_instance(stages, stage_cols); }
 
+int64_t tcp_smem_bytes(int stages, int stage_cols) {
+    return tcp_instance(stages, stage_cols) ? static_cast<int64_t>(tcp_total(stages, stage_cols)) : -1;
+}
+
 }  // namespace gemv

@@ -273,11 +273,218 @@ gemv_tc_kernel(const __grid_constant__ Params p) {
     }
 }
 
+// ---- persistent form: grids of more than one wave ---------------------------
+//
+// Where the row tiles exceed one wave, a fixed grid of G CTAs takes tiles in
+// turn (CTA c: tiles c, c + G, ...), each over the whole K (no split, no
+// combine): G is chosen so that every CTA gets the same number of tiles (up to
+// one fewer for the last few), where a grid of one CTA per tile would leave a
+// partial last wave. The ring keeps streaming across a CTA's tiles; the
+// accumulator alternates between two 16-column halves of tensor memory, so
+// the MMAs of tile i + 1 run while the epilogue warps read tile i (they
+// release each half on its "tfree" barrier) and store its outputs directly.
+
+__host__ __device__ inline uint32_t tcp_bars_offset(int ns, int sc) {
+    return static_cast<uint32_t>(ns) * (tc_wstage(sc) + tc_xstage(sc));
+}
+
+__host__ __device__ inline uint32_t tcp_total(int ns, int sc) {
+    return tcp_bars_offset(ns, sc) + static_cast<uint32_t>(2 * ns + 4) * 8u + 16u + 1024u;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(bar)) : "memory");
+}
+
+template <int NS, int SC>
+__global__ void __launch_bounds__(kThreads, NS * SC <= 256 ? 3 : 2)
+gemv_tcp_kernel(const __grid_constant__ Params p) {
+    constexpr uint32_t WST = tc_wstage(SC), XST = tc_xstage(SC);
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+
+    pdl_launch_dependents();
+
+    const int B = p.batch;
+    const uint32_t raw = smem_addr(smem_raw);
+    unsigned char* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const uint32_t ring = smem_addr(sm);
+    const uint32_t x_ring = static_cast<uint32_t>(NS) * WST;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + tcp_bars_offset(NS, SC));
+    uint64_t* empty = full + NS;
+    uint64_t* done = empty + NS;     // [2]
+    uint64_t* tfree = done + 2;      // [2]
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(tfree + 2);
+    volatile int* fail = reinterpret_cast<volatile int*>(tfree + 2) + 1;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 32;"
+                     :: "r"(smem_addr(tslot)) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2 * NS + 2; ++i) mbar_init(full + i, 1);
+        mbar_init(tfree, 4 * 32);
+        mbar_init(tfree + 1, 4 * 32);
+        *fail = 0;
+        fence_mbar_init_cluster();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    const int64_t K = p.K;
+    const int nst = static_cast<int>((K + SC - 1) / SC);
+    const int64_t tiles = p.seg[p.nseg - 1].tile_begin + (p.seg[p.nseg - 1].N + kTcRows - 1) / kTcRows;
+    const int64_t G = gridDim.x;
+    const int mine = static_cast<int>(blockIdx.x < tiles ? (tiles - 1 - blockIdx.x) / G + 1 : 0);
+    const uint32_t stage_bytes = WST + XST;
+
+    if (threadIdx.x == 0) {
+        // Producer: stage g of the CTA's sequence is stage g % nst of its tile
+        // g / nst; the first NS stages' W before the wait for the preceding grid.
+        int arms[NS];
+#pragma unroll
+        for (int i = 0; i < NS; ++i) arms[i] = 0;
+        auto issue = [&](int g, bool w, bool x) {
+            const int slot = g % NS;
+            const int64_t t = blockIdx.x + static_cast<int64_t>(g / nst) * G;
+            const int col = (g % nst) * SC;
+            if (w) {
+                const SegView sg = segment_of(p, t);
+                const uint32_t dst = ring + static_cast<uint32_t>(slot) * WST;
+#pragma unroll
+                for (int b = 0; b < SC / 64; ++b)
+                    tensor_copy_2d(dst + static_cast<uint32_t>(b) * kTcWBox, &p.wmap[sg.si], col + 64 * b,
+                                   static_cast<int>(sg.tile_local * kTcRows), full + slot);
+            }
+            if (x) {
+                const uint32_t dst = ring + x_ring + static_cast<uint32_t>(slot) * XST;
+#pragma unroll
+                for (int b = 0; b < SC / 64; ++b)
+                    tensor_copy_2d(dst + static_cast<uint32_t>(b) * kTcXBox, &p.xmap, col + 64 * b, 0, full + slot);
+            }
+        };
+        const int total = mine * nst;
+        const int npro = total < NS ? total : NS;
+        for (int g = 0; g < npro; ++g) {
+            mbar_arrive_expect_tx(full + g, stage_bytes);
+            ++arms[g];
+            issue(g, true, false);
+        }
+        if (!(p.flags & kFlagNoWait)) pdl_wait_prerequisites();
+        for (int g = 0; g < npro; ++g) issue(g, false, true);
+        for (int g = npro; g < total; ++g) {
+            const int slot = g % NS;
+            if (*fail || !mbar_wait_bounded(empty + slot, static_cast<uint32_t>((g / NS - 1) & 1))) {
+                *fail = 1;
+                break;
+            }
+            mbar_arrive_expect_tx(full + slot, stage_bytes);
+            ++arms[slot];
+            issue(g, true, true);
+        }
+#pragma unroll
+        for (int i = 0; i < NS; ++i)
+            if (arms[i] > 0 && !mbar_wait_bounded(full + i, static_cast<uint32_t>((arms[i] - 1) & 1))) *fail = 1;
+    } else {
+        // Every thread that stores y has waited for the preceding grid.
+        if (!(p.flags & kFlagNoWait)) pdl_wait_prerequisites();
+    }
+
+    if (threadIdx.x == 32) {
+        // MMA issuer: tile i accumulates into tensor-memory half i % 2, once
+        // the epilogue has released it (tile i - 2).
+        int g = 0;
+        for (int i = 0; i < mine && !*fail; ++i) {
+            const int buf = i & 1;
+            if (i >= 2 && !mbar_wait_bounded(tfree + buf, static_cast<uint32_t>((i / 2 - 1) & 1))) {
+                *fail = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d = tmem + static_cast<uint32_t>(buf * kTcN);
+            for (int s = 0; s < nst; ++s, ++g) {
+                const int slot = g % NS;
+                if (*fail || !mbar_wait_bounded(full + slot, static_cast<uint32_t>((g / NS) & 1))) {
+                    *fail = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t w = ring + static_cast<uint32_t>(slot) * WST;
+                const uint32_t x = ring + x_ring + static_cast<uint32_t>(slot) * XST;
+#pragma unroll
+                for (int k = 0; k < SC / 16; ++k) {
+                    const uint32_t kb = static_cast<uint32_t>(k >> 2), kk = static_cast<uint32_t>(k & 3) * 32u;
+                    tc_mma(d, tc_smem_desc(w + kb * kTcWBox + kk), tc_smem_desc(x + kb * kTcXBox + kk),
+                           (s | k) != 0);
+                }
+                tc_commit(empty + slot);
+            }
+            tc_commit(done + buf);
+        }
+        // Epilogue warps waiting for a tile that will not come: complete
+        // both halves' next phases (a commit with nothing pending arrives at
+        // once), so that their bounded waits end early.
+        if (*fail) {
+            tc_commit(done);
+            tc_commit(done + 1);
+        }
+    }
+
+    if (warp >= 4) {
+        // Epilogue: tile i's 128 x 16 accumulator from tensor-memory half i % 2
+        // into y, rows along the warp's lanes (coalesced per batch row).
+        const int q = warp - 4;
+        for (int i = 0; i < mine; ++i) {
+            const int buf = i & 1;
+            const bool ok = mbar_wait_bounded(done + buf, static_cast<uint32_t>((i / 2) & 1));
+            __syncwarp();
+            tc_fence_after();
+            float v[16];
+            tc_load16(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(buf * kTcN), v);
+            tc_fence_before();
+            mbar_arrive(tfree + buf);
+            if (!ok) *fail = 1;
+            const bool bad = *fail != 0;
+            const int64_t t = blockIdx.x + static_cast<int64_t>(i) * G;
+            const SegView sg = segment_of(p, t);
+            const int64_t n = sg.tile_local * kTcRows + 32 * q + lane;
+            if (n < sg.N) {
+#pragma unroll
+                for (int b = 0; b < 16; ++b)
+                    if (b < B) store_y(sg.y + static_cast<int64_t>(b) * sg.N + n, bad ? __uint_as_float(0x7fc00000u) : v[b], p.wc);
+            }
+            if (bad) break;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (*fail && threadIdx.x == 0) atomicOr(&g_device_status, kStatusWaitTimeout);
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 32;" :: "r"(tmem) : "memory");
+    }
+}
+
 // Instances by ring depth and stage width (Launch::unroll, Launch::stage_cols):
 // rings of up to 256 columns leave room for two CTAs per SM, deeper ones take one.
 #define GEMV_TC_INSTANCES(X) X(2, 128) X(3, 128) X(4, 128) X(5, 128) X(4, 64) X(8, 64) X(10, 64)
 
+// Persistent-form instances (ring depth, stage width).
+#define GEMV_TCP_INSTANCES(X) X(2, 128) X(3, 128) X(4, 128)
+
 inline cudaError_t launch_tc(const Params& p, const Launch& l, cudaStream_t s, bool pdl) {
+    if (l.tc_persist) {
+#define GEMV_TCP_LAUNCH(ns, sc) \
+    if (l.unroll == ns && l.stage_cols == sc) return launch_kernel(gemv_tcp_kernel<ns, sc>, p, l, s, pdl);
+        GEMV_TCP_INSTANCES(GEMV_TCP_LAUNCH)
+#undef GEMV_TCP_LAUNCH
+        return cudaErrorInvalidValue;
+    }
 #define GEMV_TC_LAUNCH(ns, sc) \
     if (l.unroll == ns && l.stage_cols == sc) return launch_kernel(gemv_tc_kernel<ns, sc>, p, l, s, pdl);
     GEMV_TC_INSTANCES(GEMV_TC_LAUNCH)
@@ -293,8 +500,16 @@ inline cudaError_t prepare_tc() {
                                  kTcMaxDynSmem);
     GEMV_TC_INSTANCES(GEMV_TC_PREPARE)
 #undef GEMV_TC_PREPARE
+#define GEMV_TCP_PREPARE(ns, sc)                                                                           \
+    if (e == cudaSuccess)                                                                                   \
+        e = cudaFuncSetAttribute(gemv_tcp_kernel<ns, sc>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                 kTcMaxDynSmem);
+    GEMV_TCP_INSTANCES(GEMV_TCP_PREPARE)
+#undef GEMV_TCP_PREPARE
     return e;
 }
+
+__host__ __device__ constexpr bool tcp_instance(int ns, int sc) { return sc == 128 && ns >= 2 && ns <= 4; }
 
 // Whether an instance of this depth and width exists.
 __host__ __device__ constexpr bool tc_instance(int ns, int sc) {

@@ -158,7 +158,41 @@ int plan_tc(int64_t N, int64_t K, int B, int sm_count, Launch* out, const Overri
     int64_t per_sm = kSmemPerSm / (smem + kReservedPerCta);
     if (per_sm > 2) per_sm = 2;
     const int64_t tiles = cdiv(N, kTcRows);
-    if (per_sm < 1 || tiles > per_sm * sm_count || ov.kw > 1) return GEMV_ERR_UNSUPPORTED;
+    if (per_sm < 1 || ov.kw > 1) return GEMV_ERR_UNSUPPORTED;
+    if (tiles > per_sm * sm_count) {
+        // More tiles than one wave: the persistent form, a grid that gives
+        // every CTA the same number of tiles within the CTAs resident at once
+        // (by its shared memory, at most 3 per SM).
+        const int64_t psmem = tcp_smem_bytes(stages, cols);
+        if (psmem < 0 || ov.splits > 1) return GEMV_ERR_UNSUPPORTED;
+        int64_t pper = kSmemPerSm / (psmem + kReservedPerCta);
+        if (pper > 3) pper = 3;
+        const int64_t slots = pper * sm_count;
+        const int64_t each = cdiv(tiles, slots);
+        out->rows_per_cta = kTcRows;
+        out->row_tiles = tiles;
+        out->grid = cdiv(tiles, each);
+        out->kslice = round_up(K, kTcStageCols);
+        out->kchunk = out->kslice;
+        out->kw = 1;
+        out->splits = 1;
+        out->rows_per_warp = kTcRows;
+        out->unroll = stages;
+        out->stage_cols = cols;
+        out->smem_bytes = static_cast<int32_t>(psmem);
+        out->path = kPathTc;
+        out->xstride = 0;
+        out->nbuf = 1;
+        out->mcast = 1;
+        out->xbulk = 0;
+        out->xbox = 0;
+        out->xper = 0;
+        out->xbpp = 0;
+        out->smem_rows = out->smem_bytes;
+        out->tc_persist = 1;
+        out->tc_slots = static_cast<int32_t>(slots);
+        return GEMV_OK;
+    }
     int64_t S = ov.splits;
     if (S == 0) {
         S = 1;
@@ -176,6 +210,8 @@ int plan_tc(int64_t N, int64_t K, int B, int sm_count, Launch* out, const Overri
     out->rows_per_warp = kTcRows;
     out->unroll = stages;
     out->stage_cols = cols;
+    out->tc_persist = 0;
+    out->tc_slots = 0;
     out->smem_bytes = static_cast<int32_t>(smem);
     out->path = kPathTc;
     out->xstride = 0;
@@ -415,6 +451,8 @@ int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight
     out->xbpp = 0;
     out->smem_rows = static_cast<int32_t>(smem);
     out->stage_cols = 0;
+    out->tc_persist = 0;
+    out->tc_slots = 0;
     // BF16 tensor-core path with more than 8 rows of x (the largest slices) in
     // a grid of one wave (every CTA waits for its x at the same moment, with
     // the HBM idle), x in one chunk and K a multiple of 32 (whole blocks, so

@@ -115,12 +115,18 @@ def test_plan_covers_the_problem(L, N, K, B):
     assert q["warps_per_row"] in (1, 2, 4, 8)
     assert 1 <= q["splits"] <= 8
     if q["path"] == 5:
-        # the tcgen05 kernel: more than 8 rows of x, 128-row tiles, one wave that fills
-        # the SMs, a power-of-two cluster along K, slices of whole 128-column stages
+        # the tcgen05 kernel: more than 8 rows of x, 128-row tiles, a grid of one wave that
+        # fills the SMs; a power-of-two cluster along K, slices of whole 128-column stages;
+        # or, with more tiles than one wave, a persistent grid taking equal shares of them
         assert B > 8 and q["rows_per_cta"] == 128 and q["warps_per_row"] == 1
         assert q["row_tiles"] * 128 >= N > (q["row_tiles"] - 1) * 128
-        assert q["grid"] == q["row_tiles"] * q["splits"]
-        assert GB300_SMS <= q["grid"] <= 2 * GB300_SMS
+        assert GB300_SMS <= q["grid"] <= (3 if q["persistent"] else 2) * GB300_SMS
+        if q["persistent"]:
+            each = -(-q["row_tiles"] // q["grid"])
+            assert q["splits"] == 1 and q["row_tiles"] > 2 * GB300_SMS
+            assert (q["grid"] - 1) * each < q["row_tiles"] <= q["grid"] * each
+        else:
+            assert q["grid"] == q["row_tiles"] * q["splits"]
         assert q["splits"] in (1, 2, 4, 8) and q["kslice"] % 128 == 0
         assert q["splits"] * q["kslice"] >= K > (q["splits"] - 1) * q["kslice"]
         assert q["smem_bytes"] <= 227 * 1024
@@ -358,7 +364,8 @@ def test_force_variant(L, monkeypatch):
     assert (q["path"], q["splits"], q["unroll"]) == (5, 8, 2)
     assert binding.gemv_query_launch(4096, 14336, 8, GB300_SMS)["path"] == 1     # 8 rows
     assert binding.gemv_query_launch(1024, 4096, 16, GB300_SMS)["path"] == 1     # 64 CTAs only
-    assert binding.gemv_query_launch(128256, 4096, 16, GB300_SMS)["path"] == 1   # several waves
+    q = binding.gemv_query_launch(128256, 4096, 16, GB300_SMS)                  # several waves:
+    assert (q["path"], q["persistent"], q["grid"], q["splits"]) == (5, 1, 334, 1)  # 3 tiles per CTA
     monkeypatch.setenv("GEMV_FORCE_VARIANT", "tc=1")
     q = binding.gemv_query_launch(4096, 14336, 2, GB300_SMS)
     assert q["path"] == 5

@@ -28,6 +28,7 @@ def _segments(rows, K, seed):
     ((14336, 14336), 4096, 12),         # gate, up at batch 12 (tcgen05)
     ((100, 257, 3000), 8192, 9),        # ragged segments (tcgen05)
     ((5,) * 8, 136, 16),                # the most segments, each one partial tile (tcgen05)
+    ((20000, 20000, 77), 1024, 16),     # more row tiles than one wave (persistent tcgen05)
 ])
 def test_fused_matches_oracle(rows, K, B):
     Ws, ldw = _segments(rows, K, seed=20)

@@ -74,3 +74,21 @@ def test_tc_host_x_falls_back():
     gu.assert_parity(gu.gemv(W, x, K), y_ref, s, "device x")
     gu.assert_parity(gu.gemv(W, x.cpu().pin_memory(), K), y_ref, s, "host x")
     assert binding.gemv_device_status(reset=True) == 0
+
+
+@pytest.mark.parametrize("stages", ["", "tcstages=3", "tcstages=4,tc=1"])
+@pytest.mark.parametrize("N,K,B", [(128256, 4096, 16), (60000, 1024, 9), (58600, 520, 16), (58369, 136, 12)])
+def test_tc_persistent_parity(monkeypatch, N, K, B, stages):
+    """More row tiles than one wave: the persistent grid (each CTA an equal
+    share of the tiles, the accumulator alternating between two halves of
+    tensor memory) against the oracle, ragged rows and columns included, for
+    each ring the persistent form has."""
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", stages)
+    q = binding.gemv_query_launch(N, K, B, _sms())
+    assert q["path"] == 5 and q["persistent"] == 1, q
+    W = inputs.weight(N, K, seed=N + B, device=DEV)
+    x = inputs.activations(B, K, seed=B + 1, device=DEV)
+    y = gu.gemv(W, x, K)
+    y_ref, s = gu.reference(W, x, K)
+    gu.assert_parity(y, y_ref, s, f"tc persistent N={N} K={K} B={B} launch={q}")
+    assert binding.gemv_device_status(reset=True) == 0
