@@ -330,7 +330,14 @@ typedef struct {
     int32_t path;            /* 0: CUDA-core FP32 FMA (batch 1), 1: BF16 tensor-core MMA,
                                 2: INT4 weights on the BF16 tensor cores,
                                 3: stream-K, batch 1 (CUDA cores, one-wave grid),
-                                4: FP8 weights on the BF16 tensor cores */
+                                4: FP8 weights on the BF16 tensor cores,
+                                5: BF16, 9..16 rows of x (8 on matrices of at least
+                                16,384 rows): tcgen05 MMAs with the accumulator in
+                                tensor memory, W and x streamed through a
+                                shared-memory ring by tensor copies (calls with one
+                                or more weight matrices in this GPU's memory and x
+                                16-byte aligned there, K a multiple of 8, no
+                                RMSNorm prologue; 128-row tiles, warps_per_cta 8) */
     int32_t xstride;         /* shared-memory elements per staged x row           */
     int32_t nbuf;            /* x buffers: 2 when the K-range is staged in chunks */
     /* stream-K (path 3) only; zero otherwise: */

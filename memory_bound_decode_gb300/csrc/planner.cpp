@@ -238,7 +238,12 @@ int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weig
     // 4096 x 4096 8.5 / 8.3, 6144 x 4096 12.2 / 11.4, 28672 x 4096 54.9 / 39.0;
     // 1024 x 4096 (64 CTAs) 4.4 / 5.6; 4096 x 14336 at B = 8 19.9 / 20.9 and at
     // B = 2 19.1 / 20.4.
-    if (allow_tc && weight_kind == kWeightBf16 && B >= 2 && ov.tc != 0 && (B > 8 || ov.tc == 1) &&
+    // At 8 rows the tcgen05 kernel also wins on the widest matrices (µs, register-
+    // fed / tcgen05: 28672 x 4096 40.7 / 37.7, 19456 x 14336 101.0 / 83.0, the LM
+    // head shape 165.9 / 154.5), while on the narrower ones its fixed cost per
+    // launch still loses (4096 x 14336 19.9 / 20.9, 14336 x 4096 21.1 / 21.2).
+    const bool tc_rule = B > 8 || (B == 8 && N >= 16384);
+    if (allow_tc && weight_kind == kWeightBf16 && B >= 2 && ov.tc != 0 && (tc_rule || ov.tc == 1) &&
         plan_tc(N, K, B, sm_count, out, ov) == GEMV_OK && (ov.tc == 1 || out->grid >= sm_count))
         return GEMV_OK;
     // A batch-1 launch of an independent plan runs alongside its neighbours

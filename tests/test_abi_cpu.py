@@ -118,7 +118,7 @@ def test_plan_covers_the_problem(L, N, K, B):
         # the tcgen05 kernel: more than 8 rows of x, 128-row tiles, a grid of one wave that
         # fills the SMs; a power-of-two cluster along K, slices of whole 128-column stages;
         # or, with more tiles than one wave, a persistent grid taking equal shares of them
-        assert B > 8 and q["rows_per_cta"] == 128 and q["warps_per_row"] == 1
+        assert (B > 8 or (B == 8 and N >= 16384)) and q["rows_per_cta"] == 128 and q["warps_per_row"] == 1
         assert q["row_tiles"] * 128 >= N > (q["row_tiles"] - 1) * 128
         assert GB300_SMS <= q["grid"] <= (3 if q["persistent"] else 2) * GB300_SMS
         if q["persistent"]:
@@ -363,6 +363,7 @@ def test_force_variant(L, monkeypatch):
     q = binding.gemv_query_launch(4096, 14336, 16, GB300_SMS)
     assert (q["path"], q["splits"], q["unroll"]) == (5, 8, 2)
     assert binding.gemv_query_launch(4096, 14336, 8, GB300_SMS)["path"] == 1     # 8 rows
+    assert binding.gemv_query_launch(28672, 4096, 8, GB300_SMS)["path"] == 5     # 8 rows, a wide matrix
     assert binding.gemv_query_launch(1024, 4096, 16, GB300_SMS)["path"] == 1     # 64 CTAs only
     q = binding.gemv_query_launch(128256, 4096, 16, GB300_SMS)                  # several waves:
     assert (q["path"], q["persistent"], q["grid"], q["splits"]) == (5, 1, 334, 1)  # 3 tiles per CTA
