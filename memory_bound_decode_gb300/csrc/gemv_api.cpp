@@ -47,6 +47,7 @@ struct DeviceState {
     bool ready = false;
     int status = GEMV_OK;
     int sm_count = 0;
+    int32_t tc_clusters[4] = {-1, -1, -1, -1};   // resident clusters of 1, 2, 4, 8 tcgen05 CTAs
     Workspace ws;   // shared by direct stream-K calls on this device
 };
 
@@ -74,12 +75,25 @@ int device_state(int* sm_count) {
             return cuda_fail(e);
         } else {
             st.status = GEMV_OK;
+            for (int i = 0; i < 4; ++i) st.tc_clusters[i] = gemv::tc_max_active_clusters(1 << i);
         }
         st.sm_count = sms;
         st.ready = true;
     }
     *sm_count = st.sm_count;
     return st.status;
+}
+
+// The current device's resident-cluster counts for the tcgen05 kernel (set
+// once by device_state, read-only afterwards); null if the device is unknown.
+const int32_t* current_tc_clusters() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    const DeviceState& st = g_dev[dev];
+    return st.ready ? st.tc_clusters : nullptr;
 }
 
 bool pdl_enabled() {
@@ -301,7 +315,9 @@ int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B
     bool allow_tc = B >= 2 && kind == gemv::kWeightBf16 && !(flags & GEMV_FLAG_RMSNORM) && K % 8 == 0 &&
                     aligned(x, 16) && on_current_device(x);
     for (int i = 0; allow_tc && i < nsegs; ++i) allow_tc = on_current_device(segs[i].W);
-    if ((rc = gemv::plan_launch(total, K, B, sm_count, &l, kind, overlap, allow_tc)) != GEMV_OK) return rc;
+    if ((rc = gemv::plan_launch(total, K, B, sm_count, &l, kind, overlap, allow_tc, current_tc_clusters())) !=
+        GEMV_OK)
+        return rc;
 
     Params p;
     std::memset(&p, 0, sizeof p);
@@ -1002,8 +1018,13 @@ int gemv_query_launch(int64_t N, int64_t K, int B, int sm_count, gemv_launch_inf
     if (!out) return GEMV_ERR_INVALID;
     std::memset(out, 0, sizeof *out);
     Launch l;
-    // As a call with one weight matrix and aligned operands in this GPU's memory.
-    int rc = gemv::plan_launch(N, K, B, sm_count, &l, gemv::kWeightBf16, false, B >= 2 && K % 8 == 0);
+    // As a call with one weight matrix and aligned operands in this GPU's memory
+    // (with the current GPU's resident-cluster counts where there is one).
+    int dev_sms = 0;
+    const bool have_device = device_state(&dev_sms) == GEMV_OK;
+    if (!have_device) cudaGetLastError();
+    int rc = gemv::plan_launch(N, K, B, sm_count, &l, gemv::kWeightBf16, false, B >= 2 && K % 8 == 0,
+                               have_device ? current_tc_clusters() : nullptr);
     if (rc != GEMV_OK) return rc;
     fill_info(l, out);
     return GEMV_OK;

@@ -185,8 +185,10 @@ bool plan_force_wait();
 // (see gemv_plan_create), whose neighbours run alongside it.
 // allow_tc: the call can take the tcgen05 kernel (one weight matrix, aligned
 // operands, no RMSNorm prologue); the rules (or the tc knob) decide whether it does.
+// tc_clusters: clusters of 1, 2, 4 and 8 CTAs of the tcgen05 kernel the
+// device keeps resident at once (null: not known, no limit assumed).
 int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind = kWeightBf16,
-                bool overlap = false, bool allow_tc = false);
+                bool overlap = false, bool allow_tc = false, const int32_t* tc_clusters = nullptr);
 
 // Shared memory of a tcgen05 launch with batch B and a ring of `stages` of
 // `stage_cols` columns (the ring, the combine areas, the barriers and 1 KB to
@@ -196,6 +198,9 @@ bool tc_has_instance(int stages, int stage_cols);
 // Shared memory of the persistent tcgen05 launch with that ring (the ring, its
 // barriers, 1 KB of alignment); -1 where no such instance exists.
 int64_t tcp_smem_bytes(int stages, int stage_cols);
+// Clusters of S CTAs of the tcgen05 kernel the current device keeps resident at
+// once (cudaOccupancyMaxActiveClusters); -1 if unknown.
+int tc_max_active_clusters(int S);
 
 // Stream-K launch (batch 1): the grid is one wave of GW warps. Rows (of all
 // segments, numbered consecutively) that fill whole rounds of GW are taken

@@ -149,7 +149,8 @@ int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight
 // fills the SMs (slices of whole 128-column stages). Clusters of 3 and 6 CTAs
 // measured far slower (6144 x 4096 at B = 16: 17.3-18.8 us against 11.4 with
 // 4).
-int plan_tc(int64_t N, int64_t K, int B, int sm_count, Launch* out, const Overrides& ov) {
+int plan_tc(int64_t N, int64_t K, int B, int sm_count, Launch* out, const Overrides& ov,
+            const int32_t* tc_clusters) {
     const int stages = ov.tcstages > 0 ? ov.tcstages : kTcStages;
     const int cols = ov.tccols > 0 ? ov.tccols : kTcStageCols;
     if (!tc_has_instance(stages, cols)) return GEMV_ERR_UNSUPPORTED;
@@ -193,10 +194,18 @@ int plan_tc(int64_t N, int64_t K, int B, int sm_count, Launch* out, const Overri
         out->tc_slots = static_cast<int32_t>(slots);
         return GEMV_OK;
     }
+    // A cluster must fit in one GPC: with clusters of 4 or 8 CTAs fewer CTAs
+    // are resident at once than SMs x CTAs per SM (measured, B = 16: 9728 x 14336
+    // with 4 CTAs per cluster 60.3 us, with 2 47.9; 4864 x 14336 with 8 33.6, with
+    // 4 29.0), so the split also keeps the tiles' clusters resident at once.
+    auto fits = [&](int64_t s) {
+        const int li = s == 1 ? 0 : s == 2 ? 1 : s == 4 ? 2 : 3;
+        return tc_clusters == nullptr || tc_clusters[li] < 0 || tiles <= tc_clusters[li];
+    };
     int64_t S = ov.splits;
     if (S == 0) {
         S = 1;
-        while (S < kMaxSplits && tiles * S * 2 <= per_sm * sm_count) S *= 2;
+        while (S < kMaxSplits && tiles * S * 2 <= per_sm * sm_count && fits(S * 2)) S *= 2;
     }
     const int64_t kslice = round_up(cdiv(K, S), kTcStageCols);
     S = cdiv(K, kslice);
@@ -227,7 +236,7 @@ int plan_tc(int64_t N, int64_t K, int B, int sm_count, Launch* out, const Overri
 }  // namespace
 
 int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight_kind, bool overlap,
-                bool allow_tc) {
+                bool allow_tc, const int32_t* tc_clusters) {
     const Overrides ov = read_overrides();
     if (ov.bad) return GEMV_ERR_INVALID;
     if (!out || N < 1 || K < 1 || B < 1 || B > kMaxBatch || sm_count < 1) return GEMV_ERR_INVALID;
@@ -244,7 +253,7 @@ int plan_launch(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weig
     // launch still loses (4096 x 14336 19.9 / 20.9, 14336 x 4096 21.1 / 21.2).
     const bool tc_rule = B > 8 || (B == 8 && N >= 16384);
     if (allow_tc && weight_kind == kWeightBf16 && B >= 2 && ov.tc != 0 && (tc_rule || ov.tc == 1) &&
-        plan_tc(N, K, B, sm_count, out, ov) == GEMV_OK && (ov.tc == 1 || out->grid >= sm_count))
+        plan_tc(N, K, B, sm_count, out, ov, tc_clusters) == GEMV_OK && (ov.tc == 1 || out->grid >= sm_count))
         return GEMV_OK;
     // A batch-1 launch of an independent plan runs alongside its neighbours
     // (no wait for the preceding grid): it needs only one streaming warp per
