@@ -68,11 +68,21 @@ def _newest(paths) -> float:
 
 LIB_DEBUG = os.path.join(OUT_DIR, "libgemv_debug.so")
 DEBUG_FLAGS = ("-DGEMV_DEBUG_WRITECOUNT",)
+LIB_DEBUG_DROP_X = os.path.join(OUT_DIR, "libgemv_debug_drop_x.so")
+DROP_X_FLAGS = ("-DGEMV_DEBUG_DROP_X",)
 
 
 def build_debug(force: bool = False, verbose: bool = False) -> str:
     """The test build that counts output stores (gemv_debug_write_count)."""
     return build(force=force, verbose=verbose, extra_flags=DEBUG_FLAGS, lib=LIB_DEBUG)
+
+
+def build_debug_drop_x(force: bool = False, verbose: bool = False) -> str:
+    """The test build whose tcgen05 kernels never issue their copies of x: the
+    stages' barriers wait for bytes that never come, so the bounded waits run
+    out (limit 2^14 rounds in this build) and the kernel takes its failure
+    path: NaN outputs, the status bit, its tensor memory freed."""
+    return build(force=force, verbose=verbose, extra_flags=DROP_X_FLAGS, lib=LIB_DEBUG_DROP_X)
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=(), lib: str = LIB) -> str:

@@ -102,7 +102,11 @@ __device__ __forceinline__ int div_by_batch(int i, int B, uint32_t magic) {
 // cleared by the host through gemv_device_status.
 static __device__ unsigned int g_device_status;
 constexpr unsigned int kStatusWaitTimeout = 1u;
+#ifdef GEMV_DEBUG_DROP_X
+constexpr int kMbarWaitLimit = 1 << 14;      // the test build whose waits are meant to run out
+#else
 constexpr int kMbarWaitLimit = 1 << 20;      // try_wait rounds before giving up
+#endif
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -185,6 +185,9 @@ gemv_tc_kernel(const __grid_constant__ Params p) {
                 tensor_copy_2d(w + static_cast<uint32_t>(b) * kTcWBox, wmap, col + 64 * b, row0, full + slot);
         };
         auto issue_x = [&](int s) {
+#ifdef GEMV_DEBUG_DROP_X
+            return;   // the test build: x never arrives, the stage's wait runs out
+#endif
             const int slot = s % NS;
             const int col = static_cast<int>(k0) + s * SC;
             const uint32_t x = ring + L.x_ring + static_cast<uint32_t>(slot) * XST;
@@ -289,7 +292,7 @@ __host__ __device__ inline uint32_t tcp_bars_offset(int ns, int sc) {
 }
 
 __host__ __device__ inline uint32_t tcp_total(int ns, int sc) {
-    return tcp_bars_offset(ns, sc) + static_cast<uint32_t>(2 * ns + 4) * 8u + 16u + 1024u;
+    return tcp_bars_offset(ns, sc) + static_cast<uint32_t>(2 * ns + 5) * 8u + 16u + 1024u;
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -313,8 +316,9 @@ gemv_tcp_kernel(const __grid_constant__ Params p) {
     uint64_t* empty = full + NS;
     uint64_t* done = empty + NS;     // [2]
     uint64_t* tfree = done + 2;      // [2]
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(tfree + 2);
-    volatile int* fail = reinterpret_cast<volatile int*>(tfree + 2) + 1;
+    uint64_t* drain = tfree + 2;     // every MMA issued has completed (before tensor memory is freed)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* fail = reinterpret_cast<volatile int*>(drain + 1) + 1;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
@@ -327,6 +331,7 @@ gemv_tcp_kernel(const __grid_constant__ Params p) {
         for (int i = 0; i < 2 * NS + 2; ++i) mbar_init(full + i, 1);
         mbar_init(tfree, 4 * 32);
         mbar_init(tfree + 1, 4 * 32);
+        mbar_init(drain, 1);
         *fail = 0;
         fence_mbar_init_cluster();
     }
@@ -360,6 +365,9 @@ gemv_tcp_kernel(const __grid_constant__ Params p) {
                     tensor_copy_2d(dst + static_cast<uint32_t>(b) * kTcWBox, &p.wmap[sg.si], col + 64 * b,
                                    static_cast<int>(sg.tile_local * kTcRows), full + slot);
             }
+#ifdef GEMV_DEBUG_DROP_X
+            x = false;   // the test build: x never arrives, the stage's wait runs out
+#endif
             if (x) {
                 const uint32_t dst = ring + x_ring + static_cast<uint32_t>(slot) * XST;
 #pragma unroll
@@ -425,30 +433,39 @@ gemv_tcp_kernel(const __grid_constant__ Params p) {
             }
             tc_commit(done + buf);
         }
-        // Epilogue warps waiting for a tile that will not come: complete
-        // both halves' next phases (a commit with nothing pending arrives at
-        // once), so that their bounded waits end early.
+        // Epilogue warps waiting for a tile that will not come: an ordinary
+        // arrival (release: they see the failure flag) completes the phase they
+        // may be waiting on, so their bounded waits end early.
         if (*fail) {
-            tc_commit(done);
-            tc_commit(done + 1);
+            mbar_arrive(done);
+            mbar_arrive(done + 1);
         }
+        // Every MMA issued has completed before the tensor memory is freed.
+        tc_commit(drain);
+        if (!mbar_wait_bounded(drain, 0)) *fail = 1;
     }
 
     if (warp >= 4) {
         // Epilogue: tile i's 128 x 16 accumulator from tensor-memory half i % 2
         // into y, rows along the warp's lanes (coalesced per batch row).
+        // After a failure every remaining tile of the CTA is stored as NaN
+        // (no tensor memory read, no further wait).
         const int q = warp - 4;
         for (int i = 0; i < mine; ++i) {
             const int buf = i & 1;
-            const bool ok = mbar_wait_bounded(done + buf, static_cast<uint32_t>((i / 2) & 1));
-            __syncwarp();
-            tc_fence_after();
+            bool ok = *fail == 0 && mbar_wait_bounded(done + buf, static_cast<uint32_t>((i / 2) & 1));
+            ok = __all_sync(0xffffffffu, ok && *fail == 0);   // warp-uniform: the load below is warp-wide
             float v[16];
-            tc_load16(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(buf * kTcN), v);
-            tc_fence_before();
+#pragma unroll
+            for (int b = 0; b < 16; ++b) v[b] = 0.f;
+            if (ok) {
+                tc_fence_after();
+                tc_load16(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(buf * kTcN), v);
+                tc_fence_before();
+            }
             mbar_arrive(tfree + buf);
             if (!ok) *fail = 1;
-            const bool bad = *fail != 0;
+            const bool bad = !ok;
             const int64_t t = blockIdx.x + static_cast<int64_t>(i) * G;
             const SegView sg = segment_of(p, t);
             const int64_t n = sg.tile_local * kTcRows + 32 * q + lane;
@@ -457,7 +474,6 @@ gemv_tcp_kernel(const __grid_constant__ Params p) {
                 for (int b = 0; b < 16; ++b)
                     if (b < B) store_y(sg.y + static_cast<int64_t>(b) * sg.N + n, bad ? __uint_as_float(0x7fc00000u) : v[b], p.wc);
             }
-            if (bad) break;
         }
     }
     tc_fence_before();
