@@ -76,7 +76,8 @@ class gemv_launch_info(ctypes.Structure):
                 ("xstride", ctypes.c_int32), ("nbuf", ctypes.c_int32),
                 ("units", i64), ("warps", i64), ("chunks", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
                 ("dp_rounds", ctypes.c_int32), ("mcast", ctypes.c_int32), ("xbox", ctypes.c_int32),
-                ("xpieces", ctypes.c_int32), ("xboxes_per_piece", ctypes.c_int32), ("persistent", ctypes.c_int32)]
+                ("xpieces", ctypes.c_int32), ("xboxes_per_piece", ctypes.c_int32), ("persistent", ctypes.c_int32),
+                ("l2_prefetch", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -370,6 +370,10 @@ int prepare(const gemv_segment* segs, int nsegs, const void* x, int64_t K, int B
     p.xper = l.xbox ? l.xper : 0;
     p.xbpp = l.xbox ? l.xbpp : 0;
     p.xwide = l.xbox == 2 ? 1 : 0;
+    // The bulk prefetch of W reads only from this GPU's memory.
+    for (int i = 0; l.l2pf && i < nsegs; ++i)
+        if (!on_current_device(segs[i].W)) l.l2pf = 0;
+    p.l2pf = l.l2pf;
     p.wc = g_write_count;
     out->p = p;
     out->l = l;
@@ -435,6 +439,10 @@ int prepare_quant(int kind, const QSeg* segs, int nsegs, const void* x, int64_t 
     p.flags = (flags & GEMV_FLAG_RMSNORM) ? gemv::kFlagRmsNorm : 0;
     p.rms_eps = eps;
     p.mcast = 1;
+    // The bulk prefetch of W reads only from this GPU's memory.
+    for (int i = 0; l.l2pf && i < nsegs; ++i)
+        if (!on_current_device(segs[i].Wq)) l.l2pf = 0;
+    p.l2pf = l.l2pf;
     p.wc = g_write_count;
     out->p = p;
     out->l = l;
@@ -517,6 +525,7 @@ void fill_info(const Launch& l, gemv_launch_info* out) {
     out->xpieces = l.xbox ? l.xper : 0;
     out->xboxes_per_piece = l.xbox ? l.xbpp : 0;
     out->persistent = (l.path == gemv::kPathTc && l.tc_persist) ? 1 : 0;
+    out->l2_prefetch = l.l2pf;
 }
 
 }  // namespace
@@ -1069,20 +1078,7 @@ int gemv_fp8_query_launch(int64_t N, int64_t K, int B, int sm_count, gemv_launch
     Launch l;
     int rc = gemv::plan_launch(N, K, B, sm_count, &l, gemv::kWeightFp8);
     if (rc != GEMV_OK) return rc;
-    out->rows_per_cta = l.rows_per_cta;
-    out->row_tiles = l.row_tiles;
-    out->grid = l.grid;
-    out->kslice = l.kslice;
-    out->kchunk = l.kchunk;
-    out->warps_per_cta = gemv::kWarps;
-    out->warps_per_row = l.kw;
-    out->splits = l.splits;
-    out->rows_per_warp = l.rows_per_warp;
-    out->unroll = l.unroll;
-    out->smem_bytes = l.smem_bytes;
-    out->path = l.path;
-    out->xstride = l.xstride;
-    out->nbuf = l.nbuf;
+    fill_info(l, out);
     return GEMV_OK;
 }
 
@@ -1093,20 +1089,7 @@ int gemv_w4_query_launch(int64_t N, int64_t K, int B, int sm_count, gemv_launch_
     Launch l;
     int rc = gemv::plan_launch(N, K, B, sm_count, &l, gemv::kWeightInt4);
     if (rc != GEMV_OK) return rc;
-    out->rows_per_cta = l.rows_per_cta;
-    out->row_tiles = l.row_tiles;
-    out->grid = l.grid;
-    out->kslice = l.kslice;
-    out->kchunk = l.kchunk;
-    out->warps_per_cta = gemv::kWarps;
-    out->warps_per_row = l.kw;
-    out->splits = l.splits;
-    out->rows_per_warp = l.rows_per_warp;
-    out->unroll = l.unroll;
-    out->smem_bytes = l.smem_bytes;
-    out->path = l.path;
-    out->xstride = l.xstride;
-    out->nbuf = l.nbuf;
+    fill_info(l, out);
     return GEMV_OK;
 }
 

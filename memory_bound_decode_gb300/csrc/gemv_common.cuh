@@ -157,6 +157,13 @@ __device__ __forceinline__ void bulk_copy_multicast(void* dst, const void* src, 
                  :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)), "h"(mask) : "memory");
 }
 
+// Ask the L2 for `bytes` (a multiple of 16) of global memory from `src`
+// (16-byte aligned, this GPU's memory) without waiting for them or holding a
+// register: the TMA's bulk prefetch. The later loads of those bytes then hit L2.
+__device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
+}
+
 // Copy `bytes` (a multiple of 16, both addresses 16-byte aligned) from global
 // memory into this CTA's shared memory at `dst`, completing `bytes`
 // transactions on the mbarrier `bar` (the Tensor Memory Accelerator's 1-D copy).

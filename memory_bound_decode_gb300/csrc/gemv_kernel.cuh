@@ -251,6 +251,30 @@ gemv_bf16_kernel(const __grid_constant__ Params p) {
 #pragma unroll
     for (int r = 0; r < RPW; ++r) wp[r] = wrow[r] + ch.c0 + 8 * static_cast<int64_t>(v0);
     issue_batch<RPW, UJ, true>(wv, ok, wp, v0, rg.my_steps, ch.nv, ch.nfull, ch.tail_m);
+    // L2 prefetch, p.l2pf batches ahead of the registers: lane 0 asks for the
+    // bytes of this warp's rows in warp-steps [pf, upto) of its range, so that
+    // the HBM keeps streaming while the warp waits (for the preceding grid, for
+    // x, for its registers) without holding registers for the bytes. Called
+    // just after the batch at warp-step j was issued (wp and v0 still at j;
+    // lane 0's are the warp's first vector).
+    const int ahead = p.l2pf * UJ;
+    int pf = UJ;   // warp-steps of the range loaded or prefetched so far
+    auto prefetch_to = [&](int j, int upto) {
+        if (upto > rg.my_steps) upto = rg.my_steps;
+        if (upto <= pf) return;
+        if (lane == 0) {
+            const int va = v0 + 32 * (pf - j);
+            int vb = v0 + 32 * (upto - j);
+            if (vb > ch.nv) vb = ch.nv;
+            if (vb > va) {
+#pragma unroll
+                for (int r = 0; r < RPW; ++r)
+                    l2_prefetch(wp[r] + 256 * (pf - j), 16u * static_cast<uint32_t>(vb - va));
+            }
+        }
+        pf = upto;
+    };
+    if (ahead) prefetch_to(0, UJ + ahead);
     if (!(p.flags & kFlagNoWait)) pdl_wait_prerequisites();
     if constexpr (mcast) {
         // Every CTA of the cluster has initialised its mbarrier; rank 0 copies
@@ -314,12 +338,14 @@ gemv_bf16_kernel(const __grid_constant__ Params p) {
 #pragma unroll 1
         for (; j + UJ <= rg.my_steps && (v0 - lane) + 32 * UJ <= ch.nfull; j += UJ) {
             issue_batch<RPW, UJ, false>(wv, ok, wp, v0, UJ, ch.nv, ch.nfull, 0);
+            if (ahead) prefetch_to(j, j + UJ + ahead);
             consume_batch<B, RPW, UJ, false>(acc, wv, ok, xl, xstride);
             advance();
         }
 #pragma unroll 1
         for (; j < rg.my_steps; j += UJ) {
             issue_batch<RPW, UJ, true>(wv, ok, wp, v0, rg.my_steps - j, ch.nv, ch.nfull, ch.tail_m);
+            if (ahead) prefetch_to(j, j + UJ + ahead);
             consume_batch<B, RPW, UJ, true>(acc, wv, ok, xl, xstride);
             advance();
         }
@@ -334,6 +360,8 @@ gemv_bf16_kernel(const __grid_constant__ Params p) {
 #pragma unroll
         for (int r = 0; r < RPW; ++r) wp[r] = wrow[r] + ch.c0 + 8 * static_cast<int64_t>(v0);
         issue_batch<RPW, UJ, true>(wv, ok, wp, v0, rg.my_steps, ch.nv, ch.nfull, ch.tail_m);
+        pf = UJ;
+        if (ahead) prefetch_to(0, UJ + ahead);
         __syncthreads();
     }
 

@@ -76,7 +76,7 @@ __device__ __forceinline__ W4Range w4_range(int ngroups, int kw, int kq) {
 // Launch bounds: 3 CTAs per SM for the standard one-block instance, 2 for
 // the others (the occupancy the planner assumes for each).
 template <int NB, int UJ, bool CHUNKED>
-__global__ void __launch_bounds__(kThreads, NB == 2 ? 2 : 0)
+__global__ void __launch_bounds__(kThreads, NB == 2 ? 2 : (UJ == kW4Unroll && !CHUNKED) ? 3 : 0)
 gemv_w4_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
 
@@ -144,6 +144,13 @@ gemv_w4_kernel(const __grid_constant__ Params p) {
     uint4 qa[UJ], qb[UJ];
     uint16_t sa[UJ], sb[UJ];
     int rg_begin = 0;   // first group of this warp's range in the current chunk
+    // L2 prefetch, p.l2pf batches ahead of the registers: with each batch the
+    // lanes with t == 0 (whose slices start their rows' groups) ask for their
+    // two rows' bytes of groups [pf, jr + UJ + ahead) of the warp's range (64
+    // bytes per group and row, contiguous), so that the HBM keeps streaming
+    // while the warp waits, without registers held for the bytes.
+    const int ahead = p.l2pf * UJ;
+    int pf = 0;   // groups of the range loaded or prefetched so far
 
     // Issue the slots of groups jr .. jr+UJ-1 of this warp's range (chunk at c0).
     // A full batch addresses its slots by immediate offsets; the last, partial
@@ -156,6 +163,16 @@ gemv_w4_kernel(const __grid_constant__ Params p) {
         const uint8_t* a1 = q1p + (col0 >> 1);
         const uint16_t* z0 = s0p + (col0 >> 7);
         const uint16_t* z1 = s1p + (col0 >> 7);
+        if (ahead) {
+            const int upto = rem < UJ + ahead ? my : jr + UJ + ahead;
+            const int from = pf > jr + UJ ? pf : jr + UJ;
+            if (t == 0 && upto > from) {
+                const uint32_t bytes = 64u * static_cast<uint32_t>(upto - from);
+                l2_prefetch(a0 + 64 * (from - jr), bytes);
+                l2_prefetch(a1 + 64 * (from - jr), bytes);
+            }
+            pf = upto > from ? upto : from;
+        }
         if (rem >= UJ) {
 #pragma unroll
             for (int u = 0; u < UJ; ++u) {
@@ -254,6 +271,7 @@ gemv_w4_kernel(const __grid_constant__ Params p) {
         ngroups = (ch.nv + 15) >> 4;
         rg = w4_range(ngroups, kw, kq);
         rg_begin = rg.j_begin;
+        pf = 0;
         issue(ch.c0, 0, rg.my_groups);
         __syncthreads();
     }

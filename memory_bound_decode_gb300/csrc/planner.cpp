@@ -38,7 +38,9 @@
 //                               the call allows it; GEMV_FORCE_SPLIT's CTA count
 //                               applies to it, its warp count must be 1),
 //                               tcstages=<2..10> and tccols=<64|128> (its ring
-//                               depth and stage width, where an instance exists).
+//                               depth and stage width, where an instance exists),
+//                               l2pf=<0..4> (CUDA-core and INT4 kernels: W
+//                               batches each warp prefetches into L2 ahead).
 // A value the planner cannot use makes every plan fail with GEMV_ERR_INVALID,
 // so that a mistyped sweep stops instead of timing the default.
 #include <cstdint>
@@ -63,6 +65,7 @@ struct Overrides {
     int tc = -1;               // -1: the rules decide
     int tcstages = 0;          // 0: kTcStages
     int tccols = 0;            // 0: kTcStageCols
+    int l2pf = -1;             // -1: the rules decide
     bool bad = false;
 };
 
@@ -118,6 +121,8 @@ Overrides read_overrides() {
                 o.tcstages = static_cast<int>(v);
             } else if (num && klen == 6 && std::strncmp(p, "tccols", 6) == 0 && (v == 64 || v == 128)) {
                 o.tccols = static_cast<int>(v);
+            } else if (num && klen == 4 && std::strncmp(p, "l2pf", 4) == 0 && v >= 0 && v <= 4) {
+                o.l2pf = static_cast<int>(v);
             } else {
                 o.bad = true;
                 break;
@@ -192,6 +197,7 @@ int plan_tc(int64_t N, int64_t K, int B, int sm_count, Launch* out, const Overri
         out->smem_rows = out->smem_bytes;
         out->tc_persist = 1;
         out->tc_slots = static_cast<int32_t>(slots);
+        out->l2pf = 0;
         return GEMV_OK;
     }
     // A cluster must fit in one GPC: with clusters of 4 or 8 CTAs fewer CTAs
@@ -221,6 +227,7 @@ int plan_tc(int64_t N, int64_t K, int B, int sm_count, Launch* out, const Overri
     out->stage_cols = cols;
     out->tc_persist = 0;
     out->tc_slots = 0;
+    out->l2pf = 0;
     out->smem_bytes = static_cast<int32_t>(smem);
     out->path = kPathTc;
     out->xstride = 0;
@@ -467,6 +474,16 @@ int plan_with(int64_t N, int64_t K, int B, int sm_count, Launch* out, int weight
     out->stage_cols = 0;
     out->tc_persist = 0;
     out->tc_slots = 0;
+    // L2 prefetch one batch ahead (Params::l2pf) for batch 1 on the CUDA cores
+    // in a single launch whose grid is at most two waves of 4 CTAs per SM.
+    // Measured (us per call, graph-replayed chains, without / with): QKV
+    // 9.65 / 9.48, o_proj 5.68 / 5.56, down_proj 18.14 / 17.88, k_proj 2.66 /
+    // 2.64; two or four batches ahead gained no more (down_proj 18.35, 20.33);
+    // a grid of many waves lost (gate/up, 3,584 CTAs: 33.26 / 35.32), and so
+    // did the INT4 kernel (down_proj 11.13 / 11.23).
+    constexpr int64_t kPrefetchMaxCtasPerSm = 8;
+    const int pf_rule = (path == kPathFma && B == 1 && !overlap && grid <= kPrefetchMaxCtasPerSm * sm_count) ? 1 : 0;
+    out->l2pf = (path == kPathFma || path == kPathW4) ? (ov.l2pf >= 0 ? ov.l2pf : pf_rule) : 0;
     // BF16 tensor-core path with more than 8 rows of x (the largest slices) in
     // a grid of one wave (every CTA waits for its x at the same moment, with
     // the HBM idle), x in one chunk and K a multiple of 32 (whole blocks, so

@@ -388,8 +388,23 @@ def test_force_variant(L, monkeypatch):
     monkeypatch.setenv("GEMV_FORCE_VARIANT", "tc=0,xpieces=2")
     q = binding.gemv_query_launch(4096, 14336, 16, GB300_SMS)
     assert (q["xbox"], q["xpieces"], q["xboxes_per_piece"]) == (1, 2, 4)
+    # L2 prefetch ahead of the register batch: batch 1 on the CUDA cores in
+    # grids of at most 8 CTAs per SM by default, any depth on request (also INT4)
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", "")
+    for (N, K), pf in [((4096, 14336), 1), ((6144, 4096), 1), ((4096, 4096), 1), ((1024, 4096), 1),
+                       ((28672, 4096), 0), ((128256, 4096), 0)]:
+        assert binding.gemv_query_launch(N, K, 1, GB300_SMS)["l2_prefetch"] == pf, (N, K)
+    assert binding.gemv_query_launch(4096, 14336, 2, GB300_SMS)["l2_prefetch"] == 0
+    assert binding.gemv_w4_query_launch(4096, 14336, 1, GB300_SMS)["l2_prefetch"] == 0
+    assert binding.gemv_fp8_query_launch(4096, 14336, 1, GB300_SMS)["l2_prefetch"] == 0
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", "l2pf=3")
+    assert binding.gemv_query_launch(28672, 4096, 1, GB300_SMS)["l2_prefetch"] == 3
+    assert binding.gemv_w4_query_launch(4096, 14336, 1, GB300_SMS)["l2_prefetch"] == 3
+    assert binding.gemv_query_launch(4096, 14336, 16, GB300_SMS)["l2_prefetch"] == 0   # tcgen05: none
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", "l2pf=0")
+    assert binding.gemv_query_launch(4096, 14336, 1, GB300_SMS)["l2_prefetch"] == 0
     for bad in ["mcast=3", "unroll=2", "streamk=2", "foo=1", "mcast", "mcast=", "mcast=2,,x=1", "xbox=3",
-                "xpieces=0", "xpieces=9", "tc=2", "tcstages=1", "tcstages=11", "tccols=96"]:
+                "xpieces=0", "xpieces=9", "tc=2", "tcstages=1", "tcstages=11", "tccols=96", "l2pf=5", "l2pf=-1"]:
         monkeypatch.setenv("GEMV_FORCE_VARIANT", bad)
         info = binding.gemv_launch_info()
         assert L.gemv_query_launch(4096, 14336, 1, GB300_SMS, ctypes.byref(info)) == binding.GEMV_ERR_INVALID, bad
