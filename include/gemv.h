@@ -373,9 +373,10 @@ typedef struct {
     int32_t l2_prefetch;     /* paths 0 and 2: batches of W (unroll loads per
                                 lane each) that every warp asks the L2 for ahead
                                 of the batch in its registers, by the Tensor
-                                Memory Accelerator's bulk prefetch; 0: none. A
-                                call with W outside this GPU's memory falls back
-                                to 0                                              */
+                                Memory Accelerator's bulk prefetch; path 5 (one
+                                wave): ring stages of W prefetched beyond the
+                                ring; 0: none. A call with W outside this GPU's
+                                memory falls back to 0                            */
 } gemv_launch_info;
 
 int gemv_query_launch(int64_t N, int64_t K, int B, int sm_count,

@@ -57,7 +57,9 @@ struct Params {
     int32_t xbpp;     // ... and boxes of 8 blocks (256 columns) per piece
     int32_t xwide;    // ... 1: boxes of 256 columns x B rows, 0: of 32 columns x B rows (stage_x_boxes)
     int32_t l2pf;     // CUDA-core and INT4 kernels: batches of W each warp asks the L2 for ahead of
-                      // the batch in its registers (bulk prefetch; W in this GPU's memory); 0: none
+                      // the batch in its registers (bulk prefetch); tcgen05 kernel (one wave): ring
+                      // stages of W prefetched beyond the ring (tensor prefetch); W in this GPU's
+                      // memory; 0: none
     WriteCount wc;
     CUtensorMap xmap; // ... and the 3-D view of x the boxes are copied through (stage_x_boxes);
                       // path 5: x as [B][K] in boxes of 64 columns x 16 rows
@@ -175,7 +177,7 @@ struct Launch {
     int32_t stage_cols;// path 5: columns per ring stage (64 or 128); the ring depth is in `unroll`
     int32_t tc_persist;// path 5: the persistent form (a fixed grid taking row tiles in turn, no K split)
     int32_t tc_slots;  // ... CTAs resident at once (the grid takes equal shares of the tiles within them)
-    int32_t l2pf;      // CUDA-core and INT4 paths: W batches prefetched into L2 ahead (Params::l2pf)
+    int32_t l2pf;      // W prefetched into L2 ahead (Params::l2pf)
 };
 
 // Sweep knob of the planner (GEMV_FORCE_VARIANT planwait=1): every launch of

@@ -77,6 +77,13 @@ __device__ __forceinline__ void tensor_copy_2d(uint32_t dst, const void* map, in
                  :: "r"(dst), "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar)) : "memory");
 }
 
+// Ask the L2 for the box at (x, y) of `map` (no shared memory, no barrier):
+// the later copy of the same box then reads it from L2.
+__device__ __forceinline__ void tensor_prefetch_2d(const void* map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 :: "l"(map), "r"(x), "r"(y) : "memory");
+}
+
 // 32 lanes x 16 columns of FP32 from tensor memory (lane i of the warp gets
 // lane taddr.lane + i), then the wait for the load.
 __device__ __forceinline__ void tc_load16(uint32_t taddr, float (&v)[16]) {
@@ -195,12 +202,21 @@ gemv_tc_kernel(const __grid_constant__ Params p) {
             for (int b = 0; b < SC / 64; ++b)
                 tensor_copy_2d(x + static_cast<uint32_t>(b) * kTcXBox, &p.xmap, col + 64 * b, 0, full + slot);
         };
+        // L2 prefetch of W, p.l2pf stages beyond the ring: more bytes in flight
+        // than the ring's shared memory holds.
+        auto prefetch_w = [&](int s) {
+            if (s >= nst) return;
+            const int col = static_cast<int>(k0) + s * SC;
+#pragma unroll
+            for (int b = 0; b < SC / 64; ++b) tensor_prefetch_2d(wmap, col + 64 * b, row0);
+        };
         const int npro = nst < NS ? nst : NS;
         for (int s = 0; s < npro; ++s) {
             mbar_arrive_expect_tx(full + s, stage_bytes);
             ++arms[s];
             issue_w(s);
         }
+        for (int s = npro; s < npro + p.l2pf; ++s) prefetch_w(s);
         if (!(p.flags & kFlagNoWait)) pdl_wait_prerequisites();
         for (int s = 0; s < npro; ++s) issue_x(s);
         for (int s = npro; s < nst; ++s) {
@@ -213,6 +229,7 @@ gemv_tc_kernel(const __grid_constant__ Params p) {
             ++arms[slot];
             issue_w(s);
             issue_x(s);
+            if (p.l2pf) prefetch_w(s + p.l2pf);
         }
         // Every copy issued has landed before the CTA may leave (bounded; on the
         // normal path the MMA issuer has already seen each of these phases).

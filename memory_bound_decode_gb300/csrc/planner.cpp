@@ -39,8 +39,9 @@
 //                               applies to it, its warp count must be 1),
 //                               tcstages=<2..10> and tccols=<64|128> (its ring
 //                               depth and stage width, where an instance exists),
-//                               l2pf=<0..4> (CUDA-core and INT4 kernels: W
-//                               batches each warp prefetches into L2 ahead).
+//                               l2pf=<0..4> (CUDA-core, INT4 and one-wave
+//                               tcgen05 kernels: W batches or ring stages
+//                               prefetched into L2 ahead).
 // A value the planner cannot use makes every plan fail with GEMV_ERR_INVALID,
 // so that a mistyped sweep stops instead of timing the default.
 #include <cstdint>
@@ -227,7 +228,7 @@ int plan_tc(int64_t N, int64_t K, int B, int sm_count, Launch* out, const Overri
     out->stage_cols = cols;
     out->tc_persist = 0;
     out->tc_slots = 0;
-    out->l2pf = 0;
+    out->l2pf = ov.l2pf >= 0 ? ov.l2pf : 0;
     out->smem_bytes = static_cast<int32_t>(smem);
     out->path = kPathTc;
     out->xstride = 0;

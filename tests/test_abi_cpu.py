@@ -400,7 +400,8 @@ def test_force_variant(L, monkeypatch):
     monkeypatch.setenv("GEMV_FORCE_VARIANT", "l2pf=3")
     assert binding.gemv_query_launch(28672, 4096, 1, GB300_SMS)["l2_prefetch"] == 3
     assert binding.gemv_w4_query_launch(4096, 14336, 1, GB300_SMS)["l2_prefetch"] == 3
-    assert binding.gemv_query_launch(4096, 14336, 16, GB300_SMS)["l2_prefetch"] == 0   # tcgen05: none
+    assert binding.gemv_query_launch(4096, 14336, 16, GB300_SMS)["l2_prefetch"] == 3   # tcgen05, one wave
+    assert binding.gemv_query_launch(128256, 4096, 16, GB300_SMS)["l2_prefetch"] == 0  # its persistent form
     monkeypatch.setenv("GEMV_FORCE_VARIANT", "l2pf=0")
     assert binding.gemv_query_launch(4096, 14336, 1, GB300_SMS)["l2_prefetch"] == 0
     for bad in ["mcast=3", "unroll=2", "streamk=2", "foo=1", "mcast", "mcast=", "mcast=2,,x=1", "xbox=3",

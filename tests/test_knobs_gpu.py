@@ -22,6 +22,8 @@ def _sms():
     {"GEMV_FORCE_SPLIT": "1x8"}, {"GEMV_FORCE_VARIANT": "mcast=1"}, {"GEMV_FORCE_VARIANT": "mcast=4"},
     {"GEMV_FORCE_VARIANT": "mcast=8"}, {"GEMV_FORCE_VARIANT": "streamk=1"},
     {"GEMV_FORCE_SPLIT": "4x1", "GEMV_FORCE_VARIANT": "mcast=2"},
+    {"GEMV_FORCE_VARIANT": "l2pf=0"}, {"GEMV_FORCE_VARIANT": "l2pf=4"},
+    {"GEMV_FORCE_SPLIT": "2x2", "GEMV_FORCE_VARIANT": "l2pf=2"},
 ])
 @pytest.mark.parametrize("N,K,B", [(4096, 14336, 1), (4097, 8200, 1), (1000, 4096, 3), (300, 12288, 16)])
 def test_forced_bf16_launches(monkeypatch, knobs, N, K, B):
@@ -37,7 +39,8 @@ def test_forced_bf16_launches(monkeypatch, knobs, N, K, B):
 
 
 @pytest.mark.parametrize("knobs", [{"GEMV_FORCE_SPLIT": "1x1"}, {"GEMV_FORCE_SPLIT": "4x2"},
-                                   {"GEMV_FORCE_VARIANT": "unroll=4"}, {"GEMV_FORCE_VARIANT": "unroll=8"}])
+                                   {"GEMV_FORCE_VARIANT": "unroll=4"}, {"GEMV_FORCE_VARIANT": "unroll=8"},
+                                   {"GEMV_FORCE_VARIANT": "l2pf=4"}, {"GEMV_FORCE_VARIANT": "unroll=8,l2pf=1"}])
 @pytest.mark.parametrize("kind", ["w4", "fp8"])
 @pytest.mark.parametrize("N,K,B", [(4096, 14336, 1), (1000, 4096, 4)])
 def test_forced_quantised_launches(monkeypatch, knobs, kind, N, K, B):
