@@ -376,7 +376,9 @@ typedef struct {
                                 Memory Accelerator's bulk prefetch; path 5 (one
                                 wave): ring stages of W prefetched beyond the
                                 ring; 0: none. A call with W outside this GPU's
-                                memory falls back to 0                            */
+                                memory falls back to 0, and the launches of a
+                                plan (gemv_plan_create) take 0 unless the
+                                GEMV_FORCE_VARIANT sweep knob sets l2pf           */
 } gemv_launch_info;
 
 int gemv_query_launch(int64_t N, int64_t K, int B, int sm_count,

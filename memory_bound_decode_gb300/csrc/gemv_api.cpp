@@ -19,6 +19,12 @@
 using gemv::Launch;
 using gemv::Params;
 
+namespace gemv {
+// Whether the sweep knob GEMV_FORCE_VARIANT l2pf=<n> is set (planner.cpp):
+// plans then keep the planner's L2 prefetch depth instead of turning it off.
+bool l2pf_forced();
+}  // namespace gemv
+
 namespace {
 
 thread_local int g_last_cuda_error = 0;
@@ -793,6 +799,14 @@ int gemv_plan_create(const gemv_proj* projs, int nproj, gemv_plan** out) {
                                       j - i, a.x, a.K, a.B, a.flags, eps, sm_count, &pr, overlap);
                 }
                 if (r != GEMV_OK) return r;
+                // The L2 prefetch rule was measured on chains of the same call; among
+                // a plan's differing neighbours it cost time (the decode step with
+                // every wait kept: 2.298 -> 2.325 ms), so plans leave it off unless
+                // the sweep knob sets it.
+                if (!gemv::l2pf_forced()) {
+                    pr.p.l2pf = 0;
+                    pr.l.l2pf = 0;
+                }
                 plan->launches.push_back(pr);
             }
             return GEMV_OK;

@@ -580,6 +580,11 @@ bool plan_force_wait() {
     return !ov.bad && ov.planwait == 1;
 }
 
+bool l2pf_forced() {
+    const Overrides ov = read_overrides();
+    return !ov.bad && ov.l2pf >= 0;
+}
+
 // The default grid measured faster than the stream-K grid on every decode
 // shape (batch 1, 2,000 calls each), so the rules never pick it; the sweep
 // knob streamk=1 does, for batch-1 shapes the stream-K kernel takes.
