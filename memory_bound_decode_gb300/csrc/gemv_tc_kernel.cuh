@@ -505,7 +505,7 @@ gemv_tcp_kernel(const __grid_constant__ Params p) {
 
 // Instances by ring depth and stage width (Launch::unroll, Launch::stage_cols):
 // rings of up to 256 columns leave room for two CTAs per SM, deeper ones take one.
-#define GEMV_TC_INSTANCES(X) X(2, 128) X(3, 128) X(4, 128) X(5, 128) X(4, 64) X(8, 64) X(10, 64)
+#define GEMV_TC_INSTANCES(X) X(2, 128) X(3, 128) X(4, 128) X(5, 128) X(2, 64) X(3, 64) X(4, 64) X(8, 64) X(10, 64)
 
 // Persistent-form instances (ring depth, stage width).
 #define GEMV_TCP_INSTANCES(X) X(2, 128) X(3, 128) X(4, 128)
@@ -542,12 +542,11 @@ inline cudaError_t prepare_tc() {
     return e;
 }
 
-__host__ __device__ constexpr bool tcp_instance(int ns, int sc) { return sc == 128 && ns >= 2 && ns <= 4; }
-
-// Whether an instance of this depth and width exists.
-__host__ __device__ constexpr bool tc_instance(int ns, int sc) {
-    return (sc == 128 && ns >= 2 && ns <= 5) || (sc == 64 && (ns == 4 || ns == 8 || ns == 10));
-}
+// Whether an instance of this depth and width exists (read off the lists above).
+#define GEMV_TC_IS(n, c) (ns == (n) && sc == (c)) ||
+__host__ __device__ constexpr bool tcp_instance(int ns, int sc) { return GEMV_TCP_INSTANCES(GEMV_TC_IS) false; }
+__host__ __device__ constexpr bool tc_instance(int ns, int sc) { return GEMV_TC_INSTANCES(GEMV_TC_IS) false; }
+#undef GEMV_TC_IS
 
 inline cudaError_t read_tc_status_tu(unsigned int* bits, bool reset) {
     cudaError_t e = cudaMemcpyFromSymbol(bits, g_device_status, sizeof(unsigned int));

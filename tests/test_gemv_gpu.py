@@ -74,7 +74,7 @@ def test_parity_skinny_batch(N, K, B):
     gu.assert_parity(y, y_ref, s, f"B={B}")
 
 
-@pytest.mark.parametrize("B", [2, 3, 4, 8, 16])
+@pytest.mark.parametrize("B", [2, 3, 4, 8, 9, 12, 16])
 @pytest.mark.parametrize("N,K", [(4096, 14336), (1000, 4096), (33, 65537)])
 def test_tensor_core_wide_dynamic_range(N, K, B):
     """The batch 2..16 path runs on the tensor cores, whose internal addition

@@ -18,8 +18,8 @@ def _sms():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
-@pytest.mark.parametrize("stages", ["2", "3", "4", "5", "4,tccols=64", "8,tccols=64", "10,tccols=64", "2,l2pf=2",
-                                    "4,tccols=64,l2pf=4"])
+@pytest.mark.parametrize("stages", ["2", "3", "4", "5", "2,tccols=64", "3,tccols=64", "4,tccols=64", "8,tccols=64",
+                                    "10,tccols=64", "2,l2pf=2", "4,tccols=64,l2pf=4"])
 @pytest.mark.parametrize("N,K,B", [
     (4096, 14336, 16), (4096, 14336, 2), (4096, 4096, 16), (6144, 4096, 16), (1024, 4096, 8),
     (4097, 4104, 9), (333, 8192, 13), (64, 65536, 16), (129, 136, 3), (7, 8, 2), (2000, 12288, 5),
