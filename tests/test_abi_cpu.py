@@ -411,6 +411,21 @@ def test_force_variant(L, monkeypatch):
         assert L.gemv_query_launch(4096, 14336, 1, GB300_SMS, ctypes.byref(info)) == binding.GEMV_ERR_INVALID, bad
 
 
+@pytest.mark.parametrize("stages,cols,exists", [
+    (2, 128, True), (3, 128, True), (4, 128, True), (5, 128, True), (2, 64, True), (3, 64, True),
+    (4, 64, True), (8, 64, True), (10, 64, True), (6, 128, False), (5, 64, False), (9, 64, False)])
+def test_tc_ring_instances(monkeypatch, stages, cols, exists):
+    """Every ring the tcgen05 knobs name is planned where an instance of it is
+    compiled (one wave: the stage count comes back as `unroll`); a ring with
+    no instance leaves the call to the register-fed kernel."""
+    monkeypatch.setenv("GEMV_FORCE_VARIANT", f"tc=1,tcstages={stages},tccols={cols}")
+    q = binding.gemv_query_launch(4096, 14336, 16, GB300_SMS)
+    if exists:
+        assert (q["path"], q["unroll"], q["persistent"]) == (5, stages, 0), q
+    else:
+        assert q["path"] == 1, q
+
+
 def test_host_io_calls_reject_before_any_copy(L):
     """The host-to-host entry points validate their arguments before touching
     the device (checked here without a GPU)."""
