@@ -130,7 +130,10 @@ def test_plan_covers_the_problem(L, N, K, B):
         assert q["splits"] in (1, 2, 4, 8) and q["kslice"] % 128 == 0
         assert q["splits"] * q["kslice"] >= K > (q["splits"] - 1) * q["kslice"]
         assert q["smem_bytes"] <= 227 * 1024
+        assert q["l2_prefetch"] == 0
         return
+    # L2 prefetch one batch ahead: batch 1 on the CUDA cores in grids of at most 8 CTAs per SM
+    assert q["l2_prefetch"] == (1 if B == 1 and q["grid"] <= 8 * GB300_SMS else 0)
     # batch 1 on the CUDA cores, batches 2..16 on the BF16 tensor cores (16-row tiles)
     assert q["path"] == (0 if B == 1 else 1)
     assert q["rows_per_warp"] == (1 if B == 1 else 16)
